@@ -1,0 +1,354 @@
+/*
+ * us_oracle.c -- plain, slow CPU oracle for bitmap-encoded unstructured-sparse
+ * weight matrices and for Y = W.X on them.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library's product path may link,
+ * load or call this file: only the test-suite, the smoke check and the CPU
+ * baseline leg of the benchmark use it.  It shares no code, header, table or
+ * helper with the CUDA library.
+ *
+ * Sources (each function below names the passage it restates):
+ *  [UnionSparse]  "UnionSparse: An Index-Efficient Sparsity Framework for
+ *                 Low-Bit Sparse LLM Inference on Edge", section V-A
+ *                 "IE-BME Representation" (Union Bitmaps, Union Value Offsets,
+ *                 Compressed Values, Fig. 7) with Q = RA*CA = 1, and Fig. 2
+ *                 (INT4 operands, INT32 result, dequantisation to FP16).
+ *  [SPDP]         "Unified Static-Dynamic Pruning for Efficient LLM
+ *                 Inference", section 4.1 "Tiled-CBC" (column tiles, values
+ *                 in tile-column order, 4-byte TileOffset) and section 4.2.3
+ *                 (16-byte value padding), section 2 (static mask W (.) M,
+ *                 dynamic mask W (.) M(x)).
+ *
+ * Readings taken where the pages leave a step open (all are listed in the
+ * design notes of the repository):
+ *  - Tiles are TM x TK, numbered t = tm*nTK + tk (row-band major, like the
+ *    row-major GTile order of [SPDP] 4.1).
+ *  - Scan order inside a tile: ROW  p = i*TK + j  ([UnionSparse] "scanned in
+ *    row-major order"), COL  p = j*TM + i  ([SPDP] column-major tiles).
+ *  - Bit p%64 of 64-bit word p/64 of the tile; the earlier position is the
+ *    less significant bit ([UnionSparse] "leftmost bit ... LSB").
+ *  - Presence: a bit is set iff the stored weight is nonzero.  For fp16 both
+ *    +0 and -0 count as zero; NaN counts as nonzero.
+ *  - Values of tile t start at element tile_off[t], in increasing p; each
+ *    tile's run is zero-padded to 16 bytes (8 fp16 or 32 int4 elements);
+ *    tile_off[t+1] = tile_off[t] + roundup(P_t, E16) (in elements, uint32).
+ *  - int4: element e lives in byte e>>1, even e in the low nibble, two's
+ *    complement in [-8, 7].
+ *  - W4A4 result: int32 acc = sum_k Wq*Xq; Y = fp16_rn((fp32(acc)*s_w)*s_x),
+ *    two fp32 roundings then one round-to-nearest-even to fp16.
+ *  - fp16 result: fp16_rn of the fp64 sum over increasing k.
+ *  - spMspV: column k takes part iff |x_k| > tau.
+ *
+ * Built with  gcc -O2 -ffp-contract=off -fopenmp  (scalar loops only; the
+ * OpenMP pragmas split independent output rows and never change the order
+ * of any sum).
+ */
+#include <stdint.h>
+#include <stddef.h>
+#include <string.h>
+#include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_OK = 0, OR_BAD_ARG = 1, OR_TOO_LARGE = 3, OR_CAPACITY = 4, OR_CORRUPT = 7 };
+enum { OR_F16 = 0, OR_I4 = 1 };
+enum { OR_ROW = 0, OR_COL = 1 };
+
+/* ---------------------------------------------------------------- fp16 ---- */
+/* IEEE-754 binary16 <-> binary32/64 through the compiler's _Float16 type
+ * (exact widening; narrowing is one round-to-nearest-even). */
+float or_half_to_float(uint16_t h) {
+    _Float16 v;
+    memcpy(&v, &h, 2);
+    return (float)v;
+}
+uint16_t or_float_to_half(float f) {
+    _Float16 v = (_Float16)f;
+    uint16_t h;
+    memcpy(&h, &v, 2);
+    return h;
+}
+uint16_t or_double_to_half(double d) {
+    _Float16 v = (_Float16)d;
+    uint16_t h;
+    memcpy(&h, &v, 2);
+    return h;
+}
+
+/* ------------------------------------------------------------- format ---- */
+static int elem_bits(int elem) { return elem == OR_F16 ? 16 : 4; }
+/* elements per 16-byte padding quantum */
+static int elems_per_16B(int elem) { return elem == OR_F16 ? 8 : 32; }
+
+static int check_shape(int M, int K, int TM, int TK, int elem, int order) {
+    if (M <= 0 || K <= 0 || TM <= 0 || TK <= 0) return OR_BAD_ARG;
+    if (M % TM || K % TK) return OR_BAD_ARG;
+    if (((int64_t)TM * TK) % 64) return OR_BAD_ARG;
+    if (elem != OR_F16 && elem != OR_I4) return OR_BAD_ARG;
+    if (order != OR_ROW && order != OR_COL) return OR_BAD_ARG;
+    if ((uint64_t)M * (uint64_t)K >= ((uint64_t)1 << 32)) return OR_TOO_LARGE;
+    return OR_OK;
+}
+
+/* position p inside a TM x TK tile -> (row i, column j) */
+static void pos_to_ij(int order, int TM, int TK, int64_t p, int* i, int* j) {
+    if (order == OR_ROW) { *i = (int)(p / TK); *j = (int)(p % TK); }
+    else                 { *j = (int)(p / TM); *i = (int)(p % TM); }
+}
+
+int or_num_tiles(int M, int K, int TM, int TK, int64_t* nT) {
+    int rc = check_shape(M, K, TM, TK, OR_F16, OR_ROW);
+    if (rc) return rc;
+    *nT = (int64_t)(M / TM) * (K / TK);
+    return OR_OK;
+}
+
+/* read element (r, c) of the dense matrix as "is it nonzero" and as a code */
+static int dense_nonzero(const void* W, int64_t ldw, int elem, int r, int c) {
+    if (elem == OR_F16) {
+        uint16_t h = ((const uint16_t*)W)[(int64_t)r * ldw + c];
+        return (h & 0x7FFFu) != 0;           /* +0 and -0 are zero */
+    }
+    return ((const int8_t*)W)[(int64_t)r * ldw + c] != 0;
+}
+
+static void put_value(uint8_t* values, int elem, uint64_t e, const void* W, int64_t ldw, int r, int c) {
+    if (elem == OR_F16) {
+        uint16_t h = ((const uint16_t*)W)[(int64_t)r * ldw + c];
+        values[2 * e] = (uint8_t)(h & 0xFF);
+        values[2 * e + 1] = (uint8_t)(h >> 8);
+    } else {
+        int8_t q = ((const int8_t*)W)[(int64_t)r * ldw + c];
+        uint8_t nib = (uint8_t)q & 0x0F;
+        if (e & 1) values[e >> 1] = (uint8_t)((values[e >> 1] & 0x0F) | (nib << 4));
+        else       values[e >> 1] = (uint8_t)((values[e >> 1] & 0xF0) | nib);
+    }
+}
+
+/*
+ * Encode a dense matrix into bitmap tiles.
+ * [UnionSparse] V-A: the mask of tile t is scanned in the tile's scan order
+ * and packed into 64-bit words (earlier position = less significant bit);
+ * the compact rank of a set position is the number of set positions before
+ * it; value with rank rho of tile t sits at CV[o_t + rho]; o_t is the prefix
+ * sum of the preceding tiles' payload lengths (Q = 1).  [SPDP] 4.2.3: each
+ * tile's payload is padded to 16 bytes.
+ * W: fp16 bit patterns (elem F16) or int8 codes in [-8,7] (elem I4),
+ * row-major with leading dimension ldw.
+ * Outputs: bitmap (nT*TM*TK/64 words), tile_off (nT+1 entries),
+ * values (capacity values_cap bytes; used bytes returned).
+ */
+int or_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem, int order,
+              uint64_t* bitmap, uint32_t* tile_off, uint8_t* values, uint64_t values_cap,
+              uint64_t* values_used) {
+    int rc = check_shape(M, K, TM, TK, elem, order);
+    if (rc) return rc;
+    if (ldw < K) return OR_BAD_ARG;
+    const int nTM = M / TM, nTK = K / TK;
+    const int64_t tile_pos = (int64_t)TM * TK;
+    const int64_t words_per_tile = tile_pos / 64;
+    const int E = elems_per_16B(elem);
+    if (elem == OR_I4) {
+        for (int r = 0; r < M; ++r)
+            for (int c = 0; c < K; ++c) {
+                int8_t q = ((const int8_t*)W)[(int64_t)r * ldw + c];
+                if (q < -8 || q > 7) return OR_BAD_ARG;
+            }
+    }
+    uint64_t off = 0;                      /* in elements */
+    tile_off[0] = 0;
+    for (int tm = 0; tm < nTM; ++tm) {
+        for (int tk = 0; tk < nTK; ++tk) {
+            const int64_t t = (int64_t)tm * nTK + tk;
+            uint64_t* words = bitmap + t * words_per_tile;
+            for (int64_t w = 0; w < words_per_tile; ++w) words[w] = 0;
+            uint64_t P = 0;                /* active entries of this tile */
+            for (int64_t p = 0; p < tile_pos; ++p) {
+                int i, j;
+                pos_to_ij(order, TM, TK, p, &i, &j);
+                const int r = tm * TM + i, c = tk * TK + j;
+                if (!dense_nonzero(W, ldw, elem, r, c)) continue;
+                words[p / 64] |= (uint64_t)1 << (p % 64);
+                const uint64_t e = off + P;               /* o_t + rho */
+                if ((e + 1) * elem_bits(elem) > values_cap * 8) return OR_CAPACITY;
+                put_value(values, elem, e, W, ldw, r, c);
+                ++P;
+            }
+            /* zero padding up to the next 16-byte boundary */
+            uint64_t padded = (P + E - 1) / E * E;
+            for (uint64_t e = off + P; e < off + padded; ++e) {
+                if ((e + 1) * elem_bits(elem) > values_cap * 8) return OR_CAPACITY;
+                if (elem == OR_F16) { values[2 * e] = 0; values[2 * e + 1] = 0; }
+                else if (e & 1) values[e >> 1] &= 0x0F;
+                else values[e >> 1] &= 0xF0;
+            }
+            off += padded;
+            if (off >= ((uint64_t)1 << 32)) return OR_TOO_LARGE;
+            tile_off[t + 1] = (uint32_t)off;
+        }
+    }
+    *values_used = off * elem_bits(elem) / 8;
+    return OR_OK;
+}
+
+/* value with element index e of the packed stream, as fp16 bits or int4 code */
+static uint16_t get_f16(const uint8_t* values, uint64_t e) {
+    return (uint16_t)(values[2 * e] | (values[2 * e + 1] << 8));
+}
+static int8_t get_i4(const uint8_t* values, uint64_t e) {
+    uint8_t nib = (e & 1) ? (values[e >> 1] >> 4) : (values[e >> 1] & 0x0F);
+    return (int8_t)(nib >= 8 ? (int)nib - 16 : (int)nib);
+}
+
+/*
+ * Decode (exact inverse of or_encode).  Every set position (i,j) of tile t
+ * takes value CV[o_t + rho_t(i,j)], rho = number of set positions scanned
+ * before it ([UnionSparse] V-A, "Compressed Values"); clear positions are 0.
+ * Checks that each tile's run holds its popcount and lies inside the buffer.
+ */
+int or_decode(const uint64_t* bitmap, const uint32_t* tile_off, const uint8_t* values,
+              uint64_t values_bytes, int M, int K, int TM, int TK, int elem, int order,
+              void* W, int64_t ldw) {
+    int rc = check_shape(M, K, TM, TK, elem, order);
+    if (rc) return rc;
+    const int nTM = M / TM, nTK = K / TK;
+    const int64_t tile_pos = (int64_t)TM * TK;
+    const int64_t words_per_tile = tile_pos / 64;
+    if (tile_off[0] != 0) return OR_CORRUPT;
+    for (int tm = 0; tm < nTM; ++tm) {
+        for (int tk = 0; tk < nTK; ++tk) {
+            const int64_t t = (int64_t)tm * nTK + tk;
+            const uint64_t o_t = tile_off[t], o_next = tile_off[t + 1];
+            if (o_next < o_t) return OR_CORRUPT;
+            if (o_next * elem_bits(elem) > values_bytes * 8) return OR_CORRUPT;
+            const uint64_t* words = bitmap + t * words_per_tile;
+            uint64_t rho = 0;
+            for (int64_t p = 0; p < tile_pos; ++p) {
+                int i, j;
+                pos_to_ij(order, TM, TK, p, &i, &j);
+                const int64_t idx = (int64_t)(tm * TM + i) * ldw + (tk * TK + j);
+                const int set = (int)((words[p / 64] >> (p % 64)) & 1u);
+                if (set) {
+                    if (o_t + rho >= o_next) return OR_CORRUPT;
+                    if (elem == OR_F16) ((uint16_t*)W)[idx] = get_f16(values, o_t + rho);
+                    else ((int8_t*)W)[idx] = get_i4(values, o_t + rho);
+                    ++rho;
+                } else {
+                    if (elem == OR_F16) ((uint16_t*)W)[idx] = 0;
+                    else ((int8_t*)W)[idx] = 0;
+                }
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* int4 codes packed two per byte (even index in the low nibble) -> int8 */
+void or_unpack_int4(const uint8_t* packed, int64_t n, int8_t* out) {
+    for (int64_t e = 0; e < n; ++e) out[e] = get_i4(packed, (uint64_t)e);
+}
+
+/* ----------------------------------------------------------- multiply ---- */
+/* one W4A4 output: int32 accumulation over increasing k, then dequantise
+ * ([UnionSparse] Fig. 2: INT4 x INT4 -> Y INT32 -> Dequant -> FP16). */
+static int32_t w4a4_acc(const int8_t* Wd, const int8_t* Xd, int K, int m, int n) {
+    int64_t acc = 0;
+    for (int k = 0; k < K; ++k)
+        acc += (int64_t)Wd[(int64_t)m * K + k] * (int64_t)Xd[(int64_t)n * K + k];
+    return (int32_t)acc;   /* |acc| <= 64*K < 2^31 for every supported K */
+}
+static uint16_t w4a4_dequant(int32_t acc, uint16_t s_w, uint16_t s_x) {
+    float a = (float)acc;                  /* exact: |acc| < 2^24 */
+    float t = a * or_half_to_float(s_w);   /* fp32 rounding 1 */
+    float u = t * or_half_to_float(s_x);   /* fp32 rounding 2 */
+    return or_float_to_half(u);            /* fp16 rounding */
+}
+
+/* Wd: M x K int8 codes (decoded), Xd: N x K int8 codes (token-major).
+ * Yacc: N x M int32, Y: N x M fp16 bits (may be NULL). */
+int or_spmm_w4a4(const int8_t* Wd, const int8_t* Xd, const uint16_t* s_w, const uint16_t* s_x,
+                 int M, int N, int K, int32_t* Yacc, uint16_t* Y, int nthreads) {
+    if (M <= 0 || N <= 0 || K <= 0) return OR_BAD_ARG;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            int32_t acc = w4a4_acc(Wd, Xd, K, m, n);
+            Yacc[(int64_t)n * M + m] = acc;
+            if (Y) Y[(int64_t)n * M + m] = w4a4_dequant(acc, s_w[m], s_x[n]);
+        }
+    return OR_OK;
+}
+
+/* the same outputs, only at the listed (n, m) pairs */
+int or_spmm_w4a4_at(const int8_t* Wd, const int8_t* Xd, const uint16_t* s_w, const uint16_t* s_x,
+                    int M, int N, int K, const int32_t* n_idx, const int32_t* m_idx, int64_t count,
+                    int32_t* acc_out, uint16_t* y_out) {
+    for (int64_t q = 0; q < count; ++q) {
+        int n = n_idx[q], m = m_idx[q];
+        if (n < 0 || n >= N || m < 0 || m >= M) return OR_BAD_ARG;
+        acc_out[q] = w4a4_acc(Wd, Xd, K, m, n);
+        y_out[q] = w4a4_dequant(acc_out[q], s_w[m], s_x[n]);
+    }
+    return OR_OK;
+}
+
+/* one fp16 output: fp64 sum over increasing k of exact fp16 products */
+static double f16_dot(const uint16_t* Wd, const uint16_t* X, int K, int m, int n, double tau, int skip) {
+    double s = 0.0;
+    for (int k = 0; k < K; ++k) {
+        double x = (double)or_half_to_float(X[(int64_t)n * K + k]);
+        if (skip && !(fabs(x) > tau)) continue;     /* dynamic mask M(x) */
+        double w = (double)or_half_to_float(Wd[(int64_t)m * K + k]);
+        s += w * x;
+    }
+    return s;
+}
+
+/* Wd: M x K fp16 (decoded), X: N x K fp16 token-major, Y: N x M fp16 */
+int or_spmm_f16(const uint16_t* Wd, const uint16_t* X, int M, int N, int K, uint16_t* Y, int nthreads) {
+    if (M <= 0 || N <= 0 || K <= 0) return OR_BAD_ARG;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n)
+            Y[(int64_t)n * M + m] = or_double_to_half(f16_dot(Wd, X, K, m, n, 0.0, 0));
+    return OR_OK;
+}
+
+int or_spmm_f16_at(const uint16_t* Wd, const uint16_t* X, int M, int N, int K,
+                   const int32_t* n_idx, const int32_t* m_idx, int64_t count, uint16_t* y_out,
+                   double* exact_out) {
+    for (int64_t q = 0; q < count; ++q) {
+        int n = n_idx[q], m = m_idx[q];
+        if (n < 0 || n >= N || m < 0 || m >= M) return OR_BAD_ARG;
+        double s = f16_dot(Wd, X, K, m, n, 0.0, 0);
+        if (exact_out) exact_out[q] = s;
+        y_out[q] = or_double_to_half(s);
+    }
+    return OR_OK;
+}
+
+/* spMspV ([SPDP] section 2 and 4.2): y = (W (.) M) . (x (.) M(x)), where
+ * column k is active iff |x_k| > tau; inactive columns are skipped. */
+int or_spmspv_f16(const uint16_t* Wd, const uint16_t* x, float tau, int M, int K, uint16_t* y,
+                  double* exact_out, int nthreads) {
+    if (M <= 0 || K <= 0 || !(tau >= 0.0f)) return OR_BAD_ARG;
+    if (nthreads < 1) nthreads = 1;
+#pragma omp parallel for num_threads(nthreads) schedule(static)
+    for (int m = 0; m < M; ++m) {
+        double s = f16_dot(Wd, x, K, m, 0, (double)tau, 1);
+        if (exact_out) exact_out[m] = s;
+        y[m] = or_double_to_half(s);
+    }
+    return OR_OK;
+}
+
+int or_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

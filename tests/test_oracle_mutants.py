@@ -1,0 +1,52 @@
+"""Mutation check of the oracle's pins: each plausible mistake planted in a copy
+of the oracle source (a wrong bit order, a transposed scan, a dropped term, a
+wrong sign, a dropped padding, a swapped nibble, a wrong tile numbering) must
+make the pin suite fail.  Mistakes are planted only in the CPU oracle's source
+text, in a temporary directory; the committed oracle is untouched."""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "us_oracle.c")
+
+MUTANTS = {
+    "bit_order_msb_first": ("words[p / 64] |= (uint64_t)1 << (p % 64);",
+                            "words[p / 64] |= (uint64_t)1 << (63 - p % 64);"),
+    "row_scan_transposed": ("if (order == OR_ROW) { *i = (int)(p / TK); *j = (int)(p % TK); }",
+                            "if (order == OR_ROW) { *i = (int)(p % TM); *j = (int)(p / TM); }"),
+    "col_scan_transposed": ("else                 { *j = (int)(p / TM); *i = (int)(p % TM); }",
+                            "else                 { *j = (int)(p % TK); *i = (int)(p / TK); }"),
+    "padding_dropped": ("uint64_t padded = (P + E - 1) / E * E;", "uint64_t padded = P;"),
+    "nibble_order_swapped": ("if (e & 1) values[e >> 1] = (uint8_t)((values[e >> 1] & 0x0F) | (nib << 4));",
+                             "if (!(e & 1)) values[e >> 1] = (uint8_t)((values[e >> 1] & 0x0F) | (nib << 4));"),
+    "int4_sign_wrong": ("return (int8_t)(nib >= 8 ? (int)nib - 16 : (int)nib);",
+                        "return (int8_t)(nib >= 8 ? (int)nib - 8 : (int)nib);"),
+    "first_term_dropped": ("for (int k = 0; k < K; ++k)\n        acc +=", "for (int k = 1; k < K; ++k)\n        acc +="),
+    "scales_swapped": ("float t = a * or_half_to_float(s_w);", "float t = a * or_half_to_float(s_w) * 0.5f + a * or_half_to_float(s_x) * 0.5f;"),
+    "abs_dropped_in_skip": ("if (skip && !(fabs(x) > tau)) continue;", "if (skip && !(x > tau)) continue;"),
+    "tile_numbering_colmajor": ("            const int64_t t = (int64_t)tm * nTK + tk;\n            uint64_t* words = bitmap",
+                                "            const int64_t t = (int64_t)tk * nTM + tm;\n            uint64_t* words = bitmap"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc missing")
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    mut = tmp_path / "mut.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmut.so"
+    subprocess.run(["gcc", "-O1", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=gnu11",
+                    "-o", str(lib), str(mut), "-lm"], check=True)
+    env = dict(os.environ, US_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"planted mistake {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -1,0 +1,340 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+No GPU.  Every check here compares the oracle with something other than itself:
+worked examples printed on the pages (tests/golden), the Tiled-CBC storage
+formula, a pure-Python brute force on tiny inputs (tests/brute.py), closed
+forms (sparsity 0 -> dense GEMM via numpy, sparsity 100 % -> zero, one nonzero
+-> one scaled activation), numpy's own fp16 conversions, and invariants
+(round trip, per-tile popcount, offsets).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+from bitmap_encoded_unstructured_ie_gb300 import workloads as wl
+from tests import brute
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+F16, I4, ROW, COL = 0, 1, 0, 1
+
+
+def _popcount64(a: np.ndarray) -> np.ndarray:
+    a = a.astype(np.uint64)
+    return np.array([bin(int(v)).count("1") for v in a.reshape(-1)], dtype=np.int64).reshape(a.shape)
+
+
+def _rand_i4(rng, M, K, density):
+    q = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
+    q[rng.random((M, K)) >= density] = 0
+    return q
+
+
+def _rand_f16(rng, M, K, density):
+    w = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
+    w[rng.random((M, K)) >= density] = 0
+    return w
+
+
+# --------------------------------------------------------------- page pins --
+def test_fig7_union_bitmap_words(orc):
+    """UnionSparse Fig. 7: the four printed mask rows pack (leftmost = LSB)."""
+    g = json.load(open(os.path.join(GOLD, "fig7_union_bitmap.json")))
+    rows = [int(w, 16) for w in g["row_words"]]
+    width = g["row_width"]
+    W = np.zeros((4, width), dtype=np.int8)
+    for i, word in enumerate(rows):
+        for j in range(width):
+            if (word >> j) & 1:
+                W[i, j] = 1 + (i + j) % 7          # any nonzero payload
+    # one 4 x 16 tile in row-major scan -> one 64-bit word, row i in bits 16i..16i+15
+    bm, off, vals = orc.encode(W, 4, 16, I4, ROW)
+    assert bm.size == 1
+    expect = rows[0] | rows[1] << 16 | rows[2] << 32 | rows[3] << 48
+    assert int(bm[0]) == expect
+    for i in range(4):
+        assert bin(rows[i]).count("1") == g["active_per_row"]
+    assert int(_popcount64(bm).sum()) == g["P_t"]
+    # Q = 1 here: the next offset is P_t rounded up to the 16-byte quantum
+    assert int(off[1]) == (g["P_t"] + 31) // 32 * 32
+    bmf, offf, _ = orc.encode(W.astype(np.float16), 4, 16, F16, ROW)
+    assert int(bmf[0]) == expect and int(offf[1]) == g["P_t"]    # 40 is a multiple of 8
+    # the Q-area offset of the figure is Q * P_t
+    assert g["Q"] * g["P_t"] == g["next_offset_with_Q"]
+
+
+def test_fig9c_segment_ranks(orc):
+    """UnionSparse Fig. 9(c): segment 10110100 -> payload indices b..b+3."""
+    g = json.load(open(os.path.join(GOLD, "fig9c_segment.json")))
+    seg = [int(c) for c in g["segment_bits_position0_first"]]
+    assert [p for p, b in enumerate(seg) if b] == g["active_positions"]
+    # a 1 x 64 tile: 5 set positions before the segment give base b = 5
+    W = np.zeros((1, 64), dtype=np.int8)
+    W[0, 1:6] = [1, 2, 3, 4, 5]
+    start = 16
+    payload = [-8, 7, -1, 6]
+    for v, p in zip(payload, g["active_positions"]):
+        W[0, start + p] = v
+    bm, off, vals = orc.encode(W, 1, 64, I4, ROW)
+    assert (int(bm[0]) >> start) & 0xFF == 0b00101101 == 0x2D
+    stream = orc.unpack_int4(vals, int(off[1]))
+    b = 5
+    for v, r in zip(payload, g["payload_index_minus_base"]):
+        assert stream[b + r] == v
+    dec = orc.decode(bm, off, vals, 1, 64, 1, 64, I4, ROW)
+    assert np.array_equal(dec, W)
+
+
+def test_tiled_cbc_storage_formula(orc):
+    """SPDP 4.1: Stor = 4(N_GT+1) + 4 N_GT TILE_K + 8 N_BM + 2 NNZ.  Ours drops the
+    ColInfo term and adds the 16-byte padding of each tile's run."""
+    rng = np.random.default_rng(3)
+    for (M, K, TM, TK) in [(256, 64, 256, 16), (128, 128, 64, 64), (512, 96, 256, 32)]:
+        W = _rand_f16(rng, M, K, 0.45)
+        bm, off, vals = orc.encode(W, TM, TK, F16, COL)
+        NGT = (M // TM) * (K // TK)
+        NBM = M * K // 64
+        nz = (W.view(np.uint16) & 0x7FFF) != 0
+        NNZ = int(nz.sum())
+        per_tile = nz.reshape(M // TM, TM, K // TK, TK).sum(axis=(1, 3)).reshape(-1)
+        pad_bytes = int(((-per_tile) % 8).sum()) * 2
+        formula = 4 * (NGT + 1) + 4 * NGT * TK + 8 * NBM + 2 * NNZ
+        ours = off.nbytes + bm.nbytes + vals.nbytes
+        assert ours == formula - 4 * NGT * TK + pad_bytes
+
+
+# ------------------------------------------------------------ brute force --
+@pytest.mark.parametrize("elem", [F16, I4])
+@pytest.mark.parametrize("order", [ROW, COL])
+@pytest.mark.parametrize("shape", [(8, 16, 8, 8), (16, 24, 8, 8), (4, 32, 4, 16), (64, 8, 64, 1)])
+def test_encode_matches_brute_force(orc, elem, order, shape):
+    M, K, TM, TK = shape
+    rng = np.random.default_rng(M * 31 + K + elem * 7 + order)
+    for density in (0.0, 0.3, 0.7, 1.0):
+        W = _rand_f16(rng, M, K, density).view(np.uint16) if elem == F16 else _rand_i4(rng, M, K, density)
+        bm, off, vals = orc.encode(W, TM, TK, elem, order)
+        words, offsets, data = brute.encode(brute.to_lists(W), TM, TK, elem, order)
+        assert [int(v) for v in bm] == words
+        assert [int(v) for v in off] == offsets
+        assert bytes(vals.tobytes()) == data
+
+
+def test_decode_matches_brute_force_values(orc):
+    rng = np.random.default_rng(11)
+    W = _rand_i4(rng, 8, 16, 0.5)
+    words, offsets, data = brute.encode(brute.to_lists(W), 8, 8, I4, COL)
+    dec = orc.decode(np.array(words, np.uint64), np.array(offsets, np.uint32),
+                     np.frombuffer(data, np.uint8), 8, 16, 8, 8, I4, COL)
+    assert np.array_equal(dec, W)
+
+
+# ------------------------------------------------------------- invariants --
+@pytest.mark.parametrize("elem", [F16, I4])
+@pytest.mark.parametrize("order", [ROW, COL])
+def test_round_trip_and_offsets(orc, elem, order):
+    rng = np.random.default_rng(5 + elem + 2 * order)
+    M, K, TM, TK = 256, 192, 64, 64
+    for density in (0.0, 0.01, 0.5, 0.93, 1.0):
+        W = _rand_f16(rng, M, K, density) if elem == F16 else _rand_i4(rng, M, K, density)
+        bm, off, vals = orc.encode(W, TM, TK, elem, order)
+        dec = orc.decode(bm, off, vals, M, K, TM, TK, elem, order)
+        Wv = W.view(np.uint16) if elem == F16 else W
+        assert np.array_equal(dec, Wv)
+        wpt = TM * TK // 64
+        P = _popcount64(bm).reshape(-1, wpt).sum(axis=1)
+        E = 8 if elem == F16 else 32
+        assert np.array_equal(np.diff(off.astype(np.int64)), (P + E - 1) // E * E)
+        assert vals.nbytes == int(off[-1]) * (2 if elem == F16 else 1) // (1 if elem == F16 else 2)
+        nz = (Wv & 0x7FFF) != 0 if elem == F16 else Wv != 0
+        assert int(P.sum()) == int(nz.sum())
+
+
+def test_row_and_col_orders_differ_but_decode_alike(orc):
+    rng = np.random.default_rng(9)
+    W = _rand_i4(rng, 128, 128, 0.5)
+    a = orc.encode(W, 64, 64, I4, ROW)
+    b = orc.encode(W, 64, 64, I4, COL)
+    assert not np.array_equal(a[0], b[0])
+    assert np.array_equal(orc.decode(*a, 128, 128, 64, 64, I4, ROW), orc.decode(*b, 128, 128, 64, 64, I4, COL))
+    # same popcount per tile in both orders, so the offsets agree
+    assert np.array_equal(a[1], b[1])
+
+
+def test_f16_signed_zero_and_nan_presence(orc):
+    W = np.zeros((64, 64), dtype=np.uint16)
+    W[0, 0] = 0x8000          # -0.0: not stored
+    W[0, 1] = 0x7E00          # NaN: stored
+    W[5, 7] = 0x3C00          # 1.0
+    bm, off, vals = orc.encode(W, 64, 64, F16, ROW)
+    assert int(bm[0]) == 0b10 and int(off[1]) == 8
+    dec = orc.decode(bm, off, vals, 64, 64, 64, 64, F16, ROW)
+    assert dec[0, 0] == 0 and dec[0, 1] == 0x7E00 and dec[5, 7] == 0x3C00
+
+
+def test_decode_rejects_corrupt_offsets(orc):
+    rng = np.random.default_rng(2)
+    W = _rand_i4(rng, 64, 128, 0.5)
+    bm, off, vals = orc.encode(W, 64, 64, I4, ROW)
+    bad = off.copy(); bad[1] = bad[2] + 32                     # not monotone
+    with pytest.raises(orc.OracleError):
+        orc.decode(bm, bad, vals, 64, 128, 64, 64, I4, ROW)
+    bad = off.copy(); bad[1] -= 32                              # run shorter than popcount
+    with pytest.raises(orc.OracleError):
+        orc.decode(bm, bad, vals, 64, 128, 64, 64, I4, ROW)
+    with pytest.raises(orc.OracleError):                        # values buffer too short
+        orc.decode(bm, off, vals[:-16], 64, 128, 64, 64, I4, ROW)
+
+
+def test_encode_rejects_bad_shapes_and_codes(orc):
+    with pytest.raises(orc.OracleError):
+        orc.encode(np.zeros((60, 64), np.int8), 64, 64, I4, ROW)
+    with pytest.raises(orc.OracleError):
+        orc.encode(np.full((64, 64), 9, np.int8), 64, 64, I4, ROW)
+
+
+# ---------------------------------------------------------------- fp16 ----
+def test_half_conversions_match_numpy(orc):
+    for bits in list(range(0, 65536, 97)) + [0x7BFF, 0xFBFF, 0x0001, 0x8001, 0x3C00]:
+        f = orc.half_to_float(bits)
+        ref = float(np.array([bits], np.uint16).view(np.float16)[0])
+        assert (f == ref) or (np.isnan(f) and np.isnan(ref))
+    rng = np.random.default_rng(0)
+    for x in np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-8, 5, 2000),
+                             [65519.99, 65520.0, 1e-8, 2.0 ** -25, 3 * 2.0 ** -26]]):
+        assert orc.double_to_half(float(x)) == int(np.array([x], np.float64).astype(np.float16).view(np.uint16)[0])
+        xf = np.float32(x)
+        assert orc.float_to_half(float(xf)) == int(np.array([xf]).astype(np.float16).view(np.uint16)[0])
+
+
+def test_int4_unpack_matches_independent_packer(orc):
+    rng = np.random.default_rng(4)
+    codes = rng.integers(-8, 8, size=1001).astype(np.int8)
+    packed = wl.pack_int4(codes)
+    assert np.array_equal(orc.unpack_int4(packed, codes.size), codes)
+    assert packed[0] == ((int(codes[0]) & 15) | ((int(codes[1]) & 15) << 4))
+
+
+# -------------------------------------------------------------- multiply ----
+def test_w4a4_dense_equals_numpy_gemm(orc):
+    """Sparsity 0: the product is the plain integer GEMM (numpy int64)."""
+    rng = np.random.default_rng(7)
+    M, K, N = 96, 160, 5
+    W = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
+    X = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
+    s_x = (rng.random(N) * 0.5 + 0.1).astype(np.float16)
+    acc, y = orc.spmm_w4a4(W, X, s_w, s_x)
+    ref = X.astype(np.int64) @ W.astype(np.int64).T
+    assert np.array_equal(acc.astype(np.int64), ref)
+    # dequantisation: two fp32 products, one fp16 rounding (numpy's own ops)
+    yref = ((ref.astype(np.float32) * s_w.astype(np.float32)[None, :]) * s_x.astype(np.float32)[:, None]).astype(np.float16)
+    assert np.array_equal(y.view(np.uint16), yref.view(np.uint16))
+
+
+def test_w4a4_extremes_and_threads(orc):
+    M, K, N = 64, 4096, 2
+    W = np.full((M, K), -8, np.int8)
+    X = np.full((N, K), -8, np.int8)
+    one = np.ones(M, np.float16)
+    acc, _ = orc.spmm_w4a4(W, X, one, np.ones(N, np.float16))
+    assert (acc == 64 * K).all()
+    W[:, 1::2] = 7
+    acc4, _ = orc.spmm_w4a4(W, X, one, np.ones(N, np.float16), nthreads=4)
+    assert (acc4 == (64 - 56) * K // 2).all()
+
+
+def test_sparse_special_cases(orc):
+    rng = np.random.default_rng(12)
+    M, K, N = 128, 128, 3
+    X = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    s = np.ones(M, np.float16)
+    W = np.zeros((M, K), np.int8)                                    # sparsity 100 %
+    bm, off, vals = orc.encode(W, 64, 64, I4, ROW)
+    assert vals.size == 0 and int(off[-1]) == 0
+    Wd = orc.decode(bm, off, vals, M, K, 64, 64, I4, ROW)
+    acc, y = orc.spmm_w4a4(Wd, X, s, np.ones(N, np.float16))
+    assert not acc.any() and not y.view(np.uint16).any()
+    W[37, 99] = -5                                                   # one nonzero
+    Wd = orc.decode(*orc.encode(W, 64, 64, I4, ROW), M, K, 64, 64, I4, ROW)
+    acc, _ = orc.spmm_w4a4(Wd, X, s, np.ones(N, np.float16))
+    expect = np.zeros((N, M), np.int64)
+    expect[:, 37] = -5 * X[:, 99].astype(np.int64)
+    assert np.array_equal(acc.astype(np.int64), expect)
+
+
+def test_tiny_products_match_brute_force(orc):
+    rng = np.random.default_rng(21)
+    M, K, N = 8, 24, 3
+    W = _rand_i4(rng, M, K, 0.5)
+    X = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    acc, _ = orc.spmm_w4a4(W, X, np.ones(M, np.float16), np.ones(N, np.float16))
+    for n in range(N):
+        for m in range(M):
+            assert acc[n, m] == brute.dot_w4a4(W[m], X[n])
+    Wf = _rand_f16(rng, M, K, 0.6)
+    Xf = rng.standard_normal((N, K)).astype(np.float16)
+    y = orc.spmm_f16(Wf, Xf)
+    for n in range(N):
+        for m in range(M):
+            exact = brute.dot_f16_exact(Wf[m], Xf[n])
+            assert y[n, m] == np.float16(float(exact))
+
+
+def test_f16_dense_equals_fp64_gemm(orc):
+    """Sparsity 0: fp16 output = fp16(fp64 GEMM); the fp64 sum agrees with numpy."""
+    rng = np.random.default_rng(8)
+    M, K, N = 64, 512, 4
+    W = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
+    X = rng.standard_normal((N, K)).astype(np.float16)
+    y = orc.spmm_f16(W, X)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T
+    n_idx, m_idx = np.meshgrid(np.arange(N), np.arange(M), indexing="ij")
+    y_at, exact = orc.spmm_f16_at(W, X, n_idx.reshape(-1), m_idx.reshape(-1))
+    assert np.allclose(exact, ref.reshape(-1), rtol=1e-12, atol=1e-15)
+    assert np.array_equal(y_at.view(np.uint16), exact.astype(np.float16).view(np.uint16))
+    assert np.array_equal(y.reshape(-1).view(np.uint16), y_at.view(np.uint16))
+
+
+def test_sampled_w4a4_equals_full(orc):
+    d = wl.w4a4(128, 256, 3, 0.5, seed=1)
+    acc, y = orc.spmm_w4a4(d["Wq"], d["Xq"], d["s_w"], d["s_x"])
+    n = np.array([0, 2, 1, 2]); m = np.array([0, 127, 64, 5])
+    a2, y2 = orc.spmm_w4a4_at(d["Wq"], d["Xq"], d["s_w"], d["s_x"], n, m)
+    assert np.array_equal(a2, acc[n, m]) and np.array_equal(y2.view(np.uint16), y[n, m].view(np.uint16))
+
+
+def test_spmspv_tau0_equals_spmv_and_threshold_is_mask(orc):
+    """SPDP section 2: W.(x (.) M(x)); with tau = 0 skipping zeros changes nothing,
+    and a COL-order encoding decodes to the same W as the ROW-order one."""
+    d = wl.spmspv(256, 512, 0.5, 0.7, seed=3)
+    W, x = d["W"], d["x"]
+    col = orc.encode(W, 64, 64, F16, COL)
+    row = orc.encode(W, 64, 64, F16, ROW)
+    Wc = orc.decode(*col, 256, 512, 64, 64, F16, COL)
+    Wr = orc.decode(*row, 256, 512, 64, 64, F16, ROW)
+    assert np.array_equal(Wc, Wr)
+    y, ex = orc.spmspv_f16(Wc, x, 0.0)
+    y2 = orc.spmm_f16(Wr, x.reshape(1, -1))
+    assert np.array_equal(y.view(np.uint16), y2.reshape(-1).view(np.uint16))
+    tau = 0.6
+    x = np.random.default_rng(5).standard_normal(512).astype(np.float16)   # both signs
+    y3, ex3 = orc.spmspv_f16(Wc, x, tau)
+    xm = np.where(np.abs(x.astype(np.float64)) > tau, x.astype(np.float64), 0.0)
+    ref = Wc.view(np.float16).astype(np.float64) @ xm
+    assert np.allclose(ex3, ref, rtol=1e-12, atol=1e-15)
+    assert np.array_equal(y3.view(np.uint16), ex3.astype(np.float16).view(np.uint16))
+
+
+# ----------------------------------------------------------- workloads -----
+def test_workload_statistics():
+    d = wl.w4a4(256, 1024, 2, 0.7, seed=0)
+    dens = (d["Wq"] != 0).mean()
+    assert 0.25 < dens < 0.31
+    kept_rows = (d["Wq"] != 0).sum(axis=1)
+    assert kept_rows.max() <= round(0.3 * 1024)
+    b = wl.w4a4(512, 1024, 1, 0.5, seed=0, rows="beta")
+    rd = (b["Wq"] != 0).mean(axis=1)
+    assert rd.min() > 0.25 and rd.max() < 0.71 and abs(rd.mean() - 0.5) < 0.05
+    x = wl.spmspv(64, 4096, 0.5, 0.9, seed=0)["x"]
+    assert abs((x == 0).mean() - 0.9) < 1e-3
