@@ -1,0 +1,222 @@
+"""Thin ctypes binding of libus (include/us.h) over torch tensors.
+
+Argument marshalling only: every step of encode / SpMM / spMspV runs in the
+CUDA library.  Torch supplies device memory and the current stream.  If the
+library has not been built, the first call raises ``LibraryMissing``: there is
+no CPU fallback.
+
+Function names follow the C ABI: ``us_encode``, ``us_spmm_w4a4``,
+``us_spmm_f16``, ``us_spmspv_f16``, ``us_workspace_bytes``, ``us_pick_split_k``,
+``us_validate``, ``us_get_last_device_status``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libus.so")
+
+US_OK, US_ERR_INVALID_ARG, US_ERR_UNSUPPORTED, US_ERR_TOO_LARGE = 0, 1, 2, 3
+US_ERR_WORKSPACE, US_ERR_CUDA, US_ERR_TIMEOUT, US_ERR_CORRUPT = 4, 5, 6, 7
+US_F16, US_I4 = 0, 1
+US_ORDER_ROW, US_ORDER_COL = 0, 1
+US_OP_ENCODE, US_OP_SPMM_W4A4, US_OP_SPMM_F16, US_OP_SPMSPV_F16 = 0, 1, 2, 3
+
+EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmspv_f16",
+            "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
+            "us_status_string", "us_version")
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+class UsError(RuntimeError):
+    def __init__(self, fn: str, code: int, text: str):
+        super().__init__(f"{fn}: {text} ({code})")
+        self.code = code
+
+
+class us_bitmap(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int32), ("K", ctypes.c_int32), ("TM", ctypes.c_int32), ("TK", ctypes.c_int32),
+                ("elem", ctypes.c_int32), ("order", ctypes.c_int32),
+                ("bitmap", ctypes.c_void_p), ("tile_off", ctypes.c_void_p), ("values", ctypes.c_void_p),
+                ("values_bytes", ctypes.c_uint64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libus.so (once).  Raises LibraryMissing if it was not built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise LibraryMissing(f"{path} not found: build it with __graft_entry__.build() "
+                                 f"or python -m bitmap_encoded_unstructured_ie_gb300.build")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        psz = ctypes.POINTER(ctypes.c_size_t)
+        pbm = ctypes.POINTER(us_bitmap)
+        lib.us_encode_sizes.argtypes = [i32, i32, i32, i32, i32, psz, psz, psz, psz]
+        lib.us_encode.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, P, P, P, sz, P, sz, P]
+        lib.us_spmm_w4a4.argtypes = [pbm, P, P, P, i32, P, P, P, sz, i32, P]
+        lib.us_spmm_f16.argtypes = [pbm, P, i32, P, P, sz, i32, P]
+        lib.us_spmspv_f16.argtypes = [pbm, P, ctypes.c_float, P, P, sz, P]
+        lib.us_workspace_bytes.argtypes = [i32, pbm, i32, i32, psz]
+        lib.us_pick_split_k.argtypes = [i32, pbm, i32, ctypes.POINTER(ctypes.c_int)]
+        lib.us_validate.argtypes = [pbm]
+        lib.us_get_last_device_status.argtypes = [P]
+        lib.us_status_string.argtypes = [i32]
+        lib.us_status_string.restype = ctypes.c_char_p
+        lib.us_version.argtypes = []
+        for name in EXPORTED:
+            if name != "us_status_string":
+                getattr(lib, name).restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().us_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int):
+    if code != US_OK:
+        raise UsError(fn, code, status_string(code))
+
+
+def _dptr(t: torch.Tensor | None):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "device tensors must be contiguous CUDA tensors"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+@dataclass
+class Encoded:
+    """An encoded matrix: three device tensors plus its parameters."""
+    M: int
+    K: int
+    TM: int
+    TK: int
+    elem: int
+    order: int
+    bitmap: torch.Tensor      # uint64 words (int64 storage)
+    tile_off: torch.Tensor    # uint32 (int32 storage), nT + 1
+    values: torch.Tensor      # uint8
+    values_bytes: int
+
+    def desc(self) -> us_bitmap:
+        return us_bitmap(self.M, self.K, self.TM, self.TK, self.elem, self.order,
+                         self.bitmap.data_ptr(), self.tile_off.data_ptr(), self.values.data_ptr(),
+                         self.values_bytes)
+
+    def nbytes(self) -> int:
+        return self.bitmap.numel() * 8 + self.tile_off.numel() * 4 + self.values_bytes
+
+
+def encode_sizes(M, K, TM, TK, elem):
+    b, o, v, w = (ctypes.c_size_t() for _ in range(4))
+    _check("us_encode_sizes", load().us_encode_sizes(M, K, TM, TK, elem, ctypes.byref(b), ctypes.byref(o),
+                                                     ctypes.byref(v), ctypes.byref(w)))
+    return b.value, o.value, v.value, w.value
+
+
+def us_encode(W: torch.Tensor, TM: int, TK: int, elem: int, order: int, stream=None, shrink: bool = True) -> Encoded:
+    """Encode a dense CUDA matrix (fp16 for US_F16, int8 codes for US_I4)."""
+    lib = load()
+    M, K = W.shape
+    dev = W.device
+    assert W.is_cuda and W.stride(1) == 1, "W must be a CUDA matrix with unit column stride"
+    bb, ob, vcap, wsb = encode_sizes(M, K, TM, TK, elem)
+    bitmap = torch.empty(bb // 8, dtype=torch.int64, device=dev)
+    tile_off = torch.empty(ob // 4, dtype=torch.int32, device=dev)
+    values = torch.zeros(max(vcap, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
+    _check("us_encode", lib.us_encode(ctypes.c_void_p(W.data_ptr()), W.stride(0), M, K, TM, TK, elem, order, _dptr(bitmap),
+                                      _dptr(tile_off), _dptr(values), values.numel(), _dptr(ws), ws.numel(),
+                                      _stream(stream)))
+    used_elems = int(tile_off[-1].item()) & 0xFFFFFFFF
+    used = used_elems * (2 if elem == US_F16 else 1) // (1 if elem == US_F16 else 2)
+    if shrink:
+        values = values[: max(used, 16)].clone()
+    return Encoded(M, K, TM, TK, elem, order, bitmap, tile_off, values, used)
+
+
+def from_host(bitmap, tile_off, values, M, K, TM, TK, elem, order, device="cuda") -> Encoded:
+    """Wrap host numpy arrays of an encoded matrix as device tensors."""
+    import numpy as np
+    bm = torch.from_numpy(np.ascontiguousarray(bitmap).view(np.int64)).to(device)
+    off = torch.from_numpy(np.ascontiguousarray(tile_off).view(np.int32)).to(device)
+    v = np.ascontiguousarray(values, dtype=np.uint8)
+    vb = v.size
+    v = np.concatenate([v, np.zeros((-v.size) % 16 + (16 if v.size == 0 else 0), np.uint8)])
+    return Encoded(M, K, TM, TK, elem, order, bm, off, torch.from_numpy(v).to(device), vb)
+
+
+def us_workspace_bytes(op: int, E: Encoded, N: int = 1, split_k: int = 0) -> int:
+    n = ctypes.c_size_t()
+    d = E.desc()
+    _check("us_workspace_bytes", load().us_workspace_bytes(op, ctypes.byref(d), N, split_k, ctypes.byref(n)))
+    return n.value
+
+
+def us_pick_split_k(op: int, E: Encoded, N: int = 1) -> int:
+    s = ctypes.c_int()
+    d = E.desc()
+    _check("us_pick_split_k", load().us_pick_split_k(op, ctypes.byref(d), N, ctypes.byref(s)))
+    return s.value
+
+
+def workspace(op: int, E: Encoded, N: int = 1, split_k: int = 0) -> torch.Tensor:
+    """A zero-filled workspace of the size the call needs."""
+    return torch.zeros(max(us_workspace_bytes(op, E, N, split_k), 16), dtype=torch.uint8, device=E.bitmap.device)
+
+
+def us_spmm_w4a4(E: Encoded, Xq: torch.Tensor, s_w: torch.Tensor, s_x: torch.Tensor, N: int,
+                 Yacc: torch.Tensor, Y: torch.Tensor | None, ws: torch.Tensor, split_k: int = 0, stream=None):
+    d = E.desc()
+    _check("us_spmm_w4a4", load().us_spmm_w4a4(ctypes.byref(d), _dptr(Xq), _dptr(s_w), _dptr(s_x), N, _dptr(Yacc),
+                                               _dptr(Y), _dptr(ws), ws.numel(), split_k, _stream(stream)))
+
+
+def us_spmm_f16(E: Encoded, X: torch.Tensor, N: int, Y: torch.Tensor, ws: torch.Tensor, split_k: int = 0,
+                stream=None):
+    d = E.desc()
+    _check("us_spmm_f16", load().us_spmm_f16(ctypes.byref(d), _dptr(X), N, _dptr(Y), _dptr(ws), ws.numel(),
+                                             split_k, _stream(stream)))
+
+
+def us_spmspv_f16(E: Encoded, x: torch.Tensor, tau: float, y: torch.Tensor, ws: torch.Tensor, stream=None):
+    d = E.desc()
+    _check("us_spmspv_f16", load().us_spmspv_f16(ctypes.byref(d), _dptr(x), float(tau), _dptr(y), _dptr(ws),
+                                                 ws.numel(), _stream(stream)))
+
+
+def us_validate_host(bitmap, tile_off, values, M, K, TM, TK, elem, order) -> int:
+    """us_validate on host numpy arrays; returns the status code."""
+    import numpy as np
+    bm = np.ascontiguousarray(bitmap, dtype=np.uint64)
+    off = np.ascontiguousarray(tile_off, dtype=np.uint32)
+    v = np.ascontiguousarray(values, dtype=np.uint8)
+    d = us_bitmap(M, K, TM, TK, elem, order, bm.ctypes.data, off.ctypes.data,
+                  v.ctypes.data if v.size else None, v.size)
+    return int(load().us_validate(ctypes.byref(d)))
+
+
+def us_get_last_device_status(stream=None) -> int:
+    return int(load().us_get_last_device_status(_stream(stream)))

@@ -1,0 +1,319 @@
+// us_api.cu -- the C ABI of libus: argument checks, sizes, dispatch.
+//
+// Every entry point validates on the host before enqueuing anything and
+// returns a us_status; nothing throws across the ABI.  The device status word
+// g_us_status collects device-side errors (timeouts, corrupt offsets,
+// out-of-range codes); us_get_last_device_status reads and clears it.
+#include <mutex>
+
+#include "us_common.cuh"
+#include "us_internal.h"
+
+__device__ unsigned g_us_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return (d >= 0 && d < kMaxDevices) ? d : -1;
+}
+
+// Device address of g_us_status on the current device (looked up once).
+unsigned* status_ptr() {
+    const int d = current_device();
+    if (d < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_status_ptr[d]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_us_status) != cudaSuccess) return nullptr;
+        g_status_ptr[d] = static_cast<unsigned*>(p);
+    }
+    return g_status_ptr[d];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool tile_ok(int TM, int TK) {
+    return (TM == 64 || TM == 128 || TM == 256) && (TK == 16 || TK == 32 || TK == 64 || TK == 128);
+}
+
+us_status check_shape(int M, int K, int TM, int TK, int elem) {
+    if (M <= 0 || K <= 0 || !tile_ok(TM, TK)) return US_ERR_INVALID_ARG;
+    if (M % TM || K % TK) return US_ERR_INVALID_ARG;
+    if (elem != US_F16 && elem != US_I4) return US_ERR_INVALID_ARG;
+    if ((uint64_t)M * (uint64_t)K >= (1ull << 32)) return US_ERR_TOO_LARGE;
+    return US_OK;
+}
+
+us_status check_bitmap(const us_bitmap* W, int elem, int order) {
+    if (!W) return US_ERR_INVALID_ARG;
+    us_status s = check_shape(W->M, W->K, W->TM, W->TK, W->elem);
+    if (s != US_OK) return s;
+    if (W->order != US_ORDER_ROW && W->order != US_ORDER_COL) return US_ERR_INVALID_ARG;
+    if (W->elem != elem) return US_ERR_INVALID_ARG;
+    if (W->order != order) return US_ERR_UNSUPPORTED;
+    if (!W->bitmap || !W->tile_off || (!W->values && W->values_bytes)) return US_ERR_INVALID_ARG;
+    if (!aligned16(W->bitmap) || !aligned16(W->tile_off) || !aligned16(W->values)) return US_ERR_INVALID_ARG;
+    return US_OK;
+}
+
+// split-K rule: the smallest candidate whose grid covers every SM, keeping at
+// least 4 K tiles per slice.
+int auto_split(int nTM, int nTK, int token_blocks) {
+    const int sms = us::num_sms();
+    const int cands[] = {1, 2, 4, 8, 16};
+    int best = 1;
+    for (int c : cands) {
+        if (nTK / c < 4) break;
+        best = c;
+        if ((int64_t)nTM * c * token_blocks >= sms) break;
+    }
+    return best;
+}
+
+void fill_common(UsKParams& p, const us_bitmap* W, int N) {
+    p.M = W->M; p.K = W->K; p.TM = W->TM; p.TK = W->TK;
+    p.nTM = W->M / W->TM; p.nTK = W->K / W->TK;
+    p.N = N;
+    p.bitmap = W->bitmap; p.tile_off = W->tile_off;
+    p.values = static_cast<const uint8_t*>(W->values);
+    p.values_bytes = W->values_bytes;
+    p.X = nullptr; p.s_w = nullptr; p.s_x = nullptr; p.Yacc = nullptr; p.Y = nullptr;
+    p.tau = 0.f; p.ws = nullptr; p.counters = nullptr;
+    p.status = status_ptr();
+}
+
+// Launch plan for an SpMM call: kernel family, split, token block, workspace.
+struct Plan {
+    bool fast;
+    int split;
+    int tok_block;
+    size_t ws;
+};
+
+Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
+    Plan pl{};
+    const int nTM = W->M / W->TM, nTK = W->K / W->TK;
+    pl.fast = (op == US_OP_SPMM_W4A4) && us::w4a4_fast_supported(W->TM, W->TK, N);
+    pl.tok_block = pl.fast ? N : us::spmm_generic_tok_block(N);
+    const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
+    pl.split = split_k > 0 ? split_k : auto_split(nTM, nTK, ntb);
+    if (pl.split > nTK) pl.split = nTK;
+    pl.ws = pl.fast ? us::w4a4_fast_ws(W->M, W->TM, N, pl.split)
+                    : us::spmm_generic_ws(W->M, W->TM, N, pl.split, pl.tok_block);
+    return pl;
+}
+
+Plan plan_spmspv(const us_bitmap* W) {
+    Plan pl{};
+    pl.tok_block = 1;
+    pl.split = auto_split(W->M / W->TM, W->K / W->TK, 1);
+    pl.ws = us::spmspv_ws(W->M, W->TM, pl.split);
+    return pl;
+}
+
+size_t counters_bytes(int nTM, int ntb) { return ((size_t)nTM * ntb * 4 + 255) & ~(size_t)255; }
+
+}  // namespace
+
+namespace us {
+
+int num_sms() {
+    const int d = current_device();
+    if (d < 0) return 148;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_num_sms[d]) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || v <= 0) v = 148;
+        g_num_sms[d] = v;
+    }
+    return g_num_sms[d];
+}
+
+}  // namespace us
+
+extern "C" {
+
+int us_version(void) { return 100; }
+
+const char* us_status_string(us_status s) {
+    switch (s) {
+        case US_OK: return "ok";
+        case US_ERR_INVALID_ARG: return "invalid argument";
+        case US_ERR_UNSUPPORTED: return "unsupported combination";
+        case US_ERR_TOO_LARGE: return "too large";
+        case US_ERR_WORKSPACE: return "workspace or capacity too small";
+        case US_ERR_CUDA: return "CUDA error";
+        case US_ERR_TIMEOUT: return "device wait timed out";
+        case US_ERR_CORRUPT: return "corrupt format";
+    }
+    return "unknown status";
+}
+
+us_status us_encode_sizes(int M, int K, int TM, int TK, us_elem elem, size_t* bitmap_bytes,
+                          size_t* tile_off_bytes, size_t* values_cap_bytes, size_t* ws_bytes) {
+    us_status s = check_shape(M, K, TM, TK, elem);
+    if (s != US_OK) return s;
+    const uint64_t nT = (uint64_t)(M / TM) * (K / TK);
+    if (bitmap_bytes) *bitmap_bytes = (size_t)M * K / 8;
+    if (tile_off_bytes) *tile_off_bytes = (size_t)(nT + 1) * 4;
+    if (values_cap_bytes) *values_cap_bytes = (size_t)M * K * (elem == US_F16 ? 2 : 1) / (elem == US_F16 ? 1 : 2);
+    if (ws_bytes) *ws_bytes = ((size_t)nT * 4 + 255) & ~(size_t)255;
+    return US_OK;
+}
+
+us_status us_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, us_elem elem, us_order order,
+                    uint64_t* bitmap, uint32_t* tile_off, void* values, size_t values_cap, void* ws,
+                    size_t ws_bytes, void* stream) {
+    us_status s = check_shape(M, K, TM, TK, elem);
+    if (s != US_OK) return s;
+    if (order != US_ORDER_ROW && order != US_ORDER_COL) return US_ERR_INVALID_ARG;
+    if (!W || !bitmap || !tile_off || !values || !ws || ldw < K) return US_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & (elem == US_F16 ? 1u : 0u)) != 0) return US_ERR_INVALID_ARG;
+    if (!aligned16(bitmap) || !aligned16(tile_off) || !aligned16(values) || !aligned16(ws))
+        return US_ERR_INVALID_ARG;
+    size_t need = 0;
+    us_encode_sizes(M, K, TM, TK, elem, nullptr, nullptr, nullptr, &need);
+    if (ws_bytes < need) return US_ERR_WORKSPACE;
+    return us::launch_encode(W, ldw, M, K, TM, TK, elem, order, bitmap, tile_off, values, values_cap,
+                             static_cast<uint32_t*>(ws), status_ptr(), static_cast<cudaStream_t>(stream));
+}
+
+us_status us_workspace_bytes(us_op op, const us_bitmap* W, int N, int split_k, size_t* bytes) {
+    if (!W || !bytes) return US_ERR_INVALID_ARG;
+    us_status s = check_shape(W->M, W->K, W->TM, W->TK, op == US_OP_ENCODE ? US_F16 : W->elem);
+    if (s != US_OK) return s;
+    if (split_k < 0) return US_ERR_INVALID_ARG;
+    switch (op) {
+        case US_OP_ENCODE:
+            return us_encode_sizes(W->M, W->K, W->TM, W->TK, US_F16, nullptr, nullptr, nullptr, bytes);
+        case US_OP_SPMM_W4A4:
+        case US_OP_SPMM_F16:
+            if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
+            *bytes = plan_spmm(op, W, N, split_k).ws;
+            return US_OK;
+        case US_OP_SPMSPV_F16: {
+            Plan pl = plan_spmspv(W);
+            if (split_k > 0) pl.ws = us::spmspv_ws(W->M, W->TM, split_k);
+            *bytes = pl.ws;
+            return US_OK;
+        }
+    }
+    return US_ERR_INVALID_ARG;
+}
+
+us_status us_pick_split_k(us_op op, const us_bitmap* W, int N, int* split_k) {
+    if (!W || !split_k) return US_ERR_INVALID_ARG;
+    us_status s = check_shape(W->M, W->K, W->TM, W->TK, W->elem);
+    if (s != US_OK) return s;
+    if (op == US_OP_SPMSPV_F16) { *split_k = plan_spmspv(W).split; return US_OK; }
+    if (op != US_OP_SPMM_W4A4 && op != US_OP_SPMM_F16) return US_ERR_INVALID_ARG;
+    if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
+    *split_k = plan_spmm(op, W, N, 0).split;
+    return US_OK;
+}
+
+us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_w, const uint16_t* s_x, int N,
+                       int32_t* Yacc, uint16_t* Y, void* ws, size_t ws_bytes, int split_k, void* stream) {
+    us_status s = check_bitmap(W, US_I4, US_ORDER_ROW);
+    if (s != US_OK) return s;
+    if (N < 1 || N > 2048 || W->K % 32) return US_ERR_INVALID_ARG;
+    if (!Xq || !Yacc || !aligned16(Xq) || !aligned16(Yacc)) return US_ERR_INVALID_ARG;
+    if (Y && (!s_w || !s_x || !aligned16(Y))) return US_ERR_INVALID_ARG;
+    if (split_k < 0 || split_k > W->K / W->TK) return US_ERR_INVALID_ARG;
+    if (!ws) return US_ERR_WORKSPACE;
+    const Plan pl = plan_spmm(US_OP_SPMM_W4A4, W, N, split_k);
+    if (ws_bytes < pl.ws || !aligned16(ws)) return US_ERR_WORKSPACE;
+    UsKParams p;
+    fill_common(p, W, N);
+    p.X = Xq; p.s_w = s_w; p.s_x = s_x; p.Yacc = Yacc; p.Y = Y;
+    p.split = pl.split; p.tok_block = pl.tok_block;
+    const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
+    p.counters = static_cast<unsigned*>(ws);
+    p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return pl.fast ? us::launch_w4a4_fast(p, st) : us::launch_spmm_generic(p, US_I4, st);
+}
+
+us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y, void* ws, size_t ws_bytes,
+                      int split_k, void* stream) {
+    us_status s = check_bitmap(W, US_F16, US_ORDER_ROW);
+    if (s != US_OK) return s;
+    if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
+    if (!X || !Y || !aligned16(X) || !aligned16(Y)) return US_ERR_INVALID_ARG;
+    if (split_k < 0 || split_k > W->K / W->TK) return US_ERR_INVALID_ARG;
+    if (!ws) return US_ERR_WORKSPACE;
+    const Plan pl = plan_spmm(US_OP_SPMM_F16, W, N, split_k);
+    if (ws_bytes < pl.ws || !aligned16(ws)) return US_ERR_WORKSPACE;
+    UsKParams p;
+    fill_common(p, W, N);
+    p.X = X; p.Y = Y;
+    p.split = pl.split; p.tok_block = pl.tok_block;
+    const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
+    p.counters = static_cast<unsigned*>(ws);
+    p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
+    return us::launch_spmm_generic(p, US_F16, static_cast<cudaStream_t>(stream));
+}
+
+us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y, void* ws, size_t ws_bytes,
+                        void* stream) {
+    us_status s = check_bitmap(W, US_F16, US_ORDER_COL);
+    if (s != US_OK) return s;
+    if (!x || !y || !aligned16(x) || !aligned16(y) || !(tau >= 0.f)) return US_ERR_INVALID_ARG;
+    if (!ws) return US_ERR_WORKSPACE;
+    const Plan pl = plan_spmspv(W);
+    if (ws_bytes < pl.ws || !aligned16(ws)) return US_ERR_WORKSPACE;
+    UsKParams p;
+    fill_common(p, W, 1);
+    p.X = x; p.Y = y; p.tau = tau;
+    p.split = pl.split; p.tok_block = 1;
+    p.counters = static_cast<unsigned*>(ws);
+    p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, 1);
+    return us::launch_spmspv(p, static_cast<cudaStream_t>(stream));
+}
+
+us_status us_validate(const us_bitmap* W) {
+    if (!W) return US_ERR_INVALID_ARG;
+    us_status s = check_shape(W->M, W->K, W->TM, W->TK, W->elem);
+    if (s != US_OK) return s;
+    if (W->order != US_ORDER_ROW && W->order != US_ORDER_COL) return US_ERR_INVALID_ARG;
+    if (!W->bitmap || !W->tile_off || (!W->values && W->values_bytes)) return US_ERR_INVALID_ARG;
+    const int nTM = W->M / W->TM, nTK = W->K / W->TK;
+    const int64_t nT = (int64_t)nTM * nTK;
+    const int64_t wpt = (int64_t)W->TM * W->TK / 64;
+    const int bits = W->elem == US_F16 ? 16 : 4;
+    const uint32_t E = W->elem == US_F16 ? 8u : 32u;
+    const uint8_t* vals = static_cast<const uint8_t*>(W->values);
+    if (W->tile_off[0] != 0) return US_ERR_CORRUPT;
+    for (int64_t t = 0; t < nT; ++t) {
+        const uint64_t o0 = W->tile_off[t], o1 = W->tile_off[t + 1];
+        if (o1 < o0 || (o1 - o0) % E) return US_ERR_CORRUPT;
+        if (o1 * bits > (uint64_t)W->values_bytes * 8) return US_ERR_CORRUPT;
+        uint64_t P = 0;
+        for (int64_t w = 0; w < wpt; ++w) P += (uint64_t)__builtin_popcountll(W->bitmap[t * wpt + w]);
+        if (P > o1 - o0 || (o1 - o0) - P >= E) return US_ERR_CORRUPT;
+        for (uint64_t e = o0 + P; e < o1; ++e) {   // padding must be zero
+            const uint8_t by = vals[e * bits / 8];
+            const uint8_t v = bits == 16 ? by : (uint8_t)((e & 1) ? (by >> 4) : (by & 15));
+            if (v || (bits == 16 && vals[e * 2 + 1])) return US_ERR_CORRUPT;
+        }
+    }
+    return US_OK;
+}
+
+us_status us_get_last_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return US_ERR_CUDA;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_us_status, sizeof(v)) != cudaSuccess) return US_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_us_status, &zero, sizeof(zero)) != cudaSuccess) return US_ERR_CUDA;
+    return static_cast<us_status>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,141 @@
+// us_common.cuh -- device helpers shared by the libus kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data movers used by every kernel: mbarrier
+// transaction barriers and the bulk (TMA 1-D) global->shared copy, plus the
+// bounded waits and the device status word that replace traps and endless
+// spins.  Nothing here belongs to the format's arithmetic.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include "../../include/us.h"
+
+#define US_DEV __device__ __forceinline__
+
+namespace us {
+
+// ----------------------------------------------------------------- status --
+// The first device-side error wins; later ones are dropped.
+US_DEV void set_status(unsigned* status, unsigned code) {
+    if (status) atomicCAS(status, 0u, code);
+}
+
+US_DEV uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// A wait gives up after this long; the kernel then records US_ERR_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s
+
+// --------------------------------------------------------------- mbarrier --
+US_DEV uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+US_DEV void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+US_DEV void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+US_DEV void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+US_DEV void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+US_DEV void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+US_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for phase `parity` of `bar`.  Returns false (and records
+// US_ERR_TIMEOUT) if the phase did not complete within kWaitLimitNs.
+US_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            set_status(status, US_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Bulk copy global -> shared (TMA, 1-D, no tensor map), completing `bytes`
+// transactions on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
+US_DEV void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// L2 prefetch of a global range (bytes a multiple of 16).
+US_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ------------------------------------------------------------------- misc --
+US_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
+
+US_DEV int warp_incl_scan(int v) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, v, d);
+        if ((int)lane_id() >= d) v += o;
+    }
+    return v;
+}
+
+US_DEV float half_bits_to_float(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+US_DEV uint16_t float_to_half_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+
+// int4 code in the low nibble of v -> int (two's complement)
+US_DEV int sext4(uint32_t v) { return (int)(v << 28) >> 28; }
+
+}  // namespace us
+
+// ------------------------------------------------------- kernel parameters --
+// One plain struct passed by value to every SpMM / spMspV kernel.
+struct UsKParams {
+    int M, K, TM, TK, nTM, nTK;
+    int N;              // tokens
+    int split;          // K slices
+    int tok_block;      // tokens per CTA (grid.y = ceil(N / tok_block))
+    const uint64_t* bitmap;
+    const uint32_t* tile_off;
+    const uint8_t* values;
+    uint64_t values_bytes;
+    const void* X;      // I4: packed nibbles N x K; F16: fp16 N x K
+    const uint16_t* s_w;
+    const uint16_t* s_x;
+    int32_t* Yacc;
+    uint16_t* Y;
+    float tau;
+    void* ws;           // split-K partials (after the counters)
+    unsigned* counters; // split-K arrival counters, one per (band, token block)
+    unsigned* status;
+};

@@ -1,0 +1,257 @@
+// us_encode.cu -- dense -> bitmap tiles on the GPU.
+//
+// Format: IE-BME of "UnionSparse: An Index-Efficient Sparsity Framework for
+// Low-Bit Sparse LLM Inference on Edge", section V-A (Union Bitmaps, Union
+// Value Offsets o_t = sum of earlier payload lengths, Compressed Values
+// CV[o_t + rho]) with one area (Q = 1), scanned row-major or column-major
+// (Tiled-CBC, "Unified Static-Dynamic Pruning for Efficient LLM Inference"
+// section 4.1), each tile's run padded to 16 bytes (same page, 4.2.3).
+//
+// Three launches:
+//   1. count: one CTA per tile builds the tile's 64-bit words with warp
+//      ballots over the scan positions and stores P_t (its popcount);
+//   2. scan:  one CTA turns roundup(P_t, E) into the exclusive prefix tile_off;
+//   3. pack:  one CTA per tile ranks its set positions (word prefix +
+//      masked popcount), compacts them in shared memory and writes the run,
+//      zero padding included, with 16-byte stores.
+#include "us_common.cuh"
+#include "us_internal.h"
+
+namespace {
+
+constexpr int kEncThreads = 256;
+
+template <int ELEM>
+__device__ __forceinline__ bool is_nonzero(const void* W, int64_t idx) {
+    if (ELEM == US_F16) return (reinterpret_cast<const uint16_t*>(W)[idx] & 0x7FFFu) != 0;
+    return reinterpret_cast<const int8_t*>(W)[idx] != 0;
+}
+
+// position p of a TM x TK tile -> offset (i*ldw + j) from the tile's corner
+__device__ __forceinline__ int64_t pos_offset(int order, int TM, int TK, int p, int64_t ldw) {
+    int i, j;
+    if (order == US_ORDER_ROW) { i = p / TK; j = p - i * TK; }
+    else                       { j = p / TM; i = p - j * TM; }
+    return (int64_t)i * ldw + j;
+}
+
+template <int ELEM>
+__global__ void __launch_bounds__(kEncThreads)
+enc_count_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK, int order,
+                 uint64_t* __restrict__ bitmap, uint32_t* __restrict__ counts, unsigned* status) {
+    const int t = blockIdx.x;
+    const int tm = t / nTK, tk = t - tm * nTK;
+    const int64_t corner = (int64_t)tm * TM * ldw + (int64_t)tk * TK;
+    const int nw = TM * TK / 64;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int warp_sum[kEncThreads / 32];
+    int my = 0;
+    for (int w = warp; w < nw; w += kEncThreads / 32) {
+        const int p0 = w * 64 + lane, p1 = p0 + 32;
+        const int64_t i0 = corner + pos_offset(order, TM, TK, p0, ldw);
+        const int64_t i1 = corner + pos_offset(order, TM, TK, p1, ldw);
+        const bool nz0 = is_nonzero<ELEM>(W, i0), nz1 = is_nonzero<ELEM>(W, i1);
+        if (ELEM == US_I4) {
+            const int8_t a = reinterpret_cast<const int8_t*>(W)[i0];
+            const int8_t b = reinterpret_cast<const int8_t*>(W)[i1];
+            if (a < -8 || a > 7 || b < -8 || b > 7) us::set_status(status, US_ERR_INVALID_ARG);
+        }
+        const uint32_t lo = __ballot_sync(0xffffffffu, nz0);
+        const uint32_t hi = __ballot_sync(0xffffffffu, nz1);
+        if (lane == 0) {
+            bitmap[(int64_t)t * nw + w] = (uint64_t)lo | ((uint64_t)hi << 32);
+            my += __popc(lo) + __popc(hi);
+        }
+    }
+    if (lane == 0) warp_sum[warp] = my;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int i = 0; i < kEncThreads / 32; ++i) s += warp_sum[i];
+        counts[t] = (uint32_t)s;
+    }
+}
+
+// Exclusive scan of the padded run lengths; one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024)
+enc_scan_kernel(const uint32_t* __restrict__ counts, int64_t nT, int E, uint32_t* __restrict__ tile_off,
+                unsigned* status) {
+    __shared__ uint32_t wsum[32];
+    __shared__ uint64_t carry_s;
+    if (threadIdx.x == 0) { carry_s = 0; tile_off[0] = 0; }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t base = 0; base < nT; base += 1024) {
+        const int64_t t = base + threadIdx.x;
+        uint32_t v = 0;
+        if (t < nT) v = (counts[t] + (uint32_t)E - 1u) / (uint32_t)E * (uint32_t)E;
+        uint32_t incl = v;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += o;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t s = wsum[lane];
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                uint32_t o = __shfl_up_sync(0xffffffffu, s, d);
+                if (lane >= d) s += o;
+            }
+            wsum[lane] = s;   // inclusive over warps
+        }
+        __syncthreads();
+        const uint64_t carry = carry_s;
+        const uint64_t prefix = carry + (warp > 0 ? wsum[warp - 1] : 0u) + incl;
+        if (t < nT) {
+            if (prefix >= (1ull << 32)) us::set_status(status, US_ERR_TOO_LARGE);
+            tile_off[t + 1] = (uint32_t)prefix;
+        }
+        __syncthreads();
+        if (threadIdx.x == 1023) carry_s = prefix;
+        __syncthreads();
+    }
+}
+
+template <int ELEM>
+__global__ void __launch_bounds__(kEncThreads)
+enc_pack_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK, int order,
+                const uint64_t* __restrict__ bitmap, const uint32_t* __restrict__ tile_off,
+                uint8_t* __restrict__ values, uint64_t values_cap, unsigned* status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int t = blockIdx.x;
+    const int tm = t / nTK, tk = t - tm * nTK;
+    const int64_t corner = (int64_t)tm * TM * ldw + (int64_t)tk * TK;
+    const int nw = TM * TK / 64;
+    const int npos = TM * TK;
+    constexpr int EB = (ELEM == US_F16) ? 2 : 1;       // bytes per compacted element in smem
+    uint32_t* wpre = reinterpret_cast<uint32_t*>(smem);               // nw word prefixes
+    uint8_t* cbuf = smem + ((nw * 4 + 15) & ~15);                     // compacted elements
+    __shared__ uint32_t warp_tot[kEncThreads / 32];
+
+    const uint64_t o0 = tile_off[t], o1 = tile_off[t + 1];
+    const int bits = (ELEM == US_F16) ? 16 : 4;
+    if (o1 < o0 || o1 * bits > values_cap * 8) {
+        if (threadIdx.x == 0) us::set_status(status, US_ERR_WORKSPACE);
+        return;
+    }
+    const uint64_t* words = bitmap + (int64_t)t * nw;
+
+    // exclusive prefix of the word popcounts (nw <= 512 = 2 per thread)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t c0 = 0, c1 = 0;
+    const int w0 = 2 * threadIdx.x, w1 = w0 + 1;
+    if (w0 < nw) c0 = __popcll(words[w0]);
+    if (w1 < nw) c1 = __popcll(words[w1]);
+    uint32_t incl = c0 + c1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int i = 0; i < warp; ++i) before += warp_tot[i];
+    const uint32_t excl = before + incl - (c0 + c1);
+    if (w0 < nw) wpre[w0] = excl;
+    if (w1 < nw) wpre[w1] = excl + c0;
+    uint32_t P = 0;
+    for (int i = 0; i < kEncThreads / 32; ++i) P += warp_tot[i];
+    __syncthreads();
+    if (P > o1 - o0) {                       // cannot happen after enc_scan; guard anyway
+        if (threadIdx.x == 0) us::set_status(status, US_ERR_CORRUPT);
+        return;
+    }
+
+    // compact the set positions by rank
+    for (int p = threadIdx.x; p < npos; p += kEncThreads) {
+        const int w = p >> 6, b = p & 63;
+        const uint64_t word = words[w];
+        if ((word >> b) & 1ull) {
+            const uint32_t rank = wpre[w] + __popcll(word & ((1ull << b) - 1ull));
+            const int64_t idx = corner + pos_offset(order, TM, TK, p, ldw);
+            if (ELEM == US_F16)
+                reinterpret_cast<uint16_t*>(cbuf)[rank] = reinterpret_cast<const uint16_t*>(W)[idx];
+            else
+                cbuf[rank] = (uint8_t)reinterpret_cast<const int8_t*>(W)[idx] & 0x0Fu;
+        }
+    }
+    __syncthreads();
+
+    // write the run [o0, o1) with zero padding, 16 bytes per thread-step
+    const uint64_t run_bytes = (o1 - o0) * bits / 8;
+    uint8_t* dst = values + o0 * bits / 8;
+    for (uint64_t q = (uint64_t)threadIdx.x * 16; q < run_bytes; q += (uint64_t)kEncThreads * 16) {
+        uint32_t v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int bsub = 0; bsub < 4; ++bsub) {
+                const uint64_t byte = q + r * 4 + bsub;
+                uint32_t by = 0;
+                if (ELEM == US_F16) {
+                    const uint64_t e = byte >> 1;
+                    if (e < P) {
+                        const uint16_t h = reinterpret_cast<const uint16_t*>(cbuf)[e];
+                        by = (byte & 1) ? (h >> 8) : (h & 0xFF);
+                    }
+                } else {
+                    const uint64_t e0 = byte * 2, e1 = e0 + 1;
+                    if (e0 < P) by |= cbuf[e0];
+                    if (e1 < P) by |= (uint32_t)cbuf[e1] << 4;
+                }
+                word |= (by & 0xFFu) << (8 * bsub);
+            }
+            v[r] = word;
+        }
+        *reinterpret_cast<uint4*>(dst + q) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+    (void)EB;
+}
+
+}  // namespace
+
+namespace us {
+
+size_t encode_pack_smem(int TM, int TK, int elem) {
+    const int nw = TM * TK / 64;
+    return (size_t)((nw * 4 + 15) & ~15) + (size_t)TM * TK * (elem == US_F16 ? 2 : 1);
+}
+
+us_status launch_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem, int order,
+                        uint64_t* bitmap, uint32_t* tile_off, void* values, size_t values_cap,
+                        uint32_t* counts, unsigned* status, cudaStream_t st) {
+    const int nTM = M / TM, nTK = K / TK;
+    const int64_t nT = (int64_t)nTM * nTK;
+    const size_t smem = encode_pack_smem(TM, TK, elem);
+    if (elem == US_F16) {
+        enc_count_kernel<US_F16><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, TK, nTK, order, bitmap, counts,
+                                                                      status);
+    } else {
+        enc_count_kernel<US_I4><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, TK, nTK, order, bitmap, counts,
+                                                                     status);
+    }
+    if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
+    enc_scan_kernel<<<1, 1024, 0, st>>>(counts, nT, elem == US_F16 ? 8 : 32, tile_off, status);
+    if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
+    if (elem == US_F16) {
+        if (cudaFuncSetAttribute(enc_pack_kernel<US_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return US_ERR_CUDA;
+        enc_pack_kernel<US_F16><<<(unsigned)nT, kEncThreads, smem, st>>>(
+            W, ldw, TM, TK, nTK, order, bitmap, tile_off, (uint8_t*)values, values_cap, status);
+    } else {
+        if (cudaFuncSetAttribute(enc_pack_kernel<US_I4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return US_ERR_CUDA;
+        enc_pack_kernel<US_I4><<<(unsigned)nT, kEncThreads, smem, st>>>(
+            W, ldw, TM, TK, nTK, order, bitmap, tile_off, (uint8_t*)values, values_cap, status);
+    }
+    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
+}
+
+}  // namespace us

@@ -1,0 +1,38 @@
+// us_internal.h -- host-side declarations shared by the libus translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/us.h"
+
+struct UsKParams;
+
+namespace us {
+
+// encoder (us_encode.cu)
+size_t encode_pack_smem(int TM, int TK, int elem);
+us_status launch_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem, int order,
+                        uint64_t* bitmap, uint32_t* tile_off, void* values, size_t values_cap,
+                        uint32_t* counts, unsigned* status, cudaStream_t st);
+
+// generic CUDA-core SpMM (us_spmm.cu); p.split / p.tok_block already chosen
+us_status launch_spmm_generic(const UsKParams& p, int elem, cudaStream_t st);
+// bytes of partials + counters the generic kernel needs for this launch shape
+size_t spmm_generic_ws(int M, int TM, int N, int split, int tok_block);
+int spmm_generic_tok_block(int N);
+
+// W4A4 CUDA-core decode kernel for small N (us_w4a4.cu)
+bool w4a4_fast_supported(int TM, int TK, int N);
+us_status launch_w4a4_fast(const UsKParams& p, cudaStream_t st);
+size_t w4a4_fast_ws(int M, int TM, int N, int split);
+
+// spMspV (us_spmspv.cu)
+us_status launch_spmspv(const UsKParams& p, cudaStream_t st);
+size_t spmspv_ws(int M, int TM, int split);
+
+// device properties of the current device (cached)
+int num_sms();
+
+}  // namespace us

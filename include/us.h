@@ -1,0 +1,173 @@
+/*
+ * us.h -- C ABI of libus, a GB300 (sm_103a) library for unstructured-sparse
+ * weight matrices stored as bitmap tiles, multiplied by tall-skinny
+ * activations:  Y = W . X.
+ *
+ * Sources.  The stored format is the Index-Efficient Bitmap Encoding of
+ * "UnionSparse: An Index-Efficient Sparsity Framework for Low-Bit Sparse LLM
+ * Inference on Edge" (section V-A: Union Bitmaps, Union Value Offsets,
+ * Compressed Values, Fig. 7) with one area per tile (Q = 1), in its row-major
+ * scan or in the column-major tile scan of the Tiled-CBC format of "Unified
+ * Static-Dynamic Pruning for Efficient LLM Inference" (section 4.1), with the
+ * 16-byte value padding of that page's section 4.2.3.  The products follow
+ * UnionSparse Fig. 2 (INT4 x INT4 -> INT32 -> dequantised FP16) and SPDP
+ * section 2 / 4.2 (static mask W (.) M, dynamic mask W (.) M(x), spMspV).
+ *
+ * ---------------------------------------------------------------- format --
+ * Parameters: M x K weights, tiles TM x TK with TM in {64,128,256},
+ * TK in {16,32,64,128}, M % TM == 0, K % TK == 0, M*K < 2^32.
+ * nTM = M/TM, nTK = K/TK, nT = nTM*nTK; tile t = tm*nTK + tk covers rows
+ * [tm*TM, tm*TM+TM) and columns [tk*TK, tk*TK+TK).
+ * Scan position p inside a tile:  US_ORDER_ROW  p = i*TK + j
+ *                                 US_ORDER_COL  p = j*TM + i
+ * bitmap:   uint64[nT * TM*TK/64]; tile t owns words [t*TM*TK/64, ...);
+ *           bit (p % 64) of word p/64 is set iff W[tm*TM+i][tk*TK+j] != 0
+ *           (fp16: +0 and -0 are zero; NaN is stored).  Earlier position =
+ *           less significant bit.
+ * tile_off: uint32[nT+1], in ELEMENTS; tile_off[0] = 0,
+ *           tile_off[t+1] = tile_off[t] + roundup(P_t, E) where P_t is the
+ *           popcount of tile t's words and E = 8 (fp16) or 32 (int4), i.e.
+ *           every tile's run is padded with zeros to 16 bytes.
+ * values:   the nonzeros of tile t in increasing p, starting at element
+ *           tile_off[t] (o_t + rho, rho = set positions scanned before p).
+ *           fp16: 2 bytes little-endian.  int4: element e in byte e>>1,
+ *           even e in the low nibble, two's complement in [-8, 7].
+ *
+ * ------------------------------------------------------------ conventions --
+ * All pointers are DEVICE pointers unless marked "host".  Every device
+ * pointer must be 16-byte aligned.  The caller allocates and owns every
+ * buffer; the library never allocates, never synchronises the device (except
+ * us_get_last_device_status) and never throws: every entry point returns a
+ * us_status.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ * Argument errors are detected on the host before anything is enqueued.
+ * Kernels guard every access with the offsets they read; a run that does not
+ * fit its tile, or a tile_off beyond values_bytes, is not read: the tile is
+ * treated as empty and US_ERR_CORRUPT is recorded in the device status word
+ * (us_get_last_device_status).
+ *
+ * Workspace: query its size with us_workspace_bytes / us_encode_sizes.  It
+ * must be zero-filled once before its first use; every call leaves it
+ * zero-filled again where the next call needs zeros (split-K arrival
+ * counters).  One workspace serves one call at a time: two calls in flight
+ * at once on different streams must not share it.
+ */
+#ifndef US_H_
+#define US_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    US_OK = 0,
+    US_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer, bad enum */
+    US_ERR_UNSUPPORTED = 2,   /* valid format, but no kernel for this combination */
+    US_ERR_TOO_LARGE = 3,     /* M*K >= 2^32 or another size limit */
+    US_ERR_WORKSPACE = 4,     /* workspace (or values capacity) too small */
+    US_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    US_ERR_TIMEOUT = 6,       /* a device-side wait hit its iteration limit */
+    US_ERR_CORRUPT = 7        /* inconsistent format detected (host or device) */
+} us_status;
+
+typedef enum { US_F16 = 0, US_I4 = 1 } us_elem;
+typedef enum { US_ORDER_ROW = 0, US_ORDER_COL = 1 } us_order;
+typedef enum {
+    US_OP_ENCODE = 0,
+    US_OP_SPMM_W4A4 = 1,
+    US_OP_SPMM_F16 = 2,
+    US_OP_SPMSPV_F16 = 3
+} us_op;
+
+/* A view of an encoded matrix.  Plain data, copied by value into kernel
+ * parameters; the caller owns the three arrays.  values_bytes is the
+ * readable length of `values` (at least tile_off[nT] * bits / 8). */
+typedef struct {
+    int32_t M, K, TM, TK;
+    int32_t elem;             /* us_elem */
+    int32_t order;            /* us_order */
+    const uint64_t* bitmap;
+    const uint32_t* tile_off;
+    const void* values;
+    uint64_t values_bytes;
+} us_bitmap;
+
+/* Sizes of the encoder's outputs and workspace (all host out-params).
+ * values_cap_bytes is the worst case (every position nonzero). */
+us_status us_encode_sizes(int M, int K, int TM, int TK, us_elem elem,
+                          size_t* bitmap_bytes, size_t* tile_off_bytes,
+                          size_t* values_cap_bytes, size_t* ws_bytes);
+
+/* Dense -> bitmap tiles on the GPU (UnionSparse V-A, Q = 1; SPDP 4.1 for
+ * US_ORDER_COL).  W: M x K row-major with leading dimension ldw (elements):
+ * fp16 bit patterns (US_F16) or int8 codes in [-8, 7] (US_I4).  Writes
+ * bitmap, tile_off (nT+1 entries; tile_off[nT] is the used length in
+ * elements) and values (capacity values_cap bytes).  An int4 code outside
+ * [-8, 7] records US_ERR_INVALID_ARG and a run beyond values_cap records
+ * US_ERR_WORKSPACE in the device status word (that tile's run is not
+ * written).  Output bytes are identical to those of a sequential encoder. */
+us_status us_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK,
+                    us_elem elem, us_order order, uint64_t* bitmap,
+                    uint32_t* tile_off, void* values, size_t values_cap,
+                    void* ws, size_t ws_bytes, void* stream);
+
+/* W4A4 SpMM (UnionSparse Fig. 2):  Yacc[n][m] = sum_k Wq[m][k] * Xq[n][k]
+ * (exact int32) and, if Y != NULL,
+ * Y[n][m] = fp16_rn((fp32(Yacc) * s_w[m]) * s_x[n]).
+ * W: elem US_I4, order US_ORDER_ROW.  Xq: N x K int4 codes, token-major,
+ * packed like `values` (element n*K + k); requires K % 32 == 0.
+ * s_w: M fp16 bit patterns, s_x: N fp16.  Yacc: N x M int32, Y: N x M fp16.
+ * 1 <= N <= 2048.  split_k: 0 = automatic, else K tiles are split into that
+ * many slices (1..nTK).  Results do not depend on split_k. */
+us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_w,
+                       const uint16_t* s_x, int N, int32_t* Yacc, uint16_t* Y,
+                       void* ws, size_t ws_bytes, int split_k, void* stream);
+
+/* fp16 SpMM:  Y[n][m] = fp16(sum_k W[m][k] * X[n][k]) with fp32 accumulation
+ * (tensor cores for large N).  W: elem US_F16, order US_ORDER_ROW.
+ * X: N x K fp16 token-major, Y: N x M fp16, 1 <= N <= 2048.  split_k as above;
+ * the fp32 partial sums are reduced in fixed slice order, so repeated calls
+ * give bitwise identical results. */
+us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
+                      void* ws, size_t ws_bytes, int split_k, void* stream);
+
+/* fp16 spMspV (SPDP section 4.2):  y[m] = fp16(sum over k with |x_k| > tau of
+ * W[m][k] * x[k]), fp32 accumulation.  Columns whose activation fails the
+ * test are skipped: their bitmap words are read, their values are not.
+ * W: elem US_F16, order US_ORDER_COL.  x: K fp16, y: M fp16, tau >= 0. */
+us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes for `op` on W with N tokens and the given split_k
+ * (0 = the automatic choice).  For US_OP_ENCODE only W->M, K, TM, TK are read. */
+us_status us_workspace_bytes(us_op op, const us_bitmap* W, int N, int split_k, size_t* bytes);
+
+/* The split_k the automatic rule picks for (op, W, N) on the current device:
+ * the smallest of {1,2,4,8,16} whose grid fills every SM, while each slice
+ * keeps at least 4 K tiles (split-K rule of "Realizable N:M Sparse
+ * Transformer Inference via Search-Kernel Co-Design", section 4.3). */
+us_status us_pick_split_k(us_op op, const us_bitmap* W, int N, int* split_k);
+
+/* Host-side check of an encoded matrix.  W's three pointers are HOST
+ * pointers here.  Returns US_OK, US_ERR_INVALID_ARG (bad parameters) or
+ * US_ERR_CORRUPT (offsets not monotone, a run shorter than its popcount or
+ * not padded to 16 bytes, nonzero padding, values_bytes too small). */
+us_status us_validate(const us_bitmap* W);
+
+/* Waits for `stream`, then returns and clears the device status word that
+ * kernels set on device-side errors (US_ERR_TIMEOUT, US_ERR_CORRUPT,
+ * US_ERR_INVALID_ARG, US_ERR_WORKSPACE; US_OK if none). */
+us_status us_get_last_device_status(void* stream);
+
+/* Static description of a status code. */
+const char* us_status_string(us_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int us_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* US_H_ */

@@ -1,0 +1,335 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Bars: encoder bytes, int32 accumulators and the W4A4 fp16 epilogue bit-exact;
+fp16 outputs (fp32 accumulation) within relative L2 <= 1e-3 and max-abs <= 2e-2
+of the fp64 oracle.  Shapes span several tiles, uneven split-K slices and ragged
+token blocks; edge cases cover empty and full tiles, single nonzeros, all-zero
+matrices and offsets that a kernel must refuse to follow.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bitmap_encoded_unstructured_ie_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+F16, I4, ROW, COL = 0, 1, 0, 1
+REL_L2, MAX_ABS = 1e-3, 2e-2
+
+
+@pytest.fixture(scope="module")
+def us():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from bitmap_encoded_unstructured_ie_gb300 import build, binding
+    build.build()
+    binding.load()
+    return binding
+
+
+@pytest.fixture(scope="module")
+def orc():
+    from oracle import oracle as o
+    o._load()
+    return o
+
+
+def rand_i4(rng, M, K, density):
+    q = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
+    q[rng.random((M, K)) >= density] = 0
+    return q
+
+
+def rand_f16(rng, M, K, density):
+    w = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
+    w[rng.random((M, K)) >= density] = 0
+    return w
+
+
+def check_f16(y_gpu: np.ndarray, exact: np.ndarray, what=""):
+    y = y_gpu.astype(np.float64)
+    err = y - exact
+    denom = max(np.linalg.norm(exact), 1e-30)
+    rel = np.linalg.norm(err) / denom
+    mx = np.abs(err).max() if err.size else 0.0
+    assert rel <= REL_L2 and mx <= MAX_ABS, f"{what}: rel L2 {rel:.3e}, max abs {mx:.3e}"
+
+
+def encode_gpu(us, W: np.ndarray, TM, TK, elem, order):
+    Wt = torch.from_numpy(W.view(np.int16) if elem == F16 else W).cuda()
+    E = us.us_encode(Wt, TM, TK, elem, order)
+    torch.cuda.synchronize()
+    assert us.us_get_last_device_status() == us.US_OK
+    return E
+
+
+def gpu_arrays(E):
+    bm = E.bitmap.cpu().numpy().view(np.uint64)
+    off = E.tile_off.cpu().numpy().view(np.uint32)
+    vals = E.values.cpu().numpy()[: E.values_bytes]
+    return bm, off, vals
+
+
+# ------------------------------------------------------------------ encode --
+ENC_SHAPES = [(256, 512, 64, 64), (192, 320, 64, 16), (512, 256, 128, 32), (256, 256, 256, 128),
+              (128, 384, 64, 128), (256, 64, 256, 16)]
+
+
+@pytest.mark.parametrize("shape", ENC_SHAPES)
+@pytest.mark.parametrize("elem", [F16, I4])
+@pytest.mark.parametrize("order", [ROW, COL])
+def test_encode_bytes_match_oracle(us, orc, shape, elem, order):
+    M, K, TM, TK = shape
+    rng = np.random.default_rng(M + K + TM + TK + 10 * elem + order)
+    for density in (0.0, 0.004, 0.5, 1.0):
+        W = rand_f16(rng, M, K, density) if elem == F16 else rand_i4(rng, M, K, density)
+        E = encode_gpu(us, W, TM, TK, elem, order)
+        bm, off, vals = gpu_arrays(E)
+        obm, ooff, ovals = orc.encode(W, TM, TK, elem, order)
+        assert np.array_equal(bm, obm)
+        assert np.array_equal(off, ooff)
+        assert np.array_equal(vals, ovals)
+
+
+def test_encode_strided_input_and_signed_zero(us, orc):
+    rng = np.random.default_rng(3)
+    big = rand_f16(rng, 128, 512, 0.5)
+    big[5, 9] = np.float16(-0.0)
+    Wt = torch.from_numpy(big.view(np.int16)).cuda()[:, 64:320]
+    E = us.us_encode(Wt, 64, 64, F16, ROW)
+    bm, off, vals = gpu_arrays(E)
+    obm, ooff, ovals = orc.encode(np.ascontiguousarray(big[:, 64:320]), 64, 64, F16, ROW)
+    assert np.array_equal(bm, obm) and np.array_equal(off, ooff) and np.array_equal(vals, ovals)
+
+
+def test_encode_reports_out_of_range_codes(us):
+    W = torch.zeros(64, 64, dtype=torch.int8, device="cuda")
+    W[3, 4] = 9
+    us.us_encode(W, 64, 64, I4, ROW)
+    assert us.us_get_last_device_status() == us.US_ERR_INVALID_ARG
+    assert us.us_get_last_device_status() == us.US_OK        # cleared by the read
+
+
+# -------------------------------------------------------------------- W4A4 --
+def run_w4a4(us, E, Xq_packed, s_w, s_x, N, split_k=0, want_y=True):
+    dev = "cuda"
+    X = torch.from_numpy(Xq_packed).to(dev)
+    sw = torch.from_numpy(s_w.view(np.int16)).to(dev)
+    sx = torch.from_numpy(s_x.view(np.int16)).to(dev)
+    Yacc = torch.empty(N, E.M, dtype=torch.int32, device=dev)
+    Y = torch.empty(N, E.M, dtype=torch.int16, device=dev) if want_y else None
+    ws = us.workspace(us.US_OP_SPMM_W4A4, E, N, split_k)
+    us.us_spmm_w4a4(E, X, sw, sx, N, Yacc, Y, ws, split_k)
+    torch.cuda.synchronize()
+    assert us.us_get_last_device_status() == us.US_OK
+    y = Y.cpu().numpy().view(np.float16) if want_y else None
+    return Yacc.cpu().numpy(), y
+
+
+W4A4_CASES = [
+    # M, K, TM, TK, N, density, split_k
+    (256, 512, 64, 64, 1, 0.5, 0),
+    (256, 512, 64, 64, 8, 0.5, 0),
+    (256, 512, 64, 64, 16, 0.3, 0),
+    (320, 640, 64, 64, 3, 0.7, 3),
+    (256, 512, 64, 64, 33, 0.5, 2),
+    (512, 384, 128, 32, 5, 0.5, 0),
+    (256, 256, 256, 128, 2, 0.5, 0),
+    (192, 320, 64, 16, 7, 0.5, 4),
+    (128, 1024, 64, 64, 1, 1.0, 16),
+    (128, 512, 64, 64, 64, 0.05, 0),
+]
+
+
+@pytest.mark.parametrize("case", W4A4_CASES)
+def test_w4a4_matches_oracle(us, orc, case):
+    M, K, TM, TK, N, dens, split = case
+    rng = np.random.default_rng(sum(case[:5]))
+    W = rand_i4(rng, M, K, dens)
+    Xq = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
+    s_x = (rng.random(N) * 0.5 + 0.05).astype(np.float16)
+    E = encode_gpu(us, W, TM, TK, I4, ROW)
+    acc, y = run_w4a4(us, E, wl.pack_int4(Xq), s_w, s_x, N, split)
+    oacc, oy = orc.spmm_w4a4(W, Xq, s_w, s_x)
+    assert np.array_equal(acc, oacc)
+    assert np.array_equal(y.view(np.uint16), oy.view(np.uint16))
+
+
+def test_w4a4_extreme_values_exact(us, orc):
+    """All weights and activations -8: the largest accumulators (64*K)."""
+    M, K = 128, 2048
+    W = np.full((M, K), -8, np.int8)
+    W[::3, ::5] = 7
+    X = np.full((4, K), -8, np.int8)
+    one = np.ones(M, np.float16)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    acc, _ = run_w4a4(us, E, wl.pack_int4(X), one, np.ones(4, np.float16), 4, want_y=False)
+    oacc, _ = orc.spmm_w4a4(W, X, one, np.ones(4, np.float16))
+    assert np.array_equal(acc, oacc)
+
+
+def test_w4a4_edge_matrices(us, orc):
+    M, K, N = 128, 256, 3
+    rng = np.random.default_rng(0)
+    X = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    s = np.ones(M, np.float16)
+    for W in (np.zeros((M, K), np.int8), np.eye(M, K, dtype=np.int8) * 3):
+        W = W.copy()
+        E = encode_gpu(us, W, 64, 64, I4, ROW)
+        acc, _ = run_w4a4(us, E, wl.pack_int4(X), s, np.ones(N, np.float16), N)
+        oacc, _ = orc.spmm_w4a4(W, X, s, np.ones(N, np.float16))
+        assert np.array_equal(acc, oacc)
+    W = np.zeros((M, K), np.int8)
+    W[77, 200] = -3                                     # one nonzero, everything else empty
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    acc, _ = run_w4a4(us, E, wl.pack_int4(X), s, np.ones(N, np.float16), N)
+    assert np.array_equal(acc[:, 77], -3 * X[:, 200].astype(np.int32)) and np.count_nonzero(acc[:, :77]) == 0
+
+
+def test_corrupt_offsets_are_refused_on_device(us, orc):
+    """Offsets that point outside the run are caught by the kernel's own checks:
+    the tile is treated as empty and US_ERR_CORRUPT is reported."""
+    rng = np.random.default_rng(1)
+    W = rand_i4(rng, 128, 256, 0.5)
+    bm, off, vals = orc.encode(W, 64, 64, I4, ROW)
+    bad = off.copy()
+    bad[2] = bad[1] + 16                                # misaligned, shorter than the popcount
+    E = us.from_host(bm, bad, vals, 128, 256, 64, 64, I4, ROW)
+    X = rng.integers(-8, 8, size=(1, 256)).astype(np.int8)
+    Xt = torch.from_numpy(wl.pack_int4(X)).cuda()
+    Yacc = torch.empty(1, 128, dtype=torch.int32, device="cuda")
+    ws = us.workspace(us.US_OP_SPMM_W4A4, E, 1, 1)
+    us.us_spmm_w4a4(E, Xt, None, None, 1, Yacc, None, ws, 1)
+    assert us.us_get_last_device_status() == us.US_ERR_CORRUPT
+
+
+def test_workspace_too_small_is_a_host_error(us, orc):
+    rng = np.random.default_rng(2)
+    W = rand_i4(rng, 256, 512, 0.5)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    X = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    Yacc = torch.empty(1, 256, dtype=torch.int32, device="cuda")
+    need = us.us_workspace_bytes(us.US_OP_SPMM_W4A4, E, 1, 4)
+    ws = torch.zeros(max(need - 16, 16), dtype=torch.uint8, device="cuda")
+    with pytest.raises(us.UsError) as ei:
+        us.us_spmm_w4a4(E, X, None, None, 1, Yacc, None, ws, 4)
+    assert ei.value.code == us.US_ERR_WORKSPACE
+
+
+# -------------------------------------------------------------------- fp16 --
+def run_f16(us, E, X: np.ndarray, split_k=0):
+    N = X.shape[0]
+    Xt = torch.from_numpy(X.view(np.int16)).cuda()
+    Y = torch.empty(N, E.M, dtype=torch.int16, device="cuda")
+    ws = us.workspace(us.US_OP_SPMM_F16, E, N, split_k)
+    us.us_spmm_f16(E, Xt, N, Y, ws, split_k)
+    torch.cuda.synchronize()
+    assert us.us_get_last_device_status() == us.US_OK
+    return Y.cpu().numpy().view(np.float16)
+
+
+F16_CASES = [
+    (256, 512, 64, 64, 1, 0.5, 0),
+    (256, 512, 64, 64, 5, 0.5, 3),
+    (512, 256, 128, 32, 32, 0.4, 0),
+    (256, 512, 256, 16, 70, 0.5, 2),
+    (128, 256, 128, 128, 2, 1.0, 0),
+]
+
+
+@pytest.mark.parametrize("case", F16_CASES)
+def test_f16_matches_oracle(us, orc, case):
+    M, K, TM, TK, N, dens, split = case
+    rng = np.random.default_rng(sum(case[:5]) + 1)
+    W = rand_f16(rng, M, K, dens)
+    X = rng.standard_normal((N, K)).astype(np.float16)
+    E = encode_gpu(us, W, TM, TK, F16, ROW)
+    y = run_f16(us, E, X, split)
+    n_idx, m_idx = np.meshgrid(np.arange(N), np.arange(M), indexing="ij")
+    _, exact = orc.spmm_f16_at(W, X, n_idx.reshape(-1), m_idx.reshape(-1))
+    check_f16(y.reshape(-1), exact, f"fp16 {case}")
+
+
+def test_f16_split_k_is_deterministic(us):
+    rng = np.random.default_rng(4)
+    W = rand_f16(rng, 256, 1024, 0.5)
+    X = rng.standard_normal((3, 1024)).astype(np.float16)
+    E = encode_gpu(us, W, 64, 64, F16, ROW)
+    for split in (1, 2, 5, 16):
+        a = run_f16(us, E, X, split)
+        b = run_f16(us, E, X, split)
+        assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+
+
+# ------------------------------------------------------------------ spMspV --
+def run_spmspv(us, E, x: np.ndarray, tau: float):
+    xt = torch.from_numpy(x.view(np.int16)).cuda()
+    y = torch.empty(E.M, dtype=torch.int16, device="cuda")
+    ws = us.workspace(us.US_OP_SPMSPV_F16, E, 1)
+    us.us_spmspv_f16(E, xt, tau, y, ws)
+    torch.cuda.synchronize()
+    assert us.us_get_last_device_status() == us.US_OK
+    return y.cpu().numpy().view(np.float16)
+
+
+@pytest.mark.parametrize("TM,TK", [(64, 64), (256, 16), (128, 32), (64, 128)])
+@pytest.mark.parametrize("zero_frac,tau", [(0.5, 0.0), (0.9, 0.0), (0.0, 0.7)])
+def test_spmspv_matches_oracle(us, orc, TM, TK, zero_frac, tau):
+    M, K = 512, 1024
+    d = wl.spmspv(M, K, 0.5, zero_frac, seed=TM + TK)
+    W, x = d["W"], d["x"]
+    if zero_frac == 0.0:
+        x = np.random.default_rng(9).standard_normal(K).astype(np.float16)   # both signs
+    E = encode_gpu(us, W, TM, TK, F16, COL)
+    y = run_spmspv(us, E, x, tau)
+    _, exact = orc.spmspv_f16(W, x, tau)
+    check_f16(y, exact, f"spmspv TM={TM} TK={TK} tau={tau}")
+
+
+# --------------------------------------------------------- full-size shapes --
+@pytest.mark.parametrize("s", [0.3, 0.5, 0.7])
+def test_w4a4_4096_full(us, orc, s):
+    d = wl.w4a4(4096, 4096, 16, s, seed=0)
+    E = encode_gpu(us, d["Wq"], 64, 64, I4, ROW)
+    for N in (1, 8, 16):
+        acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N)
+        oacc, oy = orc.spmm_w4a4(d["Wq"], d["Xq"][:N], d["s_w"], d["s_x"][:N], nthreads=orc.max_threads())
+        assert np.array_equal(acc, oacc)
+        assert np.array_equal(y.view(np.uint16), oy.view(np.uint16))
+
+
+@pytest.mark.parametrize("M,K", [(11008, 4096), (4096, 11008)])
+def test_w4a4_ffn_full(us, orc, M, K):
+    d = wl.w4a4(M, K, 32, 0.5, seed=0, rows="beta")
+    E = encode_gpu(us, d["Wq"], 64, 64, I4, ROW)
+    for N in (1, 4, 16, 32):
+        acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N)
+        rng = np.random.default_rng(N)
+        n_idx = rng.integers(0, N, 3000)
+        m_idx = rng.integers(0, M, 3000)
+        oacc, oy = orc.spmm_w4a4_at(d["Wq"], d["Xq"][:N], d["s_w"], d["s_x"][:N], n_idx, m_idx)
+        assert np.array_equal(acc[n_idx, m_idx], oacc)
+        assert np.array_equal(y[n_idx, m_idx].view(np.uint16), oy.view(np.uint16))
+
+
+@pytest.mark.parametrize("N", [256, 2048])
+def test_f16_prefill_sampled(us, orc, N):
+    d = wl.f16_spmm(4096, 4096, N, 0.6, seed=0)
+    E = encode_gpu(us, d["W"], 64, 64, F16, ROW)
+    y = run_f16(us, E, d["X"])
+    rng = np.random.default_rng(N)
+    n_idx = rng.integers(0, N, 4000)
+    m_idx = rng.integers(0, 4096, 4000)
+    _, exact = orc.spmm_f16_at(d["W"], d["X"], n_idx, m_idx)
+    check_f16(y[n_idx, m_idx], exact, f"prefill N={N}")
+
+
+@pytest.mark.parametrize("zero_frac", [0.5, 0.7, 0.9])
+def test_spmspv_14336_full(us, orc, zero_frac):
+    d = wl.spmspv(14336, 4096, 0.5, zero_frac, seed=0)
+    E = encode_gpu(us, d["W"], 64, 64, F16, COL)
+    y = run_spmspv(us, E, d["x"], 0.0)
+    _, exact = orc.spmspv_f16(d["W"], d["x"], 0.0, nthreads=orc.max_threads())
+    check_f16(y, exact, f"spmspv 14336 zeros={zero_frac}")
