@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Benchmark: bitmap SpMM GB/s (% of HBM peak) and effective TOPS at N = 1/8/16.
+
+Workload (headline): W4A4 SpMM, W = 4096 x 4096 int4, 50 % magnitude-pruned
+(per-row), 64 x 64 bitmap tiles, N in {1, 8, 16} int4 tokens, int32 accumulators
+plus the fp16 dequantised output.  One step = one pass of the hot path
+(staging, popcount/prefix decode, multiply, split-K reduction, epilogue) at
+N = 1, 8 and 16 over every resident weight copy.  The encoded matrix is
+replicated into enough distinct device buffers that one pass streams more than
+twice the L2 size, so each launch reads its weights from HBM.  Launches are
+captured in CUDA graphs (one per N) and timed with CUDA events on the launching
+stream.
+
+Bytes per call (algorithmic): bitmap M*K/8 + tile_off 4*(nT+1) + values (used
+bytes, padding included) + X K*N/2 + scales 2M + 2N + outputs M*N*(4 + 2).
+Effective TOPS = 2*M*K*N / t (dense-equivalent).
+
+``--impl reference`` times the CPU oracle (test infrastructure, the reference
+arm of this benchmark) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M_, K_, SPARSITY, TM_, TK_ = 4096, 4096, 0.5, 64, 64
+NS = (1, 8, 16)
+HBM_MEASURED_FALLBACK = 6800.0
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return HBM_MEASURED_FALLBACK, 1900.0, "fallback"
+
+
+def call_bytes(values_bytes: int, M: int, K: int, N: int, TM: int, TK: int) -> int:
+    nT = (M // TM) * (K // TK)
+    return M * K // 8 + 4 * (nT + 1) + values_bytes + K * N // 2 + 2 * M + 2 * N + M * N * 6
+
+
+# ----------------------------------------------------------------- clocks --
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- reference --
+class CpuSample:
+    """The oracle on one 4096 x 4096 W4A4 matrix: decode the encoded form, then
+    multiply, once for each of N = 1, 8 and 16 (one call each)."""
+
+    def __init__(self):
+        from bitmap_encoded_unstructured_ie_gb300 import workloads as wl
+        from oracle import oracle as orc
+        self.orc = orc
+        self.d = wl.w4a4(M_, K_, max(NS), SPARSITY, seed=0)
+        self.enc = orc.encode(self.d["Wq"], TM_, TK_, orc.I4, orc.ROW)
+        self.pass_bytes = sum(call_bytes(self.enc[2].size, M_, K_, N, TM_, TK_) for N in NS)
+
+    def one_pass(self, nthreads: int) -> float:
+        orc, d = self.orc, self.d
+        t0 = time.perf_counter()
+        for N in NS:
+            Wd = orc.decode(*self.enc, M_, K_, TM_, TK_, orc.I4, orc.ROW)
+            orc.spmm_w4a4(Wd, d["Xq"][:N], d["s_w"], d["s_x"][:N], nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    def timed(self, nthreads: int, min_seconds: float):
+        passes, el = 0, 0.0
+        while passes == 0 or el < min_seconds:
+            el += self.one_pass(nthreads)
+            passes += 1
+        return self.pass_bytes * passes / el / 1e9, el / passes, passes
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from oracle import oracle as orc
+    orc.build()
+    threads = orc.max_threads()
+    smp = CpuSample()
+    for _ in range(args.warmup):
+        smp.one_pass(threads)
+    times = [smp.one_pass(threads) for _ in range(args.steps)]
+    step_s = sum(times) / len(times)
+    value = smp.pass_bytes / step_s / 1e9
+    line = {
+        "impl": "reference", "metric": "bitmap SpMM GB/s (% of GB300 HBM peak) & effective TOPS at N=1/8/16",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4xint4->int32", "data": "synthetic",
+        "config": {"workload": "W4A4 bitmap SpMM 4096x4096, 50% magnitude-pruned per row, 64x64 tiles, N=1/8/16",
+                   "sample": "one weight matrix per step (of the GPU arm's rotating copies): oracle decode + "
+                             "multiply at N=1, 8, 16"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": "one 4096x4096 W4A4 matrix per step (decode + N=1,8,16)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm --
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--copies", type=int, default=0, help="resident weight copies (0 = enough for 2x L2)")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from bitmap_encoded_unstructured_ie_gb300 import build as us_build
+    from bitmap_encoded_unstructured_ie_gb300 import binding as us
+    from bitmap_encoded_unstructured_ie_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    us_build.build()
+    us.load()
+    hbm_peak, bf16_peak, peak_src = peaks()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20)
+
+    # ---- workload and resident copies
+    d = wl.w4a4(M_, K_, max(NS), SPARSITY, seed=0)
+    E0 = us.us_encode(torch.from_numpy(d["Wq"]).to(dev), TM_, TK_, us.US_I4, us.US_ORDER_ROW)
+    assert us.us_get_last_device_status() == us.US_OK
+    per_copy = E0.nbytes()
+    L = args.copies or max(4, math.ceil(2.2 * l2 / per_copy))
+    copies = [E0] + [us.Encoded(E0.M, E0.K, E0.TM, E0.TK, E0.elem, E0.order, E0.bitmap.clone(),
+                                E0.tile_off.clone(), E0.values.clone(), E0.values_bytes) for _ in range(L - 1)]
+    sw = torch.from_numpy(d["s_w"].view(np.int16)).to(dev)
+    X, SX, Yacc, Y, WS = {}, {}, {}, {}, {}
+    for N in NS:
+        X[N] = torch.from_numpy(wl.pack_int4(d["Xq"][:N])).to(dev)
+        SX[N] = torch.from_numpy(d["s_x"][:N].view(np.int16)).to(dev)
+        Yacc[N] = torch.empty(N, M_, dtype=torch.int32, device=dev)
+        Y[N] = torch.empty(N, M_, dtype=torch.int16, device=dev)
+        WS[N] = us.workspace(us.US_OP_SPMM_W4A4, E0, N)
+
+    stream = torch.cuda.Stream(dev)
+
+    def launch_all(N):
+        for E in copies:
+            us.us_spmm_w4a4(E, X[N], sw, SX[N], N, Yacc[N], Y[N], WS[N], 0, stream)
+
+    with torch.cuda.stream(stream):
+        for N in NS:                       # eager warm-up (module load, attributes)
+            launch_all(N)
+    stream.synchronize()
+    assert us.us_get_last_device_status(stream) == us.US_OK
+    graphs = {}
+    for N in NS:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch_all(N)
+        graphs[N] = g
+    for _ in range(args.warmup):
+        for N in NS:
+            graphs[N].replay()
+    stream.synchronize()
+
+    # ---- timed region
+    ev = {N: ([], []) for N in NS}
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(args.steps):
+            for N in NS:
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graphs[N].replay()
+                b.record(stream)
+                ev[N][0].append(a)
+                ev[N][1].append(b)
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert us.us_get_last_device_status(stream) == us.US_OK
+
+    per_n = {}
+    step_bytes = 0
+    for N in NS:
+        ms = sum(a.elapsed_time(b) for a, b in zip(*ev[N]))
+        us_per_launch = ms * 1e3 / (args.steps * L)
+        b_call = call_bytes(E0.values_bytes, M_, K_, N, TM_, TK_)
+        step_bytes += b_call * L
+        gbs = b_call / (us_per_launch * 1e-6) / 1e9
+        per_n[str(N)] = {
+            "us_per_launch": round(us_per_launch, 3), "bytes_per_call": b_call, "GB/s": round(gbs, 1),
+            "pct_hbm_measured": round(100 * gbs / hbm_peak, 1), "pct_hbm_8TBs": round(100 * gbs / 8000, 1),
+            "eff_TOPS": round(2 * M_ * K_ * N / (us_per_launch * 1e-6) / 1e12, 2),
+            "split_k": us.us_pick_split_k(us.US_OP_SPMM_W4A4, E0, N),
+            "kernel": kernel_name(N), "share": None,
+        }
+    tot = sum(v["us_per_launch"] for v in per_n.values())
+    for v in per_n.values():
+        v["share"] = round(v["us_per_launch"] / tot, 3)
+    step_ms = total_ms / args.steps
+    value = step_bytes * world / (step_ms * 1e-3) / 1e9
+    # dominant kernel: largest time share
+    dom_n = max(per_n, key=lambda k: per_n[k]["us_per_launch"])
+    dom = per_n[dom_n]
+    traffic = load_traffic(dom["kernel"])
+    roofline = {"bound": "hbm", "achieved": dom["GB/s"], "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(dom["GB/s"] / hbm_peak, 4), "traffic": traffic,
+                "kernel": dom["kernel"], "at_N": int(dom_n), "peak_source": peak_src}
+
+    e2e = measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L)
+
+    extras = {}
+    if not args.no_extras and rank == 0:
+        extras = measure_extras(us, torch, wl, dev, stream)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        from oracle import oracle as orc
+        threads = orc.max_threads()
+        gbs, t_pass, passes = CpuSample().timed(threads, args.cpu_seconds)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"one 4096x4096 W4A4 matrix: oracle decode + multiply at N=1,8,16, {passes} passes "
+                         f"({t_pass:.2f} s each) on {threads} threads"}
+
+    line = {
+        "metric": "bitmap SpMM GB/s (% of GB300 HBM peak) & effective TOPS at N=1/8/16",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int4xint4->int32", "data": "synthetic",
+        "config": {"workload": "W4A4 bitmap SpMM 4096x4096, 50% magnitude-pruned per row, 64x64 tiles, N=1/8/16",
+                   "weight_copies": L, "bytes_per_copy": per_copy,
+                   "l2": f"inputs larger than L2: {L} resident weight copies = {L * per_copy / 2**20:.0f} MiB "
+                         f"> 2 x L2 ({l2 / 2**20:.0f} MiB)", "graphs": "one CUDA graph per N, L launches each",
+                   "parallelism": f"replicas x{world} (independent weight sets, no collective)"},
+        "per_n": per_n,
+        "roofline": roofline,
+        "gpu_launches": args.steps * L * len(NS),
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "extras": extras,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def kernel_name(N: int) -> str:
+    return "spmm_generic_kernel<I4,64>"
+
+
+def load_traffic(kernel: str):
+    """Per-launch DRAM bytes of this kernel from the committed ncu summary, if
+    it was taken on the current kernel source (else null)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d.get(kernel)
+        if not ent:
+            return None
+        return ent.get("dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L):
+    """Same metric through the C ABI with host buffers: every step copies each
+    N's activations from pinned host memory and every output back to pinned
+    host memory, inside the timed region (captured with the launches)."""
+    steps = max(3, min(args.steps, 20))
+    hX, hY, dX, dSX, dYacc, dY, ws = {}, {}, {}, {}, {}, {}, {}
+    h2d = d2h = 0
+    for N in NS:
+        px = torch.from_numpy(wl.pack_int4(d["Xq"][:N])).pin_memory()
+        hX[N] = px
+        dX[N] = torch.empty_like(px, device=dev)
+        dSX[N] = torch.from_numpy(d["s_x"][:N].view(np.int16)).to(dev)
+        dYacc[N] = torch.empty(N, M_, dtype=torch.int32, device=dev)
+        dY[N] = torch.empty(N, M_, dtype=torch.int16, device=dev)
+        hY[N] = torch.empty(L, N, M_, dtype=torch.int16).pin_memory()
+        ws[N] = us.workspace(us.US_OP_SPMM_W4A4, copies[0], N)
+        h2d += px.numel()
+        d2h += L * N * M_ * 2
+
+    def step():
+        for N in NS:
+            dX[N].copy_(hX[N], non_blocking=True)
+            for i, E in enumerate(copies):
+                us.us_spmm_w4a4(E, dX[N], sw, dSX[N], N, dYacc[N], dY[N], ws[N], 0, stream)
+                hY[N][i].copy_(dY[N], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    for _ in range(3):
+        g.replay()
+    stream.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            g.replay()
+        b.record(stream)
+    stream.synchronize()
+    ms = a.elapsed_time(b) / steps
+    bytes_step = sum(call_bytes(copies[0].values_bytes, M_, K_, N, TM_, TK_) for N in NS) * L
+    return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "how": "CUDA graph of the C-ABI calls with pinned-host H2D of X and D2H of every fp16 output"}
+
+
+def time_graph(torch, stream, fn, reps=5):
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    g.replay()
+    stream.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+    stream.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def measure_extras(us, torch, wl, dev, stream):
+    """Secondary rows, each timed on its own: spMspV, the encoder, fp16 prefill,
+    the FFN W4A4 shapes.  Copies rotate so every launch reads from HBM."""
+    out = {}
+    l2 = 126 * 2 ** 20
+    # spMspV 14336 x 4096, 50 % static sparsity, activations with 50/70/90 % zeros
+    s = wl.spmspv(14336, 4096, 0.5, 0.5, seed=0)
+    Es = us.us_encode(torch.from_numpy(s["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_COL)
+    n_cp = max(2, math.ceil(2.2 * l2 / Es.nbytes()))
+    cps = [Es] + [us.Encoded(Es.M, Es.K, Es.TM, Es.TK, Es.elem, Es.order, Es.bitmap.clone(), Es.tile_off.clone(),
+                             Es.values.clone(), Es.values_bytes) for _ in range(n_cp - 1)]
+    wsb = us.workspace(us.US_OP_SPMSPV_F16, Es, 1)
+    ys = torch.empty(14336, dtype=torch.int16, device=dev)
+    rng = np.random.default_rng(2)
+    sp = {}
+    Wnz = (s["W"].view(np.uint16) & 0x7FFF) != 0
+    for zf in (0.5, 0.7, 0.9):
+        x = wl.relu_threshold(rng.standard_normal(4096).astype(np.float32), zf).astype(np.float16)
+        xt = torch.from_numpy(x.view(np.int16)).to(dev)
+        active = np.abs(x.astype(np.float32)) > 0
+        act_vals = int(Wnz[:, active].sum()) * 2
+        nT = (14336 // 64) * (4096 // 64)
+        alg = 14336 * 4096 // 8 + 4 * (nT + 1) + act_vals + 4096 * 2 + 14336 * 2
+        ms = time_graph(torch, stream, lambda: [us.us_spmspv_f16(E, xt, 0.0, ys, wsb, stream) for E in cps])
+        t = ms * 1e3 / n_cp
+        sp[f"zeros_{int(zf * 100)}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
+                                        "GB/s": round(alg / (t * 1e-6) / 1e9, 1)}
+    out["spmspv_f16_14336x4096"] = sp
+    # encoder, W4A4 4096^2 (dense int8 codes in): count + scan + pack
+    d = wl.w4a4(4096, 4096, 1, 0.5, seed=0)
+    Wd = torch.from_numpy(d["Wq"]).to(dev)
+    Ee = us.us_encode(Wd, 64, 64, us.US_I4, us.US_ORDER_ROW, None, False)
+    wse = torch.zeros(us.encode_sizes(4096, 4096, 64, 64, us.US_I4)[3], dtype=torch.uint8, device=dev)
+    ms = time_graph(torch, stream, lambda: us.us_encode_into(Wd, Ee, wse, stream), 5)
+    out["encode_w4a4_4096"] = {"ms_per_encode": round(ms, 4),
+                               "dense_GB/s": round(4096 * 4096 / (ms * 1e-3) / 1e9, 1)}
+    # fp16 prefill 4096^2, 60 % sparsity, N = 256 / 1024 / 2048
+    f = wl.f16_spmm(4096, 4096, 2048, 0.6, seed=0)
+    Ef = us.us_encode(torch.from_numpy(f["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_ROW)
+    Xf = torch.from_numpy(f["X"].view(np.int16)).to(dev)
+    pf = {}
+    for N in (256, 1024, 2048):
+        Yf = torch.empty(N, 4096, dtype=torch.int16, device=dev)
+        wsf = us.workspace(us.US_OP_SPMM_F16, Ef, N)
+        ms = time_graph(torch, stream, lambda: us.us_spmm_f16(Ef, Xf[:N], N, Yf, wsf, 0, stream), 3)
+        fl = 2 * 4096 * 4096 * N
+        pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
+    out["prefill_f16_4096_s60"] = pf
+    return out
+
+
+if __name__ == "__main__":
+    sys.exit(main())

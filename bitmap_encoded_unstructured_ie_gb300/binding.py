@@ -157,6 +157,16 @@ def us_encode(W: torch.Tensor, TM: int, TK: int, elem: int, order: int, stream=N
     return Encoded(M, K, TM, TK, elem, order, bitmap, tile_off, values, used)
 
 
+def us_encode_into(W: torch.Tensor, E: Encoded, ws: torch.Tensor, stream=None):
+    """Re-encode W into E's existing buffers (no readback, no synchronisation).
+    E.values must have the worst-case capacity (shrink=False)."""
+    M, K = W.shape
+    assert W.is_cuda and W.stride(1) == 1
+    _check("us_encode", load().us_encode(ctypes.c_void_p(W.data_ptr()), W.stride(0), M, K, E.TM, E.TK, E.elem,
+                                         E.order, _dptr(E.bitmap), _dptr(E.tile_off), _dptr(E.values),
+                                         E.values.numel(), _dptr(ws), ws.numel(), _stream(stream)))
+
+
 def from_host(bitmap, tile_off, values, M, K, TM, TK, elem, order, device="cuda") -> Encoded:
     """Wrap host numpy arrays of an encoded matrix as device tensors."""
     import numpy as np
