@@ -206,10 +206,12 @@ def main():
     d = wl.w4a4(M_, K_, max(NS), SPARSITY, seed=0)
     E0 = us.us_encode(torch.from_numpy(d["Wq"]).to(dev), TM_, TK_, us.US_I4, us.US_ORDER_ROW)
     assert us.us_get_last_device_status() == us.US_OK
+    E0.flags = us.US_BITMAP_STATIC          # inference weights: nothing earlier on the stream writes them
     per_copy = E0.nbytes()
     L = args.copies or max(4, math.ceil(2.2 * l2 / per_copy))
     copies = [E0] + [us.Encoded(E0.M, E0.K, E0.TM, E0.TK, E0.elem, E0.order, E0.bitmap.clone(),
-                                E0.tile_off.clone(), E0.values.clone(), E0.values_bytes) for _ in range(L - 1)]
+                                E0.tile_off.clone(), E0.values.clone(), E0.values_bytes, E0.flags)
+                     for _ in range(L - 1)]
     sw = torch.from_numpy(d["s_w"].view(np.int16)).to(dev)
     X, SX, Yacc, Y, WS = {}, {}, {}, {}, {}
     for N in NS:
@@ -326,7 +328,9 @@ def main():
                    "weight_copies": L, "bytes_per_copy": per_copy,
                    "l2": f"inputs larger than L2: {L} resident weight copies = {L * per_copy / 2**20:.0f} MiB "
                          f"> 2 x L2 ({l2 / 2**20:.0f} MiB)", "graphs": "one CUDA graph per N, L launches each",
-                   "parallelism": f"replicas x{world} (independent weight sets, no collective)"},
+                   "parallelism": f"replicas x{world} (independent weight sets, no collective)",
+                   "weights": "flagged US_BITMAP_STATIC: a launch may fetch its weights while the previous "
+                              "launch drains (programmatic dependent launch)"},
         "per_n": per_n,
         "roofline": roofline,
         "gpu_launches": args.steps * L * len(NS),
@@ -343,6 +347,9 @@ def main():
 
 
 def kernel_name(N: int) -> str:
+    """The kernel the library dispatches for W4A4 64x64 tiles at N tokens."""
+    if N <= 32:
+        return f"w4a4_small_n_kernel<{min(N, 8)}>"
     return "spmm_generic_kernel<I4,64>"
 
 

@@ -26,6 +26,7 @@ US_ERR_WORKSPACE, US_ERR_CUDA, US_ERR_TIMEOUT, US_ERR_CORRUPT = 4, 5, 6, 7
 US_F16, US_I4 = 0, 1
 US_ORDER_ROW, US_ORDER_COL = 0, 1
 US_OP_ENCODE, US_OP_SPMM_W4A4, US_OP_SPMM_F16, US_OP_SPMSPV_F16 = 0, 1, 2, 3
+US_BITMAP_STATIC = 1
 
 EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmspv_f16",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
@@ -46,7 +47,7 @@ class us_bitmap(ctypes.Structure):
     _fields_ = [("M", ctypes.c_int32), ("K", ctypes.c_int32), ("TM", ctypes.c_int32), ("TK", ctypes.c_int32),
                 ("elem", ctypes.c_int32), ("order", ctypes.c_int32),
                 ("bitmap", ctypes.c_void_p), ("tile_off", ctypes.c_void_p), ("values", ctypes.c_void_p),
-                ("values_bytes", ctypes.c_uint64)]
+                ("values_bytes", ctypes.c_uint64), ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
 
 
 _lock = threading.Lock()
@@ -119,11 +120,12 @@ class Encoded:
     tile_off: torch.Tensor    # uint32 (int32 storage), nT + 1
     values: torch.Tensor      # uint8
     values_bytes: int
+    flags: int = 0            # US_BITMAP_STATIC: not written by earlier work on the stream
 
     def desc(self) -> us_bitmap:
         return us_bitmap(self.M, self.K, self.TM, self.TK, self.elem, self.order,
                          self.bitmap.data_ptr(), self.tile_off.data_ptr(), self.values.data_ptr(),
-                         self.values_bytes)
+                         self.values_bytes, self.flags, 0)
 
     def nbytes(self) -> int:
         return self.bitmap.numel() * 8 + self.tile_off.numel() * 4 + self.values_bytes
@@ -224,7 +226,7 @@ def us_validate_host(bitmap, tile_off, values, M, K, TM, TK, elem, order) -> int
     off = np.ascontiguousarray(tile_off, dtype=np.uint32)
     v = np.ascontiguousarray(values, dtype=np.uint8)
     d = us_bitmap(M, K, TM, TK, elem, order, bm.ctypes.data, off.ctypes.data,
-                  v.ctypes.data if v.size else None, v.size)
+                  v.ctypes.data if v.size else None, v.size, 0, 0)
     return int(load().us_validate(ctypes.byref(d)))
 
 

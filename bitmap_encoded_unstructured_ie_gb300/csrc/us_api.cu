@@ -60,17 +60,18 @@ us_status check_bitmap(const us_bitmap* W, int elem, int order) {
     if (W->order != order) return US_ERR_UNSUPPORTED;
     if (!W->bitmap || !W->tile_off || (!W->values && W->values_bytes)) return US_ERR_INVALID_ARG;
     if (!aligned16(W->bitmap) || !aligned16(W->tile_off) || !aligned16(W->values)) return US_ERR_INVALID_ARG;
+    if ((W->flags & ~US_BITMAP_STATIC) || W->reserved) return US_ERR_INVALID_ARG;
     return US_OK;
 }
 
 // split-K rule: the smallest candidate whose grid covers every SM, keeping at
 // least 4 K tiles per slice.
-int auto_split(int nTM, int nTK, int token_blocks) {
-    const int sms = us::num_sms();
+int auto_split(int nTM, int nTK, int token_blocks, int target = 0, int max_split = 16) {
+    const int sms = target > 0 ? target : us::num_sms();
     const int cands[] = {1, 2, 4, 8, 16};
     int best = 1;
     for (int c : cands) {
-        if (nTK / c < 4) break;
+        if (nTK / c < 4 || c > max_split) break;
         best = c;
         if ((int64_t)nTM * c * token_blocks >= sms) break;
     }
@@ -86,12 +87,14 @@ void fill_common(UsKParams& p, const us_bitmap* W, int N) {
     p.values_bytes = W->values_bytes;
     p.X = nullptr; p.s_w = nullptr; p.s_x = nullptr; p.Yacc = nullptr; p.Y = nullptr;
     p.tau = 0.f; p.ws = nullptr; p.counters = nullptr;
+    p.flags = W->flags;
     p.status = status_ptr();
 }
 
 // Launch plan for an SpMM call: kernel family, split, token block, workspace.
 struct Plan {
-    bool fast;
+    bool fast;      // W4A4 register-decode kernel
+    bool tc;        // fp16 tensor-core kernel
     int split;
     int tok_block;
     size_t ws;
@@ -99,11 +102,22 @@ struct Plan {
 
 Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
     Plan pl{};
+    if (op == US_OP_SPMM_F16 && us::tc_f16_supported(W->TM, W->TK, W->M, N)) {
+        pl.tc = true;
+        pl.tok_block = us::tc_tok_block();
+        pl.split = split_k > 0 ? split_k : us::tc_split(W->M, N, W->K / W->TK);
+        if (pl.split > W->K / W->TK) pl.split = W->K / W->TK;
+        pl.ws = us::tc_ws(W->M, N, pl.split);
+        return pl;
+    }
     const int nTM = W->M / W->TM, nTK = W->K / W->TK;
-    pl.fast = (op == US_OP_SPMM_W4A4) && us::w4a4_fast_supported(W->TM, W->TK, N);
-    pl.tok_block = pl.fast ? N : us::spmm_generic_tok_block(N);
+    pl.fast = (op == US_OP_SPMM_W4A4) && us::w4a4_fast_supported(W->TM, W->TK, N) &&
+              split_k <= us::w4a4_fast_max_split();
+    pl.tok_block = pl.fast ? us::w4a4_fast_tok_block(N) : us::spmm_generic_tok_block(N);
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
-    pl.split = split_k > 0 ? split_k : auto_split(nTM, nTK, ntb);
+    pl.split = split_k > 0 ? split_k
+                           : auto_split(nTM, nTK, ntb, pl.fast ? us::w4a4_fast_target_ctas() : 0,
+                                        pl.fast ? us::w4a4_fast_max_split() : 16);
     if (pl.split > nTK) pl.split = nTK;
     pl.ws = pl.fast ? us::w4a4_fast_ws(W->M, W->TM, N, pl.split)
                     : us::spmm_generic_ws(W->M, W->TM, N, pl.split, pl.tok_block);
@@ -227,9 +241,8 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
     if (!Xq || !Yacc || !aligned16(Xq) || !aligned16(Yacc)) return US_ERR_INVALID_ARG;
     if (Y && (!s_w || !s_x || !aligned16(Y))) return US_ERR_INVALID_ARG;
     if (split_k < 0 || split_k > W->K / W->TK) return US_ERR_INVALID_ARG;
-    if (!ws) return US_ERR_WORKSPACE;
     const Plan pl = plan_spmm(US_OP_SPMM_W4A4, W, N, split_k);
-    if (ws_bytes < pl.ws || !aligned16(ws)) return US_ERR_WORKSPACE;
+    if (pl.ws && (!ws || ws_bytes < pl.ws || !aligned16(ws))) return US_ERR_WORKSPACE;
     UsKParams p;
     fill_common(p, W, N);
     p.X = Xq; p.s_w = s_w; p.s_x = s_x; p.Yacc = Yacc; p.Y = Y;
@@ -257,6 +270,10 @@ us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
     p.split = pl.split; p.tok_block = pl.tok_block;
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
     p.counters = static_cast<unsigned*>(ws);
+    if (pl.tc) {
+        p.ws = static_cast<uint8_t*>(ws) + (((size_t)(W->M / 128) * ntb * 4 + 255) & ~(size_t)255);
+        return us::launch_tc_f16(p, static_cast<cudaStream_t>(stream));
+    }
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
     return us::launch_spmm_generic(p, US_F16, static_cast<cudaStream_t>(stream));
 }

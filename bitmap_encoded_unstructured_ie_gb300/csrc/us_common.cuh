@@ -98,6 +98,48 @@ US_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// A kernel launched with programmatic stream serialisation may start while
+// its predecessor drains; it must not read anything a predecessor could have
+// written before pdl_wait(), which returns once every prerequisite grid has
+// completed and its memory is visible.  pdl_launch_dependents() lets the next
+// such kernel start its own prologue early.  Both are no-ops for ordinary
+// launches.
+US_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+US_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Named barrier over the first `threads` threads (a multiple of 32), id 1..15.
+US_DEV void named_bar_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ---------------------------------------------------------------- clusters --
+US_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster must call this (hardware barrier).
+US_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of `p` (this CTA's shared memory) in the shared memory of cluster CTA `rank`.
+US_DEV uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+US_DEV int ld_cluster_s32(uint32_t addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+US_DEV float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------------- misc --
 US_DEV uint32_t lane_id() { return threadIdx.x & 31u; }
 
@@ -135,6 +177,7 @@ struct UsKParams {
     int32_t* Yacc;
     uint16_t* Y;
     float tau;
+    uint32_t flags;     // US_BITMAP_* flags of the weight descriptor
     void* ws;           // split-K partials (after the counters)
     unsigned* counters; // split-K arrival counters, one per (band, token block)
     unsigned* status;

@@ -27,6 +27,16 @@ int spmm_generic_tok_block(int N);
 bool w4a4_fast_supported(int TM, int TK, int N);
 us_status launch_w4a4_fast(const UsKParams& p, cudaStream_t st);
 size_t w4a4_fast_ws(int M, int TM, int N, int split);
+int w4a4_fast_target_ctas();
+int w4a4_fast_tok_block(int N);
+int w4a4_fast_max_split();
+
+// tensor-core fp16 SpMM for many tokens (us_tc.cu)
+bool tc_f16_supported(int TM, int TK, int M, int N);
+int tc_tok_block();
+int tc_split(int M, int N, int nTK);
+size_t tc_ws(int M, int N, int split);
+us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
 
 // spMspV (us_spmspv.cu)
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st);

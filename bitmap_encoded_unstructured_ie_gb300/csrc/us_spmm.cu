@@ -230,10 +230,9 @@ spmm_generic_kernel(const UsKParams p) {
             const int64_t b2 = (((int64_t)sl * nTB + tb) * p.nTM + band) * (int64_t)kTB * TM;
 #pragma unroll
             for (int r = 0; r < R; ++r) {
-                const acc_t v = (ELEM == US_F16)
-                                    ? (acc_t)__ldcg(reinterpret_cast<const float*>(part) + b2 + (g + r * G) * TM + i_row)
-                                    : (acc_t)__ldcg(reinterpret_cast<const int*>(part) + b2 + (g + r * G) * TM + i_row);
-                acc[r] += v;
+                acc_t* src = part + b2 + (g + r * G) * TM + i_row;
+                acc[r] += __ldcg(src);
+                __stcg(src, (acc_t)0);          // leave the workspace zeroed for the next call
             }
         }
         if (threadIdx.x == 0) p.counters[band * nTB + tb] = 0u;

@@ -178,7 +178,11 @@ spmspv_kernel(const UsKParams p) {
     __threadfence();
     for (int i = threadIdx.x; i < TM; i += kThreads) {
         float s = 0.f;
-        for (int sl = 0; sl < p.split; ++sl) s += __ldcg(part + ((int64_t)sl * p.nTM + band) * TM + i);
+        for (int sl = 0; sl < p.split; ++sl) {
+            float* src = part + ((int64_t)sl * p.nTM + band) * TM + i;
+            s += __ldcg(src);
+            __stcg(src, 0.f);                   // leave the workspace zeroed for the next call
+        }
         p.Y[(int64_t)band * TM + i] = us::float_to_half_bits(s);
     }
     if (threadIdx.x == 0) p.counters[band] = 0u;

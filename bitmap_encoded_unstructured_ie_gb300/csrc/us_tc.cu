@@ -1,0 +1,412 @@
+// us_tc.cu -- tensor-core (tcgen05) bitmap SpMM for many tokens (prefill).
+//
+// Y = W . X, W fp16 stored as 64-column bitmap tiles (IE-BME of "UnionSparse:
+// An Index-Efficient Sparsity Framework for Low-Bit Sparse LLM Inference on
+// Edge", section V-A, one area, row-major scan), X fp16 token-major, fp32
+// accumulation.  Once a tile is decoded it is a dense contraction, so it runs
+// on the 5th-generation tensor cores: the prefill kernel of "Unified
+// Static-Dynamic Pruning for Efficient LLM Inference" (section 4.3) decodes
+// tiles into shared memory and re-lays them out for the tensor cores; here the
+// decode writes the tensor cores' own K-major 128-byte-swizzled layout directly,
+// so no separate alignment pass is needed.
+//
+// One CTA computes a 128-row x 256-token output tile over its K slice:
+//  * warp 0 (producer): 1-D bulk copies of both 64-row bands' bitmap words and
+//    value runs for each 64-column K step into a raw ring, and a 2-D TMA tile
+//    load (128-byte swizzle, zero fill past N) of the matching 256 x 64
+//    activation block into the B stage;
+//  * warps 2-9 (decoders): two threads per weight row; each rebuilds 32
+//    positions per K step - rank = row base (warp scan of the band's row
+//    popcounts) + running popcount, value = run[rank] or 0 - and stores them as
+//    16-byte chunks at the swizzled positions of the A stage, then fences the
+//    generic->async proxy and arrives on the stage's "A full" barrier;
+//  * warp 1 (MMA): allocates 256 TMEM columns; one thread issues four
+//    tcgen05.mma kind::f16 (M=128, N=256, K=16) per K step with the fp32
+//    accumulator in TMEM and commits to the stage's "empty" barrier;
+//  * warps 2-5 (epilogue): tcgen05.ld the accumulator (one TMEM lane per
+//    output row) and write fp16 outputs, or, under split-K, fp32 partials that
+//    the last CTA of the tile sums in fixed slice order.
+#include <cudaTypedefs.h>
+
+#include "us_common.cuh"
+#include "us_internal.h"
+
+namespace {
+
+constexpr int kBM = 128;                 // output rows per CTA (two 64-row bands)
+constexpr int kBN = 256;                 // tokens per CTA
+constexpr int kBK = 64;                  // K per step (one bitmap tile column)
+constexpr int kStages = 3;               // A/B stages
+constexpr int kRawStages = 3;            // raw W staging
+constexpr int kDecWarps = 8;
+constexpr int kThreads = 32 * (2 + kDecWarps);
+constexpr int kABytes = kBM * kBK * 2;           // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
+constexpr int kRawBm = 2 * 512;                  // two bands' bitmaps (64x64 tiles)
+constexpr int kRawVal = 2 * 64 * 64 * 2;         // two bands' fp16 runs, worst case
+constexpr int kRawBytes = kRawBm + kRawVal;      // 17 KB
+
+struct TcSmem {
+    uint64_t raw_full[kRawStages], raw_empty[kRawStages];
+    uint64_t a_full[kStages], b_full[kStages], ab_empty[kStages];
+    uint64_t done;
+    uint32_t tmem_base;
+    uint32_t raw_len[kRawStages][2];     // run length (elements) of each band's tile
+    uint32_t flag;
+};
+
+// ------------------------------------------------------------ tcgen05 PTX --
+US_DEV uint64_t umma_smem_desc_sw128(const void* p) {
+    // K-major, 128-byte swizzle: start address >> 4, LBO unused (1), SBO = 1024 B
+    // (8 rows x 128 B), descriptor version 1, layout type 2 (SWIZZLE_128B).
+    const uint64_t addr = (uint64_t)(us::smem_addr(p) >> 4) & 0x3FFFull;
+    return addr | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// kind::f16 instruction descriptor: D fp32, A/B fp16, both K-major, N>>3, M>>4
+constexpr uint32_t umma_idesc_f16(int M, int N) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+US_DEV void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+US_DEV void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     us::smem_addr(bar))
+                 : "memory");
+}
+
+US_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(us::smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+US_DEV void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+US_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+US_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base+i)
+US_DEV void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2-D TMA tile load (x = K element, y = token) completing on `bar`
+US_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(us::smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(us::smem_addr(bar))
+        : "memory");
+}
+
+struct TcParams {
+    UsKParams p;
+    int n_tiles;          // ceil(N / kBN)
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) {
+    const UsKParams& p = tp.p;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled operand tiles
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* a_st = smem;                                   // kStages x 16 KB
+    uint8_t* b_st = a_st + kStages * kABytes;               // kStages x 32 KB
+    uint8_t* raw = b_st + kStages * kBBytes;                // kRawStages x 17 KB
+    TcSmem& S = *reinterpret_cast<TcSmem*>(raw + kRawStages * kRawBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x;                              // 128-row block
+    const int nt = blockIdx.y % tp.n_tiles;                 // token tile
+    const int slice = blockIdx.y / tp.n_tiles;              // K slice
+    const int kt0 = (int)((int64_t)slice * p.nTK / p.split);
+    const int kt1 = (int)((int64_t)(slice + 1) * p.nTK / p.split);
+    const int nk = kt1 - kt0;
+    const int band0 = mt * 2;                               // two 64-row bands
+    const uint32_t idesc = umma_idesc_f16(kBM, kBN);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRawStages; ++s) {
+            us::mbar_init(&S.raw_full[s], 1);
+            us::mbar_init(&S.raw_empty[s], kDecWarps);
+        }
+        for (int s = 0; s < kStages; ++s) {
+            us::mbar_init(&S.a_full[s], kDecWarps);
+            us::mbar_init(&S.b_full[s], 1);
+            us::mbar_init(&S.ab_empty[s], 1);
+        }
+        us::mbar_init(&S.done, 1);
+        us::fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(&S.tmem_base, kBN);
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = S.tmem_base;
+    us::pdl_wait();
+    bool failed = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            for (int q = 0; q < nk && !failed; ++q) {
+                const int rs = q % kRawStages, s = q % kStages;
+                if (q >= kRawStages && !us::mbar_wait(&S.raw_empty[rs], ((q / kRawStages) - 1) & 1, p.status)) {
+                    failed = true;
+                    break;
+                }
+                uint32_t vb[2], o0[2];
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q;
+                    const uint32_t a = p.tile_off[t], b = p.tile_off[t + 1];
+                    const bool ok = b >= a && (b - a) <= 4096u && (a & 7u) == 0 && (b & 7u) == 0 &&
+                                    (uint64_t)b * 2u <= p.values_bytes;
+                    if (!ok) us::set_status(p.status, US_ERR_CORRUPT);
+                    o0[h] = a;
+                    vb[h] = ok ? (b - a) * 2u : 0u;
+                    S.raw_len[rs][h] = ok ? (b - a) : 0u;
+                }
+                uint8_t* r = raw + rs * kRawBytes;
+                us::mbar_arrive_expect_tx(&S.raw_full[rs], kRawBm + vb[0] + vb[1]);
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q;
+                    us::bulk_g2s(r + h * 512, p.bitmap + t * 64, 512, &S.raw_full[rs]);
+                    if (vb[h]) us::bulk_g2s(r + kRawBm + h * 8192, p.values + (uint64_t)o0[h] * 2u, vb[h], &S.raw_full[rs]);
+                }
+                // activation tile for this K step
+                if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
+                    failed = true;
+                    break;
+                }
+                us::mbar_arrive_expect_tx(&S.b_full[s], kBBytes);
+                tma_load_2d(b_st + s * kBBytes, &xmap, (kt0 + q) * kBK, nt * kBN, &S.b_full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            for (int q = 0; q < nk; ++q) {
+                const int s = q % kStages;
+                if (!us::mbar_wait(&S.a_full[s], (q / kStages) & 1, p.status) ||
+                    !us::mbar_wait(&S.b_full[s], (q / kStages) & 1, p.status)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = umma_smem_desc_sw128(a_st + s * kABytes);
+                const uint64_t bd = umma_smem_desc_sw128(b_st + s * kBBytes);
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk)   // K = 16 per MMA: +32 bytes = +2 in the address field
+                    umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (q > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&S.ab_empty[s]);
+            }
+            umma_commit(&S.done);
+        }
+    } else {
+        // ------------------------------------------------------------ decoders
+        const int d = warp - 2;                            // 0..7: rows 16d .. 16d+15
+        const int row = 16 * d + (lane >> 1);              // 0..127 within the block
+        const int hb = lane & 1;                           // which 32 positions of the row
+        const int band_h = row >> 6, i_in_band = row & 63;
+        for (int q = 0; q < nk; ++q) {
+            const int rs = q % kRawStages, s = q % kStages;
+            if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
+                failed = true;
+                break;
+            }
+            const uint8_t* r = raw + rs * kRawBytes;
+            const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
+            // row base: popcounts of the earlier rows of this band (warp scan)
+            const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
+            const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
+            uint32_t incl = packed;
+#pragma unroll
+            for (int dd = 1; dd < 32; dd <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
+                if (lane >= dd) incl += o;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            const uint32_t ex = incl - packed;
+            const uint32_t exr = __shfl_sync(0xffffffffu, ex, i_in_band & 31);
+            const uint32_t rowbase = (i_in_band < 32) ? (exr & 0xFFFFu) : (tot & 0xFFFFu) + (exr >> 16);
+            const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
+            const bool ok = P <= S.raw_len[rs][band_h];
+            if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
+            const uint64_t word = bm[i_in_band];
+            const uint32_t bits = hb ? (uint32_t)(word >> 32) : (uint32_t)word;
+            uint32_t rank = rowbase + (hb ? (uint32_t)__popc((uint32_t)word) : 0u);
+            const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
+            // wait for the A stage to be free (the MMA of step q - kStages finished)
+            if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
+                failed = true;
+                break;
+            }
+            uint8_t* arow = a_st + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {                  // 8 positions per 16-byte chunk
+                uint32_t h2[4];
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    const uint32_t b0 = ok ? (bits >> (8 * c + j)) & 1u : 0u;
+                    const uint32_t b1 = ok ? (bits >> (8 * c + j + 1)) & 1u : 0u;
+                    const uint32_t v0 = b0 ? run[rank] : 0u;
+                    rank += b0;
+                    const uint32_t v1 = b1 ? run[rank] : 0u;
+                    rank += b1;
+                    h2[j >> 1] = v0 | (v1 << 16);
+                }
+                const int chunk = 4 * hb + c;
+                *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            }
+            us::fence_proxy_async_smem();                  // generic writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                us::mbar_arrive(&S.a_full[s]);
+                us::mbar_arrive(&S.raw_empty[rs]);
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    __syncthreads();
+    const bool any_failed = __syncthreads_or(failed);
+    if (warp >= 2 && warp < 6) {
+        const bool ready = !any_failed && us::mbar_wait(&S.done, 0, p.status);
+        tc_fence_after();
+        const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
+        const int m = mt * kBM + quarter * 32 + lane;
+        const int nbase = nt * kBN;
+        float* part = reinterpret_cast<float*>(p.ws);
+        const int nTB = tp.n_tiles;
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+            float v[32];
+            tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+            if (!ready) continue;
+            if (p.split > 1) {
+                const int64_t base = (((int64_t)slice * nTB + nt) * p.M + m) * kBN + c0;
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    __stcg(reinterpret_cast<float4*>(part + base + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int n = nbase + c0 + i;
+                    if (n < p.N) p.Y[(int64_t)n * p.M + m] = us::float_to_half_bits(v[i]);
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, kBN);
+    if (p.split > 1 && !any_failed) {
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0)
+            S.flag = (atomicAdd(&p.counters[mt * tp.n_tiles + nt], 1u) == (unsigned)p.split - 1u) ? 1u : 0u;
+        __syncthreads();
+        if (!S.flag) return;
+        __threadfence();
+        // the last CTA of this output tile: sum the slices in order, leave zeros behind
+        float* part = reinterpret_cast<float*>(p.ws);
+        for (int idx = threadIdx.x; idx < kBM * kBN; idx += kThreads) {
+            const int mr = idx / kBN, nc = idx - mr * kBN;
+            const int m = mt * kBM + mr, n = nt * kBN + nc;
+            float acc = 0.f;
+            for (int sl = 0; sl < p.split; ++sl) {
+                float* src = part + (((int64_t)sl * tp.n_tiles + nt) * p.M + m) * kBN + nc;
+                acc += __ldcg(src);
+                __stcg(src, 0.f);
+            }
+            if (n < p.N) p.Y[(int64_t)n * p.M + m] = us::float_to_half_bits(acc);
+        }
+        if (threadIdx.x == 0) p.counters[mt * tp.n_tiles + nt] = 0u;
+    }
+}
+
+constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kRawStages * kRawBytes + 256;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+}  // namespace
+
+namespace us {
+
+bool tc_f16_supported(int TM, int TK, int M, int N) {
+    return TM == 64 && TK == 64 && M % kBM == 0 && N >= 64;
+}
+
+int tc_tok_block() { return kBN; }
+
+int tc_split(int M, int N, int nTK) {
+    const int ctas = (M / kBM) * ((N + kBN - 1) / kBN);
+    int s = 1;
+    while (ctas * s * 2 <= num_sms() && nTK / (s * 2) >= 8 && s < 8) s *= 2;
+    return s;
+}
+
+size_t tc_ws(int M, int N, int split) {
+    const int n_tiles = (N + kBN - 1) / kBN;
+    const size_t counters = ((size_t)(M / kBM) * n_tiles * 4 + 255) & ~(size_t)255;
+    return split <= 1 ? counters : counters + (size_t)split * n_tiles * M * kBN * 4;
+}
+
+us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
+    auto enc = encode_fn();
+    if (!enc) return US_ERR_CUDA;
+    CUtensorMap map;
+    const cuuint64_t gdim[2] = {(cuuint64_t)p.K, (cuuint64_t)p.N};
+    const cuuint64_t gstride[1] = {(cuuint64_t)p.K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(p.X), gdim, gstride, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return US_ERR_CUDA;
+    TcParams tp;
+    tp.p = p;
+    tp.n_tiles = (p.N + kBN - 1) / kBN;
+    if (cudaFuncSetAttribute(spmm_f16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+        cudaSuccess)
+        return US_ERR_CUDA;
+    dim3 grid((unsigned)(p.M / kBM), (unsigned)(tp.n_tiles * p.split));
+    spmm_f16_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tp, map);
+    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
+}
+
+}  // namespace us

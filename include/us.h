@@ -83,7 +83,14 @@ typedef enum {
 
 /* A view of an encoded matrix.  Plain data, copied by value into kernel
  * parameters; the caller owns the three arrays.  values_bytes is the
- * readable length of `values` (at least tile_off[nT] * bits / 8). */
+ * readable length of `values` (at least tile_off[nT] * bits / 8).
+ * flags: 0, or US_BITMAP_STATIC.  US_BITMAP_STATIC promises that no work
+ * enqueued earlier on the same stream writes bitmap, tile_off or values (the
+ * usual case for inference weights).  Kernels then start fetching them before
+ * the preceding kernel has finished (programmatic dependent launch); the
+ * activations and outputs are still touched only after it has.  Leave it 0
+ * when the matrix may still be in the making, e.g. right after us_encode. */
+#define US_BITMAP_STATIC 1u
 typedef struct {
     int32_t M, K, TM, TK;
     int32_t elem;             /* us_elem */
@@ -92,6 +99,8 @@ typedef struct {
     const uint32_t* tile_off;
     const void* values;
     uint64_t values_bytes;
+    uint32_t flags;
+    uint32_t reserved;        /* must be 0 */
 } us_bitmap;
 
 /* Sizes of the encoder's outputs and workspace (all host out-params).

@@ -139,6 +139,9 @@ W4A4_CASES = [
     (192, 320, 64, 16, 7, 0.5, 4),
     (128, 1024, 64, 64, 1, 1.0, 16),
     (128, 512, 64, 64, 64, 0.05, 0),
+    (256, 512, 64, 64, 13, 0.5, 0),      # token blocks 8 + 5
+    (256, 1024, 64, 64, 32, 0.5, 4),
+    (192, 768, 64, 64, 24, 0.3, 0),
 ]
 
 
@@ -207,15 +210,18 @@ def test_corrupt_offsets_are_refused_on_device(us, orc):
 
 def test_workspace_too_small_is_a_host_error(us, orc):
     rng = np.random.default_rng(2)
-    W = rand_i4(rng, 256, 512, 0.5)
-    E = encode_gpu(us, W, 64, 64, I4, ROW)
-    X = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    Yacc = torch.empty(1, 256, dtype=torch.int32, device="cuda")
-    need = us.us_workspace_bytes(us.US_OP_SPMM_W4A4, E, 1, 4)
+    W = rand_f16(rng, 256, 512, 0.5)
+    E = encode_gpu(us, W, 64, 64, F16, ROW)
+    X = torch.zeros(1, 512, dtype=torch.int16, device="cuda")
+    Y = torch.empty(1, 256, dtype=torch.int16, device="cuda")
+    need = us.us_workspace_bytes(us.US_OP_SPMM_F16, E, 1, 4)
     ws = torch.zeros(max(need - 16, 16), dtype=torch.uint8, device="cuda")
     with pytest.raises(us.UsError) as ei:
-        us.us_spmm_w4a4(E, X, None, None, 1, Yacc, None, ws, 4)
+        us.us_spmm_f16(E, X, 1, Y, ws, 4)
     assert ei.value.code == us.US_ERR_WORKSPACE
+    # the W4A4 decode path reduces split-K inside a cluster: no workspace at all
+    Ei = encode_gpu(us, rand_i4(rng, 256, 512, 0.5), 64, 64, I4, ROW)
+    assert us.us_workspace_bytes(us.US_OP_SPMM_W4A4, Ei, 1, 4) == 0
 
 
 # -------------------------------------------------------------------- fp16 --
@@ -231,6 +237,13 @@ def run_f16(us, E, X: np.ndarray, split_k=0):
 
 
 F16_CASES = [
+    # tensor-core path (64x64 tiles, N >= 64): two M tiles, ragged token tiles, split-K
+    (256, 512, 64, 64, 64, 0.5, 0),
+    (256, 512, 64, 64, 100, 0.4, 0),
+    (256, 1024, 64, 64, 300, 0.5, 2),
+    (384, 768, 64, 64, 257, 0.6, 3),
+    (128, 512, 64, 64, 512, 1.0, 0),
+    # CUDA-core paths
     (256, 512, 64, 64, 1, 0.5, 0),
     (256, 512, 64, 64, 5, 0.5, 3),
     (512, 256, 128, 32, 32, 0.4, 0),
@@ -333,3 +346,56 @@ def test_spmspv_14336_full(us, orc, zero_frac):
     y = run_spmspv(us, E, d["x"], 0.0)
     _, exact = orc.spmspv_f16(d["W"], d["x"], 0.0, nthreads=orc.max_threads())
     check_f16(y, exact, f"spmspv 14336 zeros={zero_frac}")
+
+
+def test_one_workspace_shared_across_calls(us, orc):
+    """Calls with different kernels, splits and token counts share one zero-filled
+    workspace; each must leave behind the zeros the next one needs."""
+    rng = np.random.default_rng(17)
+    W = rand_i4(rng, 256, 1024, 0.5)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    Wf = rand_f16(rng, 256, 1024, 0.5)
+    Ef = encode_gpu(us, Wf, 64, 64, F16, ROW)
+    need = max(us.us_workspace_bytes(us.US_OP_SPMM_W4A4, E, n, s) for n in (1, 5, 13, 40) for s in (0, 2, 4))
+    need = max(need, us.us_workspace_bytes(us.US_OP_SPMM_F16, Ef, 40, 4))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    one = np.ones(256, np.float16)
+    for N, split in [(5, 4), (40, 2), (1, 0), (13, 4), (5, 2), (40, 4), (1, 4)]:
+        Xq = rng.integers(-8, 8, size=(N, 1024)).astype(np.int8)
+        Yacc = torch.empty(N, 256, dtype=torch.int32, device="cuda")
+        us.us_spmm_w4a4(E, torch.from_numpy(wl.pack_int4(Xq)).cuda(), None, None, N, Yacc, None, ws, split)
+        oacc, _ = orc.spmm_w4a4(W, Xq, one, np.ones(N, np.float16))
+        assert np.array_equal(Yacc.cpu().numpy(), oacc), (N, split)
+        X = rng.standard_normal((N, 1024)).astype(np.float16)
+        Y = torch.empty(N, 256, dtype=torch.int16, device="cuda")
+        us.us_spmm_f16(Ef, torch.from_numpy(X.view(np.int16)).cuda(), N, Y, ws, split)
+        n_idx, m_idx = np.meshgrid(np.arange(N), np.arange(256), indexing="ij")
+        _, exact = orc.spmm_f16_at(Wf, X, n_idx.reshape(-1), m_idx.reshape(-1))
+        check_f16(Y.cpu().numpy().view(np.float16).reshape(-1), exact, f"shared ws N={N}")
+    assert not ws.any().item(), "workspace not left zeroed"
+
+
+def test_static_flag_same_results_back_to_back(us, orc):
+    """Weights flagged US_BITMAP_STATIC may be fetched before the previous kernel
+    ends; activations still are not.  Back-to-back calls where each call's
+    activations are written by the kernel just before it must stay exact."""
+    rng = np.random.default_rng(23)
+    W = rand_i4(rng, 512, 2048, 0.5)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    E.flags = us.US_BITMAP_STATIC
+    N = 4
+    ws = us.workspace(us.US_OP_SPMM_W4A4, E, N)
+    Xs = [rng.integers(-8, 8, size=(N, 2048)).astype(np.int8) for _ in range(6)]
+    packed = [torch.from_numpy(wl.pack_int4(x)).cuda() for x in Xs]
+    Xbuf = torch.empty_like(packed[0])
+    outs = []
+    for i in range(6):
+        Xbuf.copy_(packed[i])                          # written right before the call
+        Yacc = torch.empty(N, 512, dtype=torch.int32, device="cuda")
+        us.us_spmm_w4a4(E, Xbuf, None, None, N, Yacc, None, ws)
+        outs.append(Yacc)
+    torch.cuda.synchronize()
+    one = np.ones(512, np.float16)
+    for i in range(6):
+        oacc, _ = orc.spmm_w4a4(W, Xs[i], one, np.ones(N, np.float16))
+        assert np.array_equal(outs[i].cpu().numpy(), oacc)
