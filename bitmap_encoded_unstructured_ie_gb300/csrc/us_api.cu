@@ -127,7 +127,7 @@ Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
 Plan plan_spmspv(const us_bitmap* W) {
     Plan pl{};
     pl.tok_block = 1;
-    pl.split = auto_split(W->M / W->TM, W->K / W->TK, 1);
+    pl.split = auto_split(W->M / W->TM, W->K / W->TK, 1, 2 * us::num_sms(), us::spmspv_max_split());
     pl.ws = us::spmspv_ws(W->M, W->TM, pl.split);
     return pl;
 }
@@ -283,9 +283,8 @@ us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16
     us_status s = check_bitmap(W, US_F16, US_ORDER_COL);
     if (s != US_OK) return s;
     if (!x || !y || !aligned16(x) || !aligned16(y) || !(tau >= 0.f)) return US_ERR_INVALID_ARG;
-    if (!ws) return US_ERR_WORKSPACE;
     const Plan pl = plan_spmspv(W);
-    if (ws_bytes < pl.ws || !aligned16(ws)) return US_ERR_WORKSPACE;
+    if (pl.ws && (!ws || ws_bytes < pl.ws || !aligned16(ws))) return US_ERR_WORKSPACE;
     UsKParams p;
     fill_common(p, W, 1);
     p.X = x; p.Y = y; p.tau = tau;

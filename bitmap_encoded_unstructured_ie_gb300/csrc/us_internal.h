@@ -41,6 +41,7 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
 // spMspV (us_spmspv.cu)
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st);
 size_t spmspv_ws(int M, int TM, int split);
+int spmspv_max_split();
 
 // device properties of the current device (cached)
 int num_sms();

@@ -2,19 +2,27 @@
 //
 // y = (W (.) M) . (x (.) M(x)): static bitmap sparsity of W and a dynamic
 // mask that keeps column k iff |x_k| > tau ("Unified Static-Dynamic Pruning
-// for Efficient LLM Inference", section 2 and section 4.2, HAD-SMBD: an
-// inactive column is skipped entirely; an active column's nonzeros are
-// addressed by base + masked popcount).  W is stored column-major inside its
+// for Efficient LLM Inference", section 2 and section 4.2: an inactive column
+// is skipped entirely; an active column's nonzeros are addressed by its base
+// plus a masked popcount, HAD-SMBD).  W is stored column-major inside its
 // tiles (Tiled-CBC scan, same page section 4.1), so the nonzeros of one
-// column are one contiguous run: a skipped column costs no value bytes.
+// column form one contiguous run: a skipped column costs no value bytes.
 //
-// Per CTA: one tile-row band x one K slice.  The tile bitmaps stream through
-// a two-stage shared-memory ring (1-D bulk copies on mbarriers); the column
-// bases come from a block scan of the column popcounts; each warp walks its
-// columns, skips the inactive ones, and its lanes gather the active runs
-// straight from global memory (read-once, no L1 allocation) into fp32 row
-// accumulators.  Warp partials are summed in fixed warp order; split-K
-// partials in fixed slice order by the last CTA of a band.
+// Per CTA: one tile-row band x one K slice; the K slices of a band form one
+// thread-block cluster.  Eight warps, each owning whole tiles, with no block
+// barrier in the main loop:
+//  * a warp fetches its next tile's bitmap (16 bytes per lane, read-only
+//    path) while it works on the current one - the metadata-first prefetch of
+//    SPDP section 4.2.2;
+//  * column popcounts -> column bases by warp scan; a ballot of
+//    "popcount > 0 and |x_j| > tau" lists the active columns;
+//  * for each active column the lanes own rows: a set bit yields
+//    rank = base + masked popcount, and the value run[rank] is gathered
+//    straight from global memory (one column's run is contiguous, so a warp's
+//    loads coalesce); four columns' loads are issued before they are used;
+//  * fp32 row accumulators; warp partials are summed in fixed warp order and
+//    the slices of a band in fixed rank order through distributed shared
+//    memory (no workspace, bitwise reproducible).
 #include "us_common.cuh"
 #include "us_internal.h"
 
@@ -22,210 +30,258 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kBatch = 4;                 // active columns whose loads are in flight together
 
-__device__ __forceinline__ uint32_t align16(uint32_t x) { return (x + 15u) & ~15u; }
-
-__device__ __forceinline__ uint16_t ld_stream_u16(const uint16_t* p) {
+__device__ __forceinline__ uint16_t ld_once_u16(const uint16_t* p) {
     uint16_t v;
     asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
     return v;
 }
+__device__ __forceinline__ uint4 ld_once_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
 
-template <int TM>
+// TM rows per tile; NPV 16-byte pieces of a tile's bitmap held per lane
+template <int TM, int NPV>
 __global__ void __launch_bounds__(kThreads)
 spmspv_kernel(const UsKParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int WPC = TM / 64;          // 64-bit words per column
     constexpr int RPL = TM / 32;          // rows per lane
     const int TK = p.TK;
-    const int band = blockIdx.x % p.nTM;
-    const int slice = blockIdx.x / p.nTM;
+    const int band = blockIdx.x / p.split;        // the split slices of a band form one cluster
+    const int slice = blockIdx.x % p.split;
     const int kt0 = (int)((int64_t)slice * p.nTK / p.split);
     const int kt1 = (int)((int64_t)(slice + 1) * p.nTK / p.split);
     const int nk = kt1 - kt0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t bm_bytes = (uint32_t)TM * TK / 8u;            // <= NPV * 512 (launcher checks)
+    const uint32_t bm_vec = bm_bytes / 16u;                       // 16-byte pieces
+    const int nw = TM * TK / 64;
 
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem);
-    uint32_t off = 16;
-    uint32_t* offs = reinterpret_cast<uint32_t*>(smem + off);
-    off = align16(off + (uint32_t)(nk + 1) * 4u);
-    const uint32_t bm_bytes = (uint32_t)TM * TK / 8u;
-    uint8_t* stage_ptr[2];
-    stage_ptr[0] = smem + off; off += align16(bm_bytes);
-    stage_ptr[1] = smem + off; off += align16(bm_bytes);
-    uint32_t* colbase = reinterpret_cast<uint32_t*>(smem + off); off = align16(off + (uint32_t)TK * 4u);
-    float* xv = reinterpret_cast<float*>(smem + off); off = align16(off + (uint32_t)TK * 4u);
-    float* red = reinterpret_cast<float*>(smem + off);      // kWarps x TM
-    __shared__ uint32_t warp_tot[kWarps];
-    __shared__ uint32_t tile_bad;
-    __shared__ int flag_s;
+    // shared memory: per-warp bitmap and column-base scratch, activations, reduction
+    uint64_t* wbm = reinterpret_cast<uint64_t*>(smem) + (size_t)warp * (bm_bytes / 8u);
+    uint32_t off = kWarps * bm_bytes;
+    uint32_t* wbase = reinterpret_cast<uint32_t*>(smem + off) + warp * TK;
+    off += kWarps * TK * 4;
+    float* xs = reinterpret_cast<float*>(smem + off);             // nk x TK (masked activations)
+    off += ((uint32_t)nk * TK * 4u + 15u) & ~15u;
+    float* red = reinterpret_cast<float*>(smem + off);            // kWarps x TM, then TM
 
-    const int64_t tile0 = (int64_t)band * p.nTK + kt0;
-    for (int q = threadIdx.x; q <= nk; q += kThreads) offs[q] = p.tile_off[tile0 + q];
-    if (threadIdx.x == 0) {
-        us::mbar_init(&bar[0], 1);
-        us::mbar_init(&bar[1], 1);
-        us::fence_mbar_init();
+    us::pdl_launch_dependents();
+    us::pdl_wait();
+    {
+        const uint16_t* x16 = reinterpret_cast<const uint16_t*>(p.X) + (int64_t)kt0 * TK;
+        for (int i = threadIdx.x; i < nk * TK; i += kThreads) {
+            const float x = us::half_bits_to_float(x16[i]);
+            xs[i] = (fabsf(x) > p.tau) ? x : 0.f;                     // the dynamic mask M(x)
+        }
     }
     __syncthreads();
-    const int nw = TM * TK / 64;
-    auto issue = [&](int q) {
-        const int s = q & 1;
-        us::mbar_arrive_expect_tx(&bar[s], bm_bytes);
-        us::bulk_g2s(stage_ptr[s], p.bitmap + (tile0 + q) * nw, bm_bytes, &bar[s]);
-    };
-    if (threadIdx.x == 0) {
-        if (nk > 0) issue(0);
-        if (nk > 1) issue(1);
-    }
 
     float acc[RPL];
 #pragma unroll
     for (int r = 0; r < RPL; ++r) acc[r] = 0.f;
     const uint16_t* vals16 = reinterpret_cast<const uint16_t*>(p.values);
-    const uint16_t* x16 = reinterpret_cast<const uint16_t*>(p.X);
+    const int64_t tile0 = (int64_t)band * p.nTK + kt0;
 
-    uint32_t phase = 0;
-    for (int q = 0; q < nk; ++q) {
-        const int s = q & 1;
-        const bool ok = us::mbar_wait(&bar[s], (phase >> s) & 1u, p.status);
-        phase ^= 1u << s;
-        if (__syncthreads_or(!ok)) {
-            if (threadIdx.x == 0) us::mbar_wait(&bar[s ^ 1], (phase >> (s ^ 1)) & 1u, nullptr);
-            return;
-        }
-        const uint64_t* words = reinterpret_cast<const uint64_t*>(stage_ptr[s]);
-        const int kbase = (kt0 + q) * TK;
-        // column popcounts -> column bases; activation test
-        uint32_t c = 0;
-        if (threadIdx.x < TK) {
+    // prefetch registers for the next tile of this warp
+    uint4 nbm[NPV];
 #pragma unroll
-            for (int w = 0; w < WPC; ++w) c += (uint32_t)__popcll(words[threadIdx.x * WPC + w]);
-            const float x = us::half_bits_to_float(x16[kbase + threadIdx.x]);
-            xv[threadIdx.x] = (fabsf(x) > p.tau) ? x : 0.f;
+    for (int v = 0; v < NPV; ++v) nbm[v] = make_uint4(0, 0, 0, 0);
+    uint32_t no0 = 0, no1 = 0;
+    auto fetch = [&](int q) {
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.bitmap + (tile0 + q) * nw);
+#pragma unroll
+        for (int v = 0; v < NPV; ++v) {
+            const uint32_t piece = (uint32_t)lane + 32u * v;
+            if (piece < bm_vec) nbm[v] = ld_once_v4(src + 16u * piece);
         }
-        {
+        no0 = __ldg(p.tile_off + tile0 + q);
+        no1 = __ldg(p.tile_off + tile0 + q + 1);
+    };
+    if (warp < nk) fetch(warp);
+
+    for (int q = warp; q < nk; q += kWarps) {
+        // ---- this tile's bitmap into the warp's scratch; next tile's in flight
+#pragma unroll
+        for (int v = 0; v < NPV; ++v) {
+            const uint32_t piece = (uint32_t)lane + 32u * v;
+            if (piece < bm_vec) reinterpret_cast<uint4*>(wbm)[piece] = nbm[v];
+        }
+        const uint32_t o0 = no0, o1 = no1;
+        if (q + kWarps < nk) fetch(q + kWarps);
+        __syncwarp();
+        // ---- column popcounts -> bases (warp scan); active columns
+        uint32_t run_sum = 0;                            // columns of the earlier 32-column groups
+        uint32_t actmask[4] = {0u, 0u, 0u, 0u};          // up to 128 columns
+        const float* xq = xs + q * TK;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            if (g * 32 >= TK) break;
+            const int j = g * 32 + lane;
+            uint32_t c = 0;
+            bool act = false;
+            if (j < TK) {
+#pragma unroll
+                for (int w = 0; w < WPC; ++w) c += (uint32_t)__popcll(wbm[j * WPC + w]);
+                act = c > 0 && xq[j] != 0.f;
+            }
             uint32_t incl = c;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
                 if (lane >= d) incl += o;
             }
-            if (lane == 31) warp_tot[warp] = incl;
-            __syncthreads();
-            uint32_t before = 0, P = 0;
-#pragma unroll
-            for (int i = 0; i < kWarps; ++i) {
-                if (i < warp) before += warp_tot[i];
-                P += warp_tot[i];
-            }
-            if (threadIdx.x < TK) colbase[threadIdx.x] = before + incl - c;
-            if (threadIdx.x == 0) {
-                const uint32_t o0 = offs[q], o1 = offs[q + 1];
-                const bool good = o1 >= o0 && P <= o1 - o0 && (uint64_t)o1 * 2u <= p.values_bytes;
-                tile_bad = good ? 0u : 1u;
-                if (!good) us::set_status(p.status, US_ERR_CORRUPT);
-            }
+            if (j < TK) wbase[j] = run_sum + incl - c;
+            run_sum += __shfl_sync(0xffffffffu, incl, 31);
+            actmask[g] = __ballot_sync(0xffffffffu, act);
         }
-        __syncthreads();
-        if (!tile_bad) {
-            const uint16_t* run = vals16 + offs[q];
-            for (int j = warp; j < TK; j += kWarps) {
-                const float xj = xv[j];
-                if (xj == 0.f) continue;          // inactive (or zero) column: no value bytes read
-                uint32_t base = colbase[j];
+        const uint32_t P = run_sum;
+        const bool good = o1 >= o0 && (o1 - o0) <= (uint32_t)(TM * TK) && (uint64_t)o1 * 2u <= p.values_bytes &&
+                          P <= o1 - o0;
+        if (!good) {
+            if (lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
+            __syncwarp();
+            continue;
+        }
+        __syncwarp();
+        const uint16_t* run = vals16 + o0;
+        const uint32_t below = (1u << lane) - 1u;
+        // ---- active columns, kBatch at a time: issue every gather, then use them
 #pragma unroll
-                for (int w = 0; w < WPC; ++w) {
-                    const uint64_t word = words[j * WPC + w];
-                    const uint32_t lo = (uint32_t)word, hi = (uint32_t)(word >> 32);
-                    const uint32_t below = (1u << lane) - 1u;
-                    if ((lo >> lane) & 1u) {
-                        const uint32_t r = base + __popc(lo & below);
-                        acc[2 * w] = fmaf(us::half_bits_to_float(ld_stream_u16(run + r)), xj, acc[2 * w]);
+        for (int g = 0; g < 4; ++g) {
+            uint32_t m = actmask[g];
+            while (m) {
+                int js[kBatch];
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t) {
+                    js[t] = -1;
+                    if (m) {
+                        js[t] = g * 32 + __ffs(m) - 1;
+                        m &= m - 1;
                     }
-                    if ((hi >> lane) & 1u) {
-                        const uint32_t r = base + __popc(lo) + __popc(hi & below);
-                        acc[2 * w + 1] = fmaf(us::half_bits_to_float(ld_stream_u16(run + r)), xj, acc[2 * w + 1]);
-                    }
-                    base += __popc(lo) + __popc(hi);
                 }
+                uint16_t v[kBatch][2 * WPC];
+                float xj[kBatch];
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t) {
+                    const int j = js[t];
+                    xj[t] = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 2 * WPC; ++h) v[t][h] = 0;
+                    if (j < 0) continue;
+                    xj[t] = xq[j];
+                    uint32_t base = wbase[j];
+#pragma unroll
+                    for (int w = 0; w < WPC; ++w) {
+                        const uint64_t word = wbm[j * WPC + w];
+                        const uint32_t lo = (uint32_t)word, hi = (uint32_t)(word >> 32);
+                        if ((lo >> lane) & 1u) v[t][2 * w] = ld_once_u16(run + base + __popc(lo & below));
+                        if ((hi >> lane) & 1u)
+                            v[t][2 * w + 1] = ld_once_u16(run + base + __popc(lo) + __popc(hi & below));
+                        base += __popc(lo) + __popc(hi);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t)
+#pragma unroll
+                    for (int h = 0; h < 2 * WPC; ++h)
+                        acc[h] = fmaf(us::half_bits_to_float(v[t][h]), xj[t], acc[h]);
             }
         }
-        __syncthreads();
-        if (threadIdx.x == 0 && q + 2 < nk) issue(q + 2);
+        __syncwarp();
     }
 
-    // rows: lane l of word w holds row 64w + l (acc[2w]) and 64w + 32 + l (acc[2w+1])
+    // ---- rows: lane l of word w holds row 64w + l (acc[2w]) and 64w + 32 + l (acc[2w+1])
+    __syncthreads();
 #pragma unroll
     for (int w = 0; w < WPC; ++w) {
         red[warp * TM + 64 * w + lane] = acc[2 * w];
         red[warp * TM + 64 * w + 32 + lane] = acc[2 * w + 1];
     }
     __syncthreads();
-    float* part = reinterpret_cast<float*>(p.ws);
+    float* outv = red + kWarps * TM;
     for (int i = threadIdx.x; i < TM; i += kThreads) {
         float s = 0.f;
         for (int w = 0; w < kWarps; ++w) s += red[w * TM + i];
-        if (p.split > 1) part[((int64_t)slice * p.nTM + band) * TM + i] = s;
-        else p.Y[(int64_t)band * TM + i] = us::float_to_half_bits(s);
+        outv[i] = s;
     }
-    if (p.split <= 1) return;
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) flag_s = (atomicAdd(&p.counters[band], 1u) == (unsigned)p.split - 1u);
-    __syncthreads();
-    if (!flag_s) return;
-    __threadfence();
-    for (int i = threadIdx.x; i < TM; i += kThreads) {
-        float s = 0.f;
-        for (int sl = 0; sl < p.split; ++sl) {
-            float* src = part + ((int64_t)sl * p.nTM + band) * TM + i;
-            s += __ldcg(src);
-            __stcg(src, 0.f);                   // leave the workspace zeroed for the next call
+    if (p.split > 1) {
+        us::cluster_sync();
+        const int rank = (int)us::cluster_ctarank();
+        const int chunk = TM / p.split;
+        for (int i = rank * chunk + threadIdx.x; i < (rank + 1) * chunk; i += kThreads) {
+            float s = 0.f;
+            for (int r = 0; r < p.split; ++r) s += us::ld_cluster_f32(us::cluster_map(outv + i, (uint32_t)r));
+            p.Y[(int64_t)band * TM + i] = us::float_to_half_bits(s);
         }
-        p.Y[(int64_t)band * TM + i] = us::float_to_half_bits(s);
+        us::cluster_sync();
+    } else {
+        for (int i = threadIdx.x; i < TM; i += kThreads) p.Y[(int64_t)band * TM + i] = us::float_to_half_bits(outv[i]);
     }
-    if (threadIdx.x == 0) p.counters[band] = 0u;
 }
 
 size_t spmspv_smem(int TM, int TK, int nk) {
-    auto a16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
-    size_t off = 16;
-    off = a16(off + (size_t)(nk + 1) * 4);
-    off += 2 * a16((size_t)TM * TK / 8);
-    off = a16(off + (size_t)TK * 4);
-    off = a16(off + (size_t)TK * 4);
-    off += (size_t)kWarps * TM * 4;
+    size_t off = (size_t)kWarps * TM * TK / 8;
+    off += (size_t)kWarps * TK * 4;
+    off += ((size_t)nk * TK * 4 + 15) & ~(size_t)15;
+    off += (size_t)(kWarps + 1) * TM * 4;
     return off;
 }
 
-template <int TM>
+template <int TM, int NPV>
 us_status launch_t(const UsKParams& p, cudaStream_t st) {
     const int nk = (p.nTK + p.split - 1) / p.split;
     const size_t smem = spmspv_smem(TM, p.TK, nk);
-    if (smem > 227 * 1024) return US_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(spmspv_kernel<TM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (smem > 220 * 1024) return US_ERR_UNSUPPORTED;
+    auto kern = spmspv_kernel<TM, NPV>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
-    spmspv_kernel<TM><<<(unsigned)(p.nTM * p.split), kThreads, smem, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.nTM * p.split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.split;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? US_OK : US_ERR_CUDA;
 }
 
 }  // namespace
 
 namespace us {
 
-size_t spmspv_ws(int M, int TM, int split) {
-    const int nTM = M / TM;
-    const size_t counters = ((size_t)nTM * 4 + 255) & ~(size_t)255;
-    return split <= 1 ? counters : counters + (size_t)split * M * 4;
+size_t spmspv_ws(int, int, int) { return 0; }     // slices reduce inside the cluster
+
+int spmspv_max_split() { return 8; }
+
+template <int TM>
+us_status launch_tm(const UsKParams& p, cudaStream_t st) {
+    const int bm_bytes = TM * p.TK / 8;                  // 128 .. 4096
+    if (bm_bytes <= 512) return launch_t<TM, 1>(p, st);
+    if (bm_bytes <= 1024) return launch_t<TM, 2>(p, st);
+    if (bm_bytes <= 2048) return launch_t<TM, 4>(p, st);
+    return launch_t<TM, 8>(p, st);
 }
 
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st) {
     switch (p.TM) {
-        case 64: return launch_t<64>(p, st);
-        case 128: return launch_t<128>(p, st);
-        case 256: return launch_t<256>(p, st);
+        case 64: return launch_tm<64>(p, st);
+        case 128: return launch_tm<128>(p, st);
+        case 256: return launch_tm<256>(p, st);
     }
     return US_ERR_UNSUPPORTED;
 }

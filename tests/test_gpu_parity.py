@@ -287,7 +287,7 @@ def run_spmspv(us, E, x: np.ndarray, tau: float):
     return y.cpu().numpy().view(np.float16)
 
 
-@pytest.mark.parametrize("TM,TK", [(64, 64), (256, 16), (128, 32), (64, 128)])
+@pytest.mark.parametrize("TM,TK", [(64, 64), (256, 16), (128, 32), (64, 128), (256, 64), (256, 128)])
 @pytest.mark.parametrize("zero_frac,tau", [(0.5, 0.0), (0.9, 0.0), (0.0, 0.7)])
 def test_spmspv_matches_oracle(us, orc, TM, TK, zero_frac, tau):
     M, K = 512, 1024
