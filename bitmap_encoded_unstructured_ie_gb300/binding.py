@@ -28,7 +28,7 @@ US_ORDER_ROW, US_ORDER_COL = 0, 1
 US_OP_ENCODE, US_OP_SPMM_W4A4, US_OP_SPMM_F16, US_OP_SPMSPV_F16 = 0, 1, 2, 3
 US_BITMAP_STATIC = 1
 
-EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmspv_f16",
+EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmm_f16_noalloc", "us_spmspv_f16",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
             "us_status_string", "us_version")
 
@@ -71,6 +71,7 @@ def load(path: str = LIB_PATH):
         lib.us_encode.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, P, P, P, sz, P, sz, P]
         lib.us_spmm_w4a4.argtypes = [pbm, P, P, P, i32, P, P, P, sz, i32, P]
         lib.us_spmm_f16.argtypes = [pbm, P, i32, P, P, sz, i32, P]
+        lib.us_spmm_f16_noalloc.argtypes = [pbm, P, i32, P, i32, P]
         lib.us_spmspv_f16.argtypes = [pbm, P, ctypes.c_float, P, P, sz, P]
         lib.us_workspace_bytes.argtypes = [i32, pbm, i32, i32, psz]
         lib.us_pick_split_k.argtypes = [i32, pbm, i32, ctypes.POINTER(ctypes.c_int)]
@@ -211,6 +212,13 @@ def us_spmm_f16(E: Encoded, X: torch.Tensor, N: int, Y: torch.Tensor, ws: torch.
     d = E.desc()
     _check("us_spmm_f16", load().us_spmm_f16(ctypes.byref(d), _dptr(X), N, _dptr(Y), _dptr(ws), ws.numel(),
                                              split_k, _stream(stream)))
+
+
+def us_spmm_f16_noalloc(E: Encoded, X: torch.Tensor, N: int, Y: torch.Tensor, split_k: int = 0, stream=None):
+    """fp16 SpMM whose split-K scratch lives inside the library (no workspace)."""
+    d = E.desc()
+    _check("us_spmm_f16_noalloc", load().us_spmm_f16_noalloc(ctypes.byref(d), _dptr(X), N, _dptr(Y), split_k,
+                                                             _stream(stream)))
 
 
 def us_spmspv_f16(E: Encoded, x: torch.Tensor, tau: float, y: torch.Tensor, ws: torch.Tensor, stream=None):

@@ -278,6 +278,60 @@ us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
     return us::launch_spmm_generic(p, US_F16, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------- no-allocation fp16 SpMM --
+// Some callers cannot allocate device memory at the point where they multiply:
+// code running while a CUDA graph is being captured (a cudaMalloc there breaks
+// the capture), allocators that hand out a fixed arena, or embedders that own
+// every device allocation themselves.  us_spmm_f16_noalloc serves them with
+// split-K scratch that lives in this library: a file-scope device array sized
+// US_NOALLOC_SCRATCH_BYTES, created when the library is loaded onto a device
+// and kept until the process exits.
+static __device__ __align__(256) uint8_t g_us_noalloc_scratch[US_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+uint8_t* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (host code may not use the array's name as a device address).
+uint8_t* noalloc_scratch_ptr() {
+    const int d = current_device();
+    if (d < 0) return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_noalloc_ptr[d]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_us_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+        g_noalloc_ptr[d] = static_cast<uint8_t*>(ptr);
+    }
+    return g_noalloc_ptr[d];
+}
+}  // namespace
+
+us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y, int split_k, void* stream) {
+    us_status s = check_bitmap(W, US_F16, US_ORDER_ROW);
+    if (s != US_OK) return s;
+    if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
+    if (!X || !Y || !aligned16(X) || !aligned16(Y)) return US_ERR_INVALID_ARG;
+    if (split_k < 0 || split_k > W->K / W->TK) return US_ERR_INVALID_ARG;
+    Plan pl = plan_spmm(US_OP_SPMM_F16, W, N, split_k);
+    if (pl.ws > US_NOALLOC_SCRATCH_BYTES && split_k == 0) pl = plan_spmm(US_OP_SPMM_F16, W, N, 1);
+    if (pl.ws > US_NOALLOC_SCRATCH_BYTES) return US_ERR_TOO_LARGE;
+    uint8_t* scratch = noalloc_scratch_ptr();
+    if (!scratch) return US_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    UsKParams p;
+    fill_common(p, W, N);
+    p.X = X; p.Y = Y;
+    p.split = pl.split; p.tok_block = pl.tok_block;
+    const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
+    const size_t cbytes = pl.tc ? (((size_t)(W->M / 128) * ntb * 4 + 255) & ~(size_t)255) : counters_bytes(p.nTM, ntb);
+    // the split-K arrival counters must start at zero; the partials are fully
+    // written before they are read, so only the counters are cleared
+    if (cudaMemsetAsync(scratch, 0, cbytes, st) != cudaSuccess) return US_ERR_CUDA;
+    p.counters = reinterpret_cast<unsigned*>(scratch);
+    p.ws = scratch + cbytes;
+    return pl.tc ? us::launch_tc_f16(p, st) : us::launch_spmm_generic(p, US_F16, st);
+}
+
 us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y, void* ws, size_t ws_bytes,
                         void* stream) {
     us_status s = check_bitmap(W, US_F16, US_ORDER_COL);

@@ -142,6 +142,26 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
 us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
                       void* ws, size_t ws_bytes, int split_k, void* stream);
 
+/* fp16 SpMM with no workspace argument and no allocation.  (No counterpart on
+ * the pages: this is a convenience of this library.)  For callers that cannot
+ * allocate device memory where they multiply - code running inside CUDA graph
+ * capture, where a cudaMalloc would break the capture; fixed-arena allocators;
+ * embedders that own every allocation - the split-K scratch comes from a
+ * device array inside the library, US_NOALLOC_SCRATCH_BYTES (8 MiB), which
+ * every GPU that loads the library keeps until the process exits.
+ * Same arguments and results as us_spmm_f16 without ws/ws_bytes.  With
+ * split_k = 0 the automatic split is lowered to 1 if its scratch would not
+ * fit; an explicit split_k whose scratch exceeds the array returns
+ * US_ERR_TOO_LARGE before anything is enqueued.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  Each call clears the split-K
+ * counters with cudaMemsetAsync on `stream` (no allocation).  All calls share
+ * the one array: calls that may run at the same time on the GPU (different
+ * streams, overlapping graph branches) race and must not be issued. */
+#define US_NOALLOC_SCRATCH_BYTES (8u << 20)
+us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
+                              int split_k, void* stream);
+
 /* fp16 spMspV (SPDP section 4.2):  y[m] = fp16(sum over k with |x_k| > tau of
  * W[m][k] * x[k]), fp32 accumulation.  Columns whose activation fails the
  * test are skipped: their bitmap words are read, their values are not.
