@@ -348,8 +348,10 @@ def main():
 
 def kernel_name(N: int) -> str:
     """The kernel the library dispatches for W4A4 64x64 tiles at N tokens."""
+    if N <= 8:
+        return f"w4a4_sk_kernel<{N}>"
     if N <= 32:
-        return f"w4a4_small_n_kernel<{min(N, 8)}>"
+        return f"w4a4_tc_kernel<{16 if N <= 16 else 32}>"
     return "spmm_generic_kernel<I4,64>"
 
 

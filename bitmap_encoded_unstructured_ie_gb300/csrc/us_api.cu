@@ -87,14 +87,17 @@ void fill_common(UsKParams& p, const us_bitmap* W, int N) {
     p.values_bytes = W->values_bytes;
     p.X = nullptr; p.s_w = nullptr; p.s_x = nullptr; p.Yacc = nullptr; p.Y = nullptr;
     p.tau = 0.f; p.ws = nullptr; p.counters = nullptr;
+    p.sk_grid = p.sk_per = p.sk_ring = p.sk_xcols = p.sk_nb = 0;
     p.flags = W->flags;
     p.status = status_ptr();
 }
 
 // Launch plan for an SpMM call: kernel family, split, token block, workspace.
 struct Plan {
+    bool sk;        // W4A4 CUDA-core kernel over a balanced partition of the tiles
     bool fast;      // W4A4 register-decode kernel
     bool tc;        // fp16 tensor-core kernel
+    bool tcw;       // W4A4 tensor-core kernel
     int split;
     int tok_block;
     size_t ws;
@@ -102,6 +105,23 @@ struct Plan {
 
 Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
     Plan pl{};
+    if (op == US_OP_SPMM_W4A4 && split_k == 0 && us::w4a4_sk_supported(W->TM, W->TK, W->M, W->K, N)) {
+        pl.sk = true;
+        pl.split = 0;                               // no K slices: tiles spread evenly over the SMs
+        pl.tok_block = N;
+        pl.ws = us::w4a4_sk_ws(W->M, W->K, N);
+        return pl;
+    }
+    if (op == US_OP_SPMM_W4A4 && us::tc_w4a4_supported(W->TM, W->TK, W->M, W->K, N) &&
+        split_k <= us::w4a4_fast_max_split()) {
+        pl.tcw = true;
+        pl.tok_block = N;
+        pl.split = split_k > 0 ? split_k : us::tc_w4a4_split(W->M, N, W->K / W->TK);
+        if (pl.split > W->K / W->TK) pl.split = W->K / W->TK;
+        pl.ws = 0;                                  // split-K reduces inside the cluster
+        if (us::tc_w4a4_fits(N, W->K / W->TK, pl.split)) return pl;
+        pl = Plan{};                                // activations of a slice too large: CUDA-core path
+    }
     if (op == US_OP_SPMM_F16 && us::tc_f16_supported(W->TM, W->TK, W->M, N)) {
         pl.tc = true;
         pl.tok_block = us::tc_tok_block();
@@ -251,6 +271,11 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
     p.counters = static_cast<unsigned*>(ws);
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (pl.sk) {
+        p.ws = ws;
+        return us::launch_w4a4_sk(p, st);
+    }
+    if (pl.tcw) return us::launch_tc_w4a4(p, st);
     return pl.fast ? us::launch_w4a4_fast(p, st) : us::launch_spmm_generic(p, US_I4, st);
 }
 

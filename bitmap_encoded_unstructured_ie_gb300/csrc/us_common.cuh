@@ -129,6 +129,17 @@ US_DEV uint32_t cluster_map(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
     return r;
 }
+// 64-bit global word, relaxed at GPU scope: single-copy atomic, never served
+// from a stale L1 line.  Used for {value, tag} messages between CTAs.
+US_DEV uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+US_DEV void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 US_DEV int ld_cluster_s32(uint32_t addr) {
     int v;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -158,6 +169,41 @@ US_DEV uint16_t float_to_half_bits(float f) { return __half_as_ushort(__float2ha
 // int4 code in the low nibble of v -> int (two's complement)
 US_DEV int sext4(uint32_t v) { return (int)(v << 28) >> 28; }
 
+// PTX shl clamps shift counts >= 32 to a zero result (C++ leaves them undefined)
+US_DEV uint32_t shl_clamp(uint32_t x, uint32_t n) {
+    uint32_t r;
+    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(n));
+    return r;
+}
+
+// v = shared-memory word at `addr` if `pred`, else v unchanged (a predicated
+// load: lanes with pred == 0 touch no bank).  volatile keeps it in program
+// order with the mbarrier operations around it.
+US_DEV void lds_u32_if(uint32_t& v, uint32_t pred, uint32_t addr) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p ld.shared.u32 %0, [%2];\n\t}"
+        : "+r"(v)
+        : "r"(pred), "r"(addr));
+}
+
+// Byte-step decode of packed int4 runs (used by the W4A4 kernels).  For one
+// bitmap byte v (8 positions) the run's next popc(v) nibbles are split into
+// even and odd ranks, one byte each; make_sel(v) is the PRMT selector pair
+// that moves rank r to its position p: byte r/2 of the even register or
+// 4 + r/2 of the odd one.  Clear positions take byte 7 (rank 7), which the
+// masked window leaves empty unless all eight positions are set.  Low 16 bits
+// cover positions 0-3, high 16 bits positions 4-7.
+US_DEV uint32_t make_sel(uint32_t v) {
+    uint32_t sel = 0, r = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint32_t set = (v >> p) & 1u;
+        const uint32_t idx = set ? ((r & 1u) ? 4u + (r >> 1) : (r >> 1)) : 7u;
+        sel |= idx << (4 * (p & 3) + 16 * (p >> 2));
+        r += set;
+    }
+    return sel;
+}
+
 }  // namespace us
 
 // ------------------------------------------------------- kernel parameters --
@@ -181,4 +227,7 @@ struct UsKParams {
     void* ws;           // split-K partials (after the counters)
     unsigned* counters; // split-K arrival counters, one per (band, token block)
     unsigned* status;
+    // balanced (stream-K) W4A4 kernel only: CTAs, most tiles of one CTA, value
+    // ring bytes, staged activation columns (tiles), most bands one CTA touches
+    int sk_grid, sk_per, sk_ring, sk_xcols, sk_nb;
 };

@@ -31,12 +31,22 @@ int w4a4_fast_target_ctas();
 int w4a4_fast_tok_block(int N);
 int w4a4_fast_max_split();
 
+// W4A4 CUDA-core kernel over a balanced partition of the tile sequence
+// (us_w4a4_sk.cu); launch_w4a4_sk takes p.ws = start of the workspace
+bool w4a4_sk_supported(int TM, int TK, int M, int K, int N);
+size_t w4a4_sk_ws(int M, int K, int N);
+us_status launch_w4a4_sk(UsKParams p, cudaStream_t st);
+
 // tensor-core fp16 SpMM for many tokens (us_tc.cu)
 bool tc_f16_supported(int TM, int TK, int M, int N);
 int tc_tok_block();
 int tc_split(int M, int N, int nTK);
 size_t tc_ws(int M, int N, int split);
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
+bool tc_w4a4_supported(int TM, int TK, int M, int K, int N);
+bool tc_w4a4_fits(int N, int nTK, int split);   // shared memory of one CTA within the limit
+int tc_w4a4_split(int M, int N, int nTK);
+us_status launch_tc_w4a4(const UsKParams& p, cudaStream_t st);
 
 // spMspV (us_spmspv.cu)
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st);

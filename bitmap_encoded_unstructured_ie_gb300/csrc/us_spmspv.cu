@@ -215,8 +215,8 @@ spmspv_kernel(const UsKParams p) {
     if (p.split > 1) {
         us::cluster_sync();
         const int rank = (int)us::cluster_ctarank();
-        const int chunk = TM / p.split;
-        for (int i = rank * chunk + threadIdx.x; i < (rank + 1) * chunk; i += kThreads) {
+        const int i0 = rank * TM / p.split, i1 = (rank + 1) * TM / p.split;
+        for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
             float s = 0.f;
             for (int r = 0; r < p.split; ++r) s += us::ld_cluster_f32(us::cluster_map(outv + i, (uint32_t)r));
             p.Y[(int64_t)band * TM + i] = us::float_to_half_bits(s);

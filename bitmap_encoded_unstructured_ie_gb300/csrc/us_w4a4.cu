@@ -55,30 +55,6 @@ constexpr int kBufBytes = kChunk * (kBmBytes + kValCap);   // 20480 per chunk bu
 constexpr int kLutRep = 16;                             // LUT replicas (bank spreading)
 constexpr int kHeader = 256;
 
-// Selector pair for bitmap byte v: dense position p takes rank r (the number
-// of set bits of v below p) from the (even ranks | odd ranks) register pair,
-// i.e. byte r/2 or 4 + r/2; clear positions take byte 7 (rank 7, which the
-// masked window leaves zero unless all eight positions are set).  Low 16 bits:
-// positions 0-3, high 16 bits: positions 4-7.
-__device__ __forceinline__ uint32_t make_sel(uint32_t v) {
-    uint32_t sel = 0, r = 0;
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const uint32_t set = (v >> p) & 1u;
-        const uint32_t idx = set ? ((r & 1u) ? 4u + (r >> 1) : (r >> 1)) : 7u;
-        sel |= idx << (4 * (p & 3) + 16 * (p >> 2));
-        r += set;
-    }
-    return sel;
-}
-
-// PTX shl clamps shift counts >= 32 to a zero result (C++ leaves them undefined)
-__device__ __forceinline__ uint32_t shl_clamp(uint32_t x, uint32_t n) {
-    uint32_t r;
-    asm("shl.b32 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(n));
-    return r;
-}
-
 struct Smem {
     uint64_t full[2];
     uint64_t empty[2];
@@ -144,6 +120,9 @@ w4a4_small_n_kernel(const UsKParams p) {
                      (uint64_t)o1 * 4u <= p.values_bytes * 8ull;
             }
             const bool all_ok = __all_sync(0xffffffffu, ok);
+            // the consumers start only after the previous launch has finished: wait
+            // for that too before a bounded wait on them
+            if (c == 2 && early) us::pdl_wait();
             if (lane == 0) {
                 if (c >= 2 && !us::mbar_wait(&S.empty[b], ((c >> 1) - 1) & 1, p.status)) {
                     S.abort = 1;
@@ -173,7 +152,7 @@ w4a4_small_n_kernel(const UsKParams p) {
         // ---------------------------------------------------------- consumers
         // selector table, kLutRep copies (bank spreading)
         for (int e = threadIdx.x; e < 256; e += kConsumerThreads) {
-            const uint32_t sel = make_sel((uint32_t)e);
+            const uint32_t sel = us::make_sel((uint32_t)e);
 #pragma unroll
             for (int r = 0; r < kLutRep; ++r) lut[e * kLutRep + r] = sel;
         }
@@ -232,16 +211,22 @@ w4a4_small_n_kernel(const UsKParams p) {
                     const uint64_t w = h ? wB : wA;
                     const uint32_t o = h ? totA + (ex >> 16) : (ex & 0xFFFFu);
                     const uint32_t lo = (uint32_t)w, hi = (uint32_t)(w >> 32);
-                    int wi = (int)(o >> 3);
-                    uint32_t sh = (o & 7u) << 2;
-                    uint32_t cur = vw[wi], nxt = vw[wi + 1];
+                    const uint32_t plo = (uint32_t)__popc(lo);
+                    // eight independent byte-steps: each finds its own place in the
+                    // run (row base + popcount of the lower bits), so all are in flight
 #pragma unroll
                     for (int bt = 0; bt < 8; ++bt) {
                         const uint32_t bb = ((bt < 4 ? lo : hi) >> (8 * (bt & 3))) & 0xFFu;
+                        const uint32_t below =
+                            bt == 0 ? 0u
+                                    : (bt < 4 ? (uint32_t)__popc(lo & ((1u << (8 * bt)) - 1u))
+                                              : plo + (bt == 4 ? 0u : (uint32_t)__popc(hi & ((1u << (8 * (bt - 4))) - 1u))));
+                        const uint32_t ob = o + below;
                         const uint32_t sel = lut[bb * kLutRep + lut_lane];
                         const uint32_t c4 = (uint32_t)__popc(bb) << 2;
-                        const uint32_t nib = __funnelshift_r(cur, nxt, sh);
-                        const uint32_t nm = nib & ~shl_clamp(0xFFFFFFFFu, c4);   // first c nibbles
+                        const uint32_t wi = ob >> 3;
+                        const uint32_t nm = __funnelshift_r(vw[wi], vw[wi + 1], ob << 2) &
+                                            ~us::shl_clamp(0xFFFFFFFFu, c4);           // first c nibbles
                         const uint32_t odd = nm & 0xF0F0F0F0u;                   // 16 * w of ranks 1,3,5,7
                         const uint32_t even = (nm << 4) & 0xF0F0F0F0u;           // 16 * w of ranks 0,2,4,6
                         const int d0 = (int)__byte_perm(even, odd, sel);
@@ -251,13 +236,6 @@ w4a4_small_n_kernel(const UsKParams p) {
                             const uint2 xv = *reinterpret_cast<const uint2*>(xt + (int64_t)n * krange + 8 * bt);
                             acc[h][n] = __dp4a(d0, (int)xv.x, acc[h][n]);
                             acc[h][n] = __dp4a(d1, (int)xv.y, acc[h][n]);
-                        }
-                        sh += c4;
-                        if (sh >= 32u) {
-                            sh -= 32u;
-                            cur = nxt;
-                            ++wi;
-                            nxt = vw[wi + 1];
                         }
                     }
                 }
@@ -312,8 +290,9 @@ w4a4_small_n_kernel(const UsKParams p) {
     if (p.split > 1) {
         us::cluster_sync();
         const int rank = (int)us::cluster_ctarank();
-        const int chunk = N * kTM / p.split;
-        for (int i = rank * chunk + threadIdx.x; i < (rank + 1) * chunk; i += kThreads) {
+        // rank r reduces elements [r*total/split, (r+1)*total/split): any split, no remainder lost
+        const int i0 = rank * (N * kTM) / p.split, i1 = (rank + 1) * (N * kTM) / p.split;
+        for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
             int a = 0;
             for (int r = 0; r < p.split; ++r) a += us::ld_cluster_s32(us::cluster_map(outv + i, (uint32_t)r));
             store(i, a);

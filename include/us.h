@@ -129,7 +129,10 @@ us_status us_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK,
  * packed like `values` (element n*K + k); requires K % 32 == 0.
  * s_w: M fp16 bit patterns, s_x: N fp16.  Yacc: N x M int32, Y: N x M fp16.
  * 1 <= N <= 2048.  split_k: 0 = automatic, else K tiles are split into that
- * many slices (1..nTK).  Results do not depend on split_k. */
+ * many slices (1..nTK).  Results do not depend on split_k.  With 64 x 64 tiles
+ * and N <= 8 the automatic choice slices nothing: the tile sequence is spread
+ * evenly over the SMs and a band shared by several CTAs is finished by the last
+ * one to arrive (arrival counters in the workspace). */
 us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_w,
                        const uint16_t* s_x, int N, int32_t* Yacc, uint16_t* Y,
                        void* ws, size_t ws_bytes, int split_k, void* stream);
@@ -176,7 +179,8 @@ us_status us_workspace_bytes(us_op op, const us_bitmap* W, int N, int split_k, s
 /* The split_k the automatic rule picks for (op, W, N) on the current device:
  * the smallest of {1,2,4,8,16} whose grid fills every SM, while each slice
  * keeps at least 4 K tiles (split-K rule of "Realizable N:M Sparse
- * Transformer Inference via Search-Kernel Co-Design", section 4.3). */
+ * Transformer Inference via Search-Kernel Co-Design", section 4.3); 0 when the
+ * automatic choice spreads the tiles evenly instead (see us_spmm_w4a4). */
 us_status us_pick_split_k(us_op op, const us_bitmap* W, int N, int* split_k);
 
 /* Host-side check of an encoded matrix.  W's three pointers are HOST

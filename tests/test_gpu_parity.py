@@ -139,9 +139,15 @@ W4A4_CASES = [
     (192, 320, 64, 16, 7, 0.5, 4),
     (128, 1024, 64, 64, 1, 1.0, 16),
     (128, 512, 64, 64, 64, 0.05, 0),
-    (256, 512, 64, 64, 13, 0.5, 0),      # token blocks 8 + 5
+    (256, 512, 64, 64, 13, 0.5, 0),      # tensor path: 13 tokens padded to 16
     (256, 1024, 64, 64, 32, 0.5, 4),
-    (192, 768, 64, 64, 24, 0.3, 0),
+    (192, 768, 64, 64, 24, 0.3, 0),      # M % 128 != 0: CUDA-core path, token blocks 8+8+8
+    (384, 2048, 64, 64, 17, 0.5, 0),     # tensor path, BN = 32
+    (128, 4096, 64, 64, 8, 1.0, 8),      # tensor path, full tiles, 8-slice cluster
+    (256, 640, 64, 64, 9, 0.05, 3),      # tensor path, nearly empty tiles, uneven slices
+    (320, 640, 64, 64, 4, 0.7, 3),       # cluster of 3: 256 outputs do not divide by 3
+    (256, 640, 64, 64, 16, 0.3, 3),      # tensor path, cluster of 3 over 2048 outputs
+    (128, 16384, 64, 64, 32, 0.2, 1),    # one slice: packed activations too large for the tensor path
 ]
 
 
@@ -160,16 +166,65 @@ def test_w4a4_matches_oracle(us, orc, case):
     assert np.array_equal(y.view(np.uint16), oy.view(np.uint16))
 
 
-def test_w4a4_extreme_values_exact(us, orc):
-    """All weights and activations -8: the largest accumulators (64*K)."""
-    M, K = 128, 2048
+# Shapes for the balanced W4A4 kernel (automatic choice, 64 x 64 tiles, N <= 8):
+# bands shared by two or three CTAs, one CTA spanning several bands (K of one
+# tile), fewer tiles than SMs, K wider than a CTA's range, ragged everything.
+SK_SHAPES = [
+    # M, K, N, density
+    (64 * 200, 64, 3, 0.5),        # nTK = 1: every CTA covers whole bands
+    (128, 64 * 300, 1, 0.4),       # two bands, 300 K tiles: each band split over ~76 CTAs
+    (192, 64 * 7, 8, 0.6),         # 21 tiles: fewer tiles than SMs, one tile per CTA
+    (64 * 37, 64 * 13, 5, 0.3),    # 481 tiles: ranges of 3-4 tiles crossing band edges
+    (64 * 9, 64 * 61, 2, 0.9),     # dense runs: the value ring wraps many times
+    (64 * 3, 64 * 5, 7, 0.0),      # all tiles empty
+]
+
+
+@pytest.mark.parametrize("M,K,N,dens", SK_SHAPES)
+def test_w4a4_balanced_partition(us, orc, M, K, N, dens):
+    """Automatic W4A4 path for few tokens against the oracle, three times in a
+    row (the posted partial sums of shared bands must be cleared for the next
+    call), and against an explicit K split, which takes the cluster kernel."""
+    rng = np.random.default_rng(M + K + N)
+    W = rand_i4(rng, M, K, dens)
+    Xq = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
+    s_x = (rng.random(N) * 0.5 + 0.05).astype(np.float16)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    assert us.us_pick_split_k(us.US_OP_SPMM_W4A4, E, N) == 0
+    Xp = wl.pack_int4(Xq)
+    dev = "cuda"
+    X = torch.from_numpy(Xp).to(dev)
+    sw = torch.from_numpy(s_w.view(np.int16)).to(dev)
+    sx = torch.from_numpy(s_x.view(np.int16)).to(dev)
+    ws = us.workspace(us.US_OP_SPMM_W4A4, E, N, 0)
+    oacc, oy = orc.spmm_w4a4(W, Xq, s_w, s_x)
+    for _ in range(3):
+        Yacc = torch.full((N, M), 12345, dtype=torch.int32, device=dev)
+        Y = torch.empty(N, M, dtype=torch.int16, device=dev)
+        us.us_spmm_w4a4(E, X, sw, sx, N, Yacc, Y, ws, 0)
+        torch.cuda.synchronize()
+        assert us.us_get_last_device_status() == us.US_OK
+        assert np.array_equal(Yacc.cpu().numpy(), oacc)
+        assert np.array_equal(Y.cpu().numpy().view(np.uint16), oy.view(np.uint16))
+    assert torch.count_nonzero(ws).item() == 0                    # every posted partial cleared
+    acc2, _ = run_w4a4(us, E, Xp, s_w, s_x, N, split_k=min(2, K // 64))
+    assert np.array_equal(acc2, oacc)
+
+
+@pytest.mark.parametrize("N", [4, 16, 32])
+def test_w4a4_extreme_values_exact(us, orc, N):
+    """All weights and activations -8: the largest accumulators (64*K); both the
+    CUDA-core (N = 4) and the tensor-core (N = 16, 32) paths must stay exact."""
+    M, K = 128, 8192
     W = np.full((M, K), -8, np.int8)
     W[::3, ::5] = 7
-    X = np.full((4, K), -8, np.int8)
+    X = np.full((N, K), -8, np.int8)
+    X[1::2, ::7] = 7
     one = np.ones(M, np.float16)
     E = encode_gpu(us, W, 64, 64, I4, ROW)
-    acc, _ = run_w4a4(us, E, wl.pack_int4(X), one, np.ones(4, np.float16), 4, want_y=False)
-    oacc, _ = orc.spmm_w4a4(W, X, one, np.ones(4, np.float16))
+    acc, _ = run_w4a4(us, E, wl.pack_int4(X), one, np.ones(N, np.float16), N, want_y=False)
+    oacc, _ = orc.spmm_w4a4(W, X, one, np.ones(N, np.float16))
     assert np.array_equal(acc, oacc)
 
 
