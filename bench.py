@@ -355,6 +355,23 @@ def kernel_name(N: int) -> str:
     return "spmm_generic_kernel<I4,64>"
 
 
+KERNEL_SOURCES = {"w4a4_sk_kernel": "us_w4a4_sk.cu", "w4a4_tc_kernel": "us_tc.cu",
+                  "w4a4_small_n_kernel": "us_w4a4.cu", "spmm_generic_kernel": "us_spmm.cu"}
+
+
+def kernel_source_sha(kernel: str):
+    """sha256 over the kernel's translation unit and the shared device header."""
+    import hashlib
+    src = KERNEL_SOURCES.get(kernel.split("<")[0])
+    if not src:
+        return None
+    h = hashlib.sha256()
+    for f in (src, "us_common.cuh"):
+        with open(os.path.join(ROOT, "bitmap_encoded_unstructured_ie_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_traffic(kernel: str):
     """Per-launch DRAM bytes of this kernel from the committed ncu summary, if
     it was taken on the current kernel source (else null)."""
@@ -363,7 +380,7 @@ def load_traffic(kernel: str):
         with open(path) as f:
             d = json.load(f)
         ent = d.get(kernel)
-        if not ent:
+        if not ent or ent.get("source_sha256") != kernel_source_sha(kernel):
             return None
         return ent.get("dram_bytes_per_launch")
     except Exception:
