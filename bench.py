@@ -348,14 +348,15 @@ def main():
 
 def kernel_name(N: int) -> str:
     """The kernel the library dispatches for W4A4 64x64 tiles at N tokens."""
-    if N <= 8:
-        return f"w4a4_sk_kernel<{N}>"
+    if N <= 7:
+        return f"w4a4_sk_kernel<{N},0>"             # dp4a consumer
     if N <= 32:
-        return f"w4a4_tc_kernel<{16 if N <= 16 else 32}>"
+        nt = 1 if N <= 8 else (2 if N <= 16 else 4)
+        return f"w4a4_sk_kernel<{8 * nt},{nt}>"      # mma.sync consumer, 8-token blocks
     return "spmm_generic_kernel<I4,64>"
 
 
-KERNEL_SOURCES = {"w4a4_sk_kernel": "us_w4a4_sk.cu", "w4a4_tc_kernel": "us_tc.cu",
+KERNEL_SOURCES = {"w4a4_sk_kernel": "us_w4a4_sk.cu",
                   "w4a4_small_n_kernel": "us_w4a4.cu", "spmm_generic_kernel": "us_spmm.cu"}
 
 

@@ -97,7 +97,6 @@ struct Plan {
     bool sk;        // W4A4 CUDA-core kernel over a balanced partition of the tiles
     bool fast;      // W4A4 register-decode kernel
     bool tc;        // fp16 tensor-core kernel
-    bool tcw;       // W4A4 tensor-core kernel
     int split;
     int tok_block;
     size_t ws;
@@ -105,22 +104,15 @@ struct Plan {
 
 Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
     Plan pl{};
-    if (op == US_OP_SPMM_W4A4 && split_k == 0 && us::w4a4_sk_supported(W->TM, W->TK, W->M, W->K, N)) {
-        pl.sk = true;
-        pl.split = 0;                               // no K slices: tiles spread evenly over the SMs
-        pl.tok_block = N;
-        pl.ws = us::w4a4_sk_ws(W->M, W->K, N);
-        return pl;
-    }
-    if (op == US_OP_SPMM_W4A4 && us::tc_w4a4_supported(W->TM, W->TK, W->M, W->K, N) &&
-        split_k <= us::w4a4_fast_max_split()) {
-        pl.tcw = true;
-        pl.tok_block = N;
-        pl.split = split_k > 0 ? split_k : us::tc_w4a4_split(W->M, N, W->K / W->TK);
-        if (pl.split > W->K / W->TK) pl.split = W->K / W->TK;
-        pl.ws = 0;                                  // split-K reduces inside the cluster
-        if (us::tc_w4a4_fits(N, W->K / W->TK, pl.split)) return pl;
-        pl = Plan{};                                // activations of a slice too large: CUDA-core path
+    // W4A4, automatic split: the balanced kernels (no K slices; tiles spread
+    // evenly over the SMs)
+    if (op == US_OP_SPMM_W4A4 && split_k == 0) {
+        if (us::w4a4_sk_supported(W->TM, W->TK, W->M, W->K, N)) {
+            pl.sk = true;
+            pl.tok_block = N;
+            pl.ws = us::w4a4_sk_ws(W->M, W->K, N);
+            return pl;
+        }
     }
     if (op == US_OP_SPMM_F16 && us::tc_f16_supported(W->TM, W->TK, W->M, N)) {
         pl.tc = true;
@@ -275,7 +267,6 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
         p.ws = ws;
         return us::launch_w4a4_sk(p, st);
     }
-    if (pl.tcw) return us::launch_tc_w4a4(p, st);
     return pl.fast ? us::launch_w4a4_fast(p, st) : us::launch_spmm_generic(p, US_I4, st);
 }
 

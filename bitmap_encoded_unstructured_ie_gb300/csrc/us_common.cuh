@@ -185,6 +185,36 @@ US_DEV void lds_u32_if(uint32_t& v, uint32_t pred, uint32_t addr) {
         : "r"(pred), "r"(addr));
 }
 
+// Bytes (w + 8) of ranks 0,2,4,6 (even) and 1,3,5,7 (odd) -> eight fp16 values
+// at the positions the PRMT selector pair names: 0x6400 | (w + 8) is the fp16
+// number 1024 + w + 8, minus 1032 leaves w exactly.
+US_DEV uint4 u8x8_to_f16x8(uint32_t even, uint32_t odd, uint32_t sel) {
+    const uint32_t d0 = __byte_perm(even, odd, sel);
+    const uint32_t d1 = __byte_perm(even, odd, sel >> 16);
+    const uint32_t k64 = 0x64646464u;
+    const uint32_t b[4] = {__byte_perm(d0, k64, 0x5140), __byte_perm(d0, k64, 0x7362),
+                           __byte_perm(d1, k64, 0x5140), __byte_perm(d1, k64, 0x7362)};
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&b[i]), bias);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// d += A . B for one m16n8k16 tile: fp16 A (row-major fragment a0..a3), fp16 B
+// (column-major fragment b0, b1), fp32 accumulators.
+US_DEV void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                             uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Byte-step decode of packed int4 runs (used by the W4A4 kernels).  For one
 // bitmap byte v (8 positions) the run's next popc(v) nibbles are split into
 // even and odd ranks, one byte each; make_sel(v) is the PRMT selector pair

@@ -35,6 +35,7 @@ int w4a4_fast_max_split();
 // (us_w4a4_sk.cu); launch_w4a4_sk takes p.ws = start of the workspace
 bool w4a4_sk_supported(int TM, int TK, int M, int K, int N);
 size_t w4a4_sk_ws(int M, int K, int N);
+int w4a4_sk_variant(int N);   // 0: dp4a consumer, else the mma consumer's 8-token blocks
 us_status launch_w4a4_sk(UsKParams p, cudaStream_t st);
 
 // tensor-core fp16 SpMM for many tokens (us_tc.cu)
@@ -43,10 +44,7 @@ int tc_tok_block();
 int tc_split(int M, int N, int nTK);
 size_t tc_ws(int M, int N, int split);
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
-bool tc_w4a4_supported(int TM, int TK, int M, int K, int N);
-bool tc_w4a4_fits(int N, int nTK, int split);   // shared memory of one CTA within the limit
-int tc_w4a4_split(int M, int N, int nTK);
-us_status launch_tc_w4a4(const UsKParams& p, cudaStream_t st);
+
 
 // spMspV (us_spmspv.cu)
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st);

@@ -212,6 +212,47 @@ def test_w4a4_balanced_partition(us, orc, M, K, N, dens):
     assert np.array_equal(acc2, oacc)
 
 
+# Shapes for the balanced kernel's tensor-core consumer (automatic choice, 64 x
+# 64 tiles, 8..32 tokens: decoded tiles feed mma.sync in 8-token blocks; fewer
+# tokens use dp4a).
+TC_SHAPES = [
+    # M, K, N, density
+    (128 * 100, 64, 8, 0.5),       # nTK = 1: 200 tiles over 152 CTAs, bands whole or split in two
+    (256, 64 * 300, 16, 0.4),      # four bands of 300 tiles: owners add ~38 posts each
+    (128 * 9, 64 * 61, 12, 0.9),   # dense runs, 1098 tiles: ranges cross band edges
+    (128 * 3, 64 * 5, 20, 0.3),    # 30 tiles, 20 tokens padded to 32
+    (128 * 7, 64 * 33, 32, 0.6),   # 462 tiles, 32 tokens
+    (192, 64 * 6, 9, 0.0),         # all tiles empty, 9 tokens padded to 16
+]
+
+
+@pytest.mark.parametrize("M,K,N,dens", TC_SHAPES)
+def test_w4a4_tensor_cores_balanced(us, orc, M, K, N, dens):
+    """Automatic W4A4 path with the mma.sync consumer against the oracle, three
+    calls in a row on one workspace (posted partials must be cleared each time)."""
+    rng = np.random.default_rng(M * 7 + K + N)
+    W = rand_i4(rng, M, K, dens)
+    Xq = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
+    s_x = (rng.random(N) * 0.5 + 0.05).astype(np.float16)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    dev = "cuda"
+    X = torch.from_numpy(wl.pack_int4(Xq)).to(dev)
+    sw = torch.from_numpy(s_w.view(np.int16)).to(dev)
+    sx = torch.from_numpy(s_x.view(np.int16)).to(dev)
+    ws = us.workspace(us.US_OP_SPMM_W4A4, E, N, 0)
+    oacc, oy = orc.spmm_w4a4(W, Xq, s_w, s_x)
+    for _ in range(3):
+        Yacc = torch.full((N, M), -777, dtype=torch.int32, device=dev)
+        Y = torch.empty(N, M, dtype=torch.int16, device=dev)
+        us.us_spmm_w4a4(E, X, sw, sx, N, Yacc, Y, ws, 0)
+        torch.cuda.synchronize()
+        assert us.us_get_last_device_status() == us.US_OK
+        assert np.array_equal(Yacc.cpu().numpy(), oacc)
+        assert np.array_equal(Y.cpu().numpy().view(np.uint16), oy.view(np.uint16))
+    assert torch.count_nonzero(ws).item() == 0
+
+
 @pytest.mark.parametrize("N", [4, 16, 32])
 def test_w4a4_extreme_values_exact(us, orc, N):
     """All weights and activations -8: the largest accumulators (64*K); both the
