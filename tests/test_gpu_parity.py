@@ -397,6 +397,28 @@ def test_spmspv_matches_oracle(us, orc, TM, TK, zero_frac, tau):
     check_f16(y, exact, f"spmspv TM={TM} TK={TK} tau={tau}")
 
 
+@pytest.mark.parametrize("M,K,TM,TK", [(64 * 400, 128, 64, 64), (512, 64 * 97, 64, 64), (1024, 1024, 128, 32)])
+def test_spmspv_repeat(us, orc, M, K, TM, TK):
+    """spMspV on tall, wide and mid-sized shapes (bands with one or several K
+    slices): three calls on one workspace give bitwise identical results
+    (fixed-order sums) and leave the workspace zero."""
+    d = wl.spmspv(M, K, 0.5, 0.6, seed=M + K)
+    E = encode_gpu(us, d["W"], TM, TK, F16, COL)
+    xt = torch.from_numpy(d["x"].view(np.int16)).cuda()
+    ws = us.workspace(us.US_OP_SPMSPV_F16, E, 1)
+    outs = []
+    for _ in range(3):
+        y = torch.full((M,), 0x7E00, dtype=torch.int16, device="cuda")   # NaN until written
+        us.us_spmspv_f16(E, xt, 0.0, y, ws)
+        torch.cuda.synchronize()
+        assert us.us_get_last_device_status() == us.US_OK
+        outs.append(y.cpu().numpy())
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    assert torch.count_nonzero(ws).item() == 0
+    _, exact = orc.spmspv_f16(d["W"], d["x"], 0.0)
+    check_f16(outs[0].view(np.float16), exact, f"spmspv repeat {M}x{K}")
+
+
 # --------------------------------------------------------- full-size shapes --
 @pytest.mark.parametrize("s", [0.3, 0.5, 0.7])
 def test_w4a4_4096_full(us, orc, s):
