@@ -257,10 +257,11 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
             us::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
             if (!ready) continue;
             if (p.split > 1) {
-                const int64_t base = (((int64_t)slice * nTB + nt) * p.M + m) * kBN + c0;
+                // partials token-major, [slice][token tile][n][m]: a warp's 32 lanes
+                // (rows) store 128 contiguous bytes per column
+                const int64_t base = (((int64_t)slice * nTB + nt) * kBN + c0) * p.M + m;
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    __stcg(reinterpret_cast<float4*>(part + base + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+                for (int i = 0; i < 32; ++i) __stcg(part + base + (int64_t)i * p.M, v[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -281,18 +282,36 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         __syncthreads();
         if (!S.flag) return;
         __threadfence();
-        // the last CTA of this output tile: sum the slices in order, leave zeros behind
+        // the last CTA of this output tile sums the slices in fixed order: four
+        // consecutive rows per thread (float4), every slice's load in flight at
+        // once, outputs written row-contiguous; the partials are cleared behind
+        // (a workspace may be shared with kernels that need it all zero)
         float* part = reinterpret_cast<float*>(p.ws);
-        for (int idx = threadIdx.x; idx < kBM * kBN; idx += kThreads) {
-            const int mr = idx / kBN, nc = idx - mr * kBN;
+        // every column is cleared (the slices wrote all kBN of them, padding -0.0
+        // included); outputs only for real tokens
+        for (int idx = threadIdx.x; idx < kBN * (kBM / 4); idx += kThreads) {
+            const int nc = idx / (kBM / 4), mr = (idx - nc * (kBM / 4)) * 4;
             const int m = mt * kBM + mr, n = nt * kBN + nc;
-            float acc = 0.f;
-            for (int sl = 0; sl < p.split; ++sl) {
-                float* src = part + (((int64_t)sl * tp.n_tiles + nt) * p.M + m) * kBN + nc;
-                acc += __ldcg(src);
-                __stcg(src, 0.f);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int s0 = 0; s0 < p.split; s0 += 8) {
+                float4 w[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s0 + u < p.split)
+                        w[u] = __ldcg(reinterpret_cast<float4*>(
+                            part + (((int64_t)(s0 + u) * tp.n_tiles + nt) * kBN + nc) * p.M + m));
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (s0 + u < p.split) {
+                        acc.x += w[u].x; acc.y += w[u].y; acc.z += w[u].z; acc.w += w[u].w;
+                        __stcg(reinterpret_cast<float4*>(part + (((int64_t)(s0 + u) * tp.n_tiles + nt) * kBN + nc) * p.M + m),
+                               make_float4(0.f, 0.f, 0.f, 0.f));
+                    }
             }
-            if (n < p.N) p.Y[(int64_t)n * p.M + m] = us::float_to_half_bits(acc);
+            if (n >= p.N) continue;
+            const uint32_t lo = (uint32_t)us::float_to_half_bits(acc.x) | ((uint32_t)us::float_to_half_bits(acc.y) << 16);
+            const uint32_t hi = (uint32_t)us::float_to_half_bits(acc.z) | ((uint32_t)us::float_to_half_bits(acc.w) << 16);
+            *reinterpret_cast<uint2*>(p.Y + (int64_t)n * p.M + m) = make_uint2(lo, hi);
         }
         if (threadIdx.x == 0) p.counters[mt * tp.n_tiles + nt] = 0u;
     }

@@ -476,6 +476,7 @@ def test_one_workspace_shared_across_calls(us, orc):
     Ef = encode_gpu(us, Wf, 64, 64, F16, ROW)
     need = max(us.us_workspace_bytes(us.US_OP_SPMM_W4A4, E, n, s) for n in (1, 5, 13, 40) for s in (0, 2, 4))
     need = max(need, us.us_workspace_bytes(us.US_OP_SPMM_F16, Ef, 40, 4))
+    need = max(need, us.us_workspace_bytes(us.US_OP_SPMM_F16, Ef, 100, 2))
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
     one = np.ones(256, np.float16)
     for N, split in [(5, 4), (40, 2), (1, 0), (13, 4), (5, 2), (40, 4), (1, 4)]:
@@ -490,6 +491,13 @@ def test_one_workspace_shared_across_calls(us, orc):
         n_idx, m_idx = np.meshgrid(np.arange(N), np.arange(256), indexing="ij")
         _, exact = orc.spmm_f16_at(Wf, X, n_idx.reshape(-1), m_idx.reshape(-1))
         check_f16(Y.cpu().numpy().view(np.float16).reshape(-1), exact, f"shared ws N={N}")
+    # tensor-core fp16 path with split-K and a ragged token tile: partials cleared too
+    X = rng.standard_normal((100, 1024)).astype(np.float16)
+    Y = torch.empty(100, 256, dtype=torch.int16, device="cuda")
+    us.us_spmm_f16(Ef, torch.from_numpy(X.view(np.int16)).cuda(), 100, Y, ws, 2)
+    n_idx, m_idx = np.meshgrid(np.arange(100), np.arange(256), indexing="ij")
+    _, exact = orc.spmm_f16_at(Wf, X, n_idx.reshape(-1), m_idx.reshape(-1))
+    check_f16(Y.cpu().numpy().view(np.float16).reshape(-1), exact, "shared ws tensor path")
     assert not ws.any().item(), "workspace not left zeroed"
 
 
