@@ -506,6 +506,16 @@ def measure_extras(us, torch, wl, dev, stream):
         fl = 2 * 4096 * 4096 * N
         pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_4096_s60"] = pf
+    # per-token activation quantisation, fp16 -> int4 + scale (reads 2NK, writes NK/2 + 2N bytes)
+    qz = {}
+    for N in (16, 2048):
+        Xh = torch.from_numpy(np.random.default_rng(4).standard_normal((N, 4096)).astype(np.float16).view(np.int16)).to(dev)
+        Xq = torch.empty(N, 2048, dtype=torch.uint8, device=dev)
+        sq = torch.empty(N, dtype=torch.int16, device=dev)
+        ms = time_graph(torch, stream, lambda: us.us_quantize_x(Xh, N, 4096, Xq, sq, stream), 20)
+        byt = N * 4096 * 2 + N * 2048 + N * 2
+        qz[str(N)] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1)}
+    out["quantize_x_k4096"] = qz
     return out
 
 

@@ -6,7 +6,7 @@ library has not been built, the first call raises ``LibraryMissing``: there is
 no CPU fallback.
 
 Function names follow the C ABI: ``us_encode``, ``us_spmm_w4a4``,
-``us_spmm_f16``, ``us_spmspv_f16``, ``us_workspace_bytes``, ``us_pick_split_k``,
+``us_spmm_f16``, ``us_spmspv_f16``, ``us_quantize_x``, ``us_workspace_bytes``, ``us_pick_split_k``,
 ``us_validate``, ``us_get_last_device_status``.
 """
 from __future__ import annotations
@@ -29,6 +29,7 @@ US_OP_ENCODE, US_OP_SPMM_W4A4, US_OP_SPMM_F16, US_OP_SPMSPV_F16 = 0, 1, 2, 3
 US_BITMAP_STATIC = 1
 
 EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmm_f16_noalloc", "us_spmspv_f16",
+            "us_quantize_x",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
             "us_status_string", "us_version")
 
@@ -73,6 +74,7 @@ def load(path: str = LIB_PATH):
         lib.us_spmm_f16.argtypes = [pbm, P, i32, P, P, sz, i32, P]
         lib.us_spmm_f16_noalloc.argtypes = [pbm, P, i32, P, i32, P]
         lib.us_spmspv_f16.argtypes = [pbm, P, ctypes.c_float, P, P, sz, P]
+        lib.us_quantize_x.argtypes = [P, i32, i32, P, P, P]
         lib.us_workspace_bytes.argtypes = [i32, pbm, i32, i32, psz]
         lib.us_pick_split_k.argtypes = [i32, pbm, i32, ctypes.POINTER(ctypes.c_int)]
         lib.us_validate.argtypes = [pbm]
@@ -225,6 +227,12 @@ def us_spmspv_f16(E: Encoded, x: torch.Tensor, tau: float, y: torch.Tensor, ws: 
     d = E.desc()
     _check("us_spmspv_f16", load().us_spmspv_f16(ctypes.byref(d), _dptr(x), float(tau), _dptr(y), _dptr(ws),
                                                  ws.numel(), _stream(stream)))
+
+
+def us_quantize_x(X: torch.Tensor, N: int, K: int, Xq: torch.Tensor, s_x: torch.Tensor, stream=None):
+    """fp16 activations (N x K, token-major) -> packed int4 codes (N x K/2 bytes)
+    and one fp16 scale per token."""
+    _check("us_quantize_x", load().us_quantize_x(_dptr(X), N, K, _dptr(Xq), _dptr(s_x), _stream(stream)))
 
 
 def us_validate_host(bitmap, tile_off, values, M, K, TM, TK, elem, order) -> int:

@@ -364,6 +364,13 @@ us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16
     return us::launch_spmspv(p, static_cast<cudaStream_t>(stream));
 }
 
+us_status us_quantize_x(const uint16_t* X, int N, int K, uint8_t* Xq, uint16_t* s_x, void* stream) {
+    if (N < 1 || K < 32 || K % 32 || (int64_t)N * K >= ((int64_t)1 << 32)) return US_ERR_INVALID_ARG;
+    if (!X || !Xq || !s_x || !aligned16(X) || !aligned16(Xq)) return US_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(s_x) & 1u) != 0) return US_ERR_INVALID_ARG;
+    return us::launch_quantize_x(X, N, K, Xq, s_x, static_cast<cudaStream_t>(stream));
+}
+
 us_status us_validate(const us_bitmap* W) {
     if (!W) return US_ERR_INVALID_ARG;
     us_status s = check_shape(W->M, W->K, W->TM, W->TK, W->elem);

@@ -51,6 +51,9 @@ us_status launch_spmspv(const UsKParams& p, cudaStream_t st);
 size_t spmspv_ws(int M, int TM, int split);
 int spmspv_max_split();
 
+// per-token int4 quantisation of fp16 activations (us_quant.cu)
+us_status launch_quantize_x(const uint16_t* X, int N, int K, uint8_t* Xq, uint16_t* s_x, cudaStream_t st);
+
 // device properties of the current device (cached)
 int num_sms();
 

@@ -172,6 +172,17 @@ us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint
 us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* Per-token int4 quantisation of fp16 activations (UnionSparse Fig. 2, the
+ * "Quant" step from FP16 X to INT4 X with a per-token scale; the page does not
+ * fix the rounding, this is the plain symmetric reading):
+ *   s_x[n]   = fp16_rn(max_k |X[n][k]| / 7)   (fp32 division), 1 if that is 0
+ *   Xq[n][k] = clamp(rint(X[n][k] / s_x[n]), -8, 7)   (fp32 division, ties to even)
+ * X: N x K fp16 token-major.  Xq: N x K int4 packed like us_spmm_w4a4's Xq
+ * (element n*K + k in byte (n*K + k) >> 1, even elements in the low nibble).
+ * s_x: N fp16.  1 <= N, K % 32 == 0.  NaN does not take part in the maximum and
+ * gives code 0.  One pass over X: its output feeds us_spmm_w4a4 directly. */
+us_status us_quantize_x(const uint16_t* X, int N, int K, uint8_t* Xq, uint16_t* s_x, void* stream);
+
 /* Workspace bytes for `op` on W with N tokens and the given split_k
  * (0 = the automatic choice).  For US_OP_ENCODE only W->M, K, TM, TK are read. */
 us_status us_workspace_bytes(us_op op, const us_bitmap* W, int N, int split_k, size_t* bytes);

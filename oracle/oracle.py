@@ -87,6 +87,7 @@ def _load():
         lib.or_spmm_f16.argtypes = [P, P, i32, i32, i32, P, i32]
         lib.or_spmm_f16_at.argtypes = [P, P, i32, i32, i32, P, P, i64, P, P]
         lib.or_spmspv_f16.argtypes = [P, P, ctypes.c_float, i32, i32, P, P, i32]
+        lib.or_quantize_x.argtypes = [P, i32, i32, P, P]
         lib.or_max_threads.argtypes = []
         for name in ("or_num_tiles", "or_encode", "or_decode", "or_spmm_w4a4", "or_spmm_w4a4_at",
                      "or_spmm_f16", "or_spmm_f16_at", "or_spmspv_f16", "or_max_threads"):
@@ -250,3 +251,14 @@ def spmspv_f16(Wd: np.ndarray, x: np.ndarray, tau: float = 0.0, nthreads: int = 
     _check(_load().or_spmspv_f16(_ptr(Wd), _ptr(x), float(tau), M, K, _ptr(y), _ptr(ex), nthreads),
            "spmspv_f16")
     return y.view(np.float16), ex
+
+
+def quantize_x(X: np.ndarray):
+    """Per-token int4 quantisation of fp16 activations (UnionSparse Fig. 2,
+    "Quant"): codes int8 in [-8, 7] (N x K) and s_x fp16 (N)."""
+    Xh = np.ascontiguousarray(_f16bits(np.atleast_2d(X)))
+    N, K = Xh.shape
+    codes = np.zeros((N, K), np.int8)
+    s = np.zeros(N, np.uint16)
+    _check(_load().or_quantize_x(_ptr(Xh), N, K, _ptr(codes), _ptr(s)), "or_quantize_x")
+    return codes, s.view(np.float16)

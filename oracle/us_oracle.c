@@ -345,6 +345,40 @@ int or_spmspv_f16(const uint16_t* Wd, const uint16_t* x, float tau, int M, int K
     return OR_OK;
 }
 
+/* ------------------------------------------- activation quantisation ---- */
+/* Per-token symmetric int4 quantisation of fp16 activations ([UnionSparse]
+ * Fig. 2, the "Quant" step between FP16 X and INT4 X; the page fixes the
+ * per-token scale, not its rounding, so the plain reading is used):
+ *   amax = max_k |x[n][k]|                       (fp16 values are exact in fp32)
+ *   s_x[n] = fp16_rn(amax / 7)                   (fp32 division), 1 if that is 0
+ *   code[n][k] = clamp(rint(x[n][k] / s_x[n]), -8, 7)
+ *                                                (fp32 division, ties to even)
+ * NaN inputs do not take part in amax and give code 0. */
+int or_quantize_x(const uint16_t* X, int N, int K, int8_t* codes, uint16_t* s_x) {
+    if (N < 0 || K < 0 || (N * (int64_t)K > 0 && (!X || !codes || !s_x))) return OR_BAD_ARG;
+    for (int n = 0; n < N; ++n) {
+        const uint16_t* x = X + (int64_t)n * K;
+        float amax = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            const float a = fabsf(or_half_to_float(x[k]));
+            if (a > amax) amax = a;             /* NaN compares false */
+        }
+        uint16_t s16 = or_float_to_half(amax / 7.0f);
+        if ((s16 & 0x7FFFu) == 0) s16 = 0x3C00u;   /* 1.0 */
+        s_x[n] = s16;
+        const float s = or_half_to_float(s16);
+        for (int k = 0; k < K; ++k) {
+            const float v = or_half_to_float(x[k]);
+            float q = rintf(v / s);             /* default rounding mode: to nearest even */
+            if (!(q == q)) q = 0.0f;
+            if (q < -8.0f) q = -8.0f;
+            if (q > 7.0f) q = 7.0f;
+            codes[(int64_t)n * K + k] = (int8_t)q;
+        }
+    }
+    return OR_OK;
+}
+
 int or_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -123,3 +123,9 @@ def test_bad_arguments_rejected_without_launch(lib):
     assert L.us_spmm_w4a4(ctypes.byref(odd), X, None, None, 1, Y, None, ws, 1 << 20, 0, None) == 1  # K % 32
     assert L.us_encode(None, 64, 64, 64, 64, 64, 0, 0, P(16), P(32), P(48), 100, P(64), 1 << 20, None) == 1
     assert L.us_encode(P(16), 64, 64, 64, 64, 64, 0, 0, P(16), P(32), P(48), 100, P(64), 4, None) == 4
+    # activation quantisation: K % 32, N >= 1, null and misaligned pointers
+    assert L.us_quantize_x(X, 4, 48, Y, P(0x40000), None) == 1
+    assert L.us_quantize_x(X, 0, 64, Y, P(0x40000), None) == 1
+    assert L.us_quantize_x(None, 4, 64, Y, P(0x40000), None) == 1
+    assert L.us_quantize_x(P(0x20008), 4, 64, Y, P(0x40000), None) == 1
+    assert L.us_quantize_x(X, 4, 64, Y, P(0x40001), None) == 1

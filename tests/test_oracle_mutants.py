@@ -28,6 +28,10 @@ MUTANTS = {
     "first_term_dropped": ("for (int k = 0; k < K; ++k)\n        acc +=", "for (int k = 1; k < K; ++k)\n        acc +="),
     "scales_swapped": ("float t = a * or_half_to_float(s_w);", "float t = a * or_half_to_float(s_w) * 0.5f + a * or_half_to_float(s_x) * 0.5f;"),
     "abs_dropped_in_skip": ("if (skip && !(fabs(x) > tau)) continue;", "if (skip && !(x > tau)) continue;"),
+    "quant_divisor_8": ("uint16_t s16 = or_float_to_half(amax / 7.0f);", "uint16_t s16 = or_float_to_half(amax / 8.0f);"),
+    "quant_truncates": ("float q = rintf(v / s);", "float q = truncf(v / s);"),
+    "quant_rounds_half_up": ("float q = rintf(v / s);", "float q = floorf(v / s + 0.5f);"),
+    "quant_signed_max": ("const float a = fabsf(or_half_to_float(x[k]));", "const float a = or_half_to_float(x[k]);"),
     "tile_numbering_colmajor": ("            const int64_t t = (int64_t)tm * nTK + tk;\n            uint64_t* words = bitmap",
                                 "            const int64_t t = (int64_t)tk * nTM + tm;\n            uint64_t* words = bitmap"),
 }

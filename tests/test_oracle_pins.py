@@ -338,3 +338,40 @@ def test_workload_statistics():
     assert rd.min() > 0.25 and rd.max() < 0.71 and abs(rd.mean() - 0.5) < 0.05
     x = wl.spmspv(64, 4096, 0.5, 0.9, seed=0)["x"]
     assert abs((x == 0).mean() - 0.9) < 1e-3
+
+
+# ------------------------------------------------- activation quantisation --
+# UnionSparse Fig. 2 "Quant" (FP16 X -> INT4 X, per-token scale): s = fp16(amax / 7),
+# codes = clamp(rint(x / s), -8, 7) with ties to even, s = 1 for an all-zero token.
+
+def test_quantize_worked_examples(orc):
+    """Hand-worked tokens: amax 7 gives s = 1 exactly, so codes are rint(x)."""
+    X = np.array([[1, -2, 3.5, 7],          # 3.5 -> 4 (tie to even)
+                  [0.5, 1.5, 2.5, -7],       # ties: 0.5 -> 0, 1.5 -> 2, 2.5 -> 2
+                  [-7, 3, 0, 6.5],           # the maximum magnitude may be negative; 6.5 -> 6
+                  [0, 0, 0, 0]], np.float16)  # all zero: scale 1, codes 0
+    codes, s = orc.quantize_x(X)
+    assert codes.tolist() == [[1, -2, 4, 7], [0, 2, 2, -7], [-7, 3, 0, 6], [0, 0, 0, 0]]
+    assert s.tolist() == [1.0, 1.0, 1.0, 1.0]
+    # amax 14 -> s = 2: every code halves
+    c2, s2 = orc.quantize_x(X[:1] * 2)
+    assert s2.tolist() == [2.0] and c2.tolist() == [[1, -2, 4, 7]]
+    # amax 3.5: s = fp16(0.5) exactly; x = 1.25 -> 2.5 -> 2 (tie to even), 1.75 -> 3.5 -> 4
+    c3, s3 = orc.quantize_x(np.array([[1.25, 1.75, -3.5, 0.25]], np.float16))
+    assert s3.tolist() == [0.5] and c3.tolist() == [[2, 4, -7, 0]]
+
+
+def test_quantize_invariants(orc):
+    """On random tokens: the largest magnitude lands on +-7, every other value
+    is within half a step, and scaling a token by a power of two scales s only."""
+    rng = np.random.default_rng(5)
+    X = (rng.standard_normal((64, 256)) * rng.uniform(0.01, 50, (64, 1))).astype(np.float16)
+    codes, s = orc.quantize_x(X)
+    xf, sf = X.astype(np.float64), s.astype(np.float64)
+    assert codes.min() >= -8 and codes.max() <= 7
+    big = np.argmax(np.abs(xf), axis=1)
+    assert np.all(np.abs(codes[np.arange(64), big]) == 7)
+    err = np.abs(xf - codes * sf[:, None])
+    assert np.all(err <= sf[:, None] * (0.5 + 1e-3))
+    c4, s4 = orc.quantize_x((X.astype(np.float32) * 4).astype(np.float16))
+    assert np.array_equal(c4, codes) and np.array_equal(s4.astype(np.float32), s.astype(np.float32) * 4)
