@@ -196,20 +196,45 @@ w4a4_sk_kernel(const UsKParams p) {
             const bool all_k = xcols == p.nTK;
             const int tk0 = t0 % p.nTK;
             const int ncols = all_k ? p.nTK : per;
-            const int words = ncols * 8;                      // 8 nibbles per word, 8 words per tile
-            for (int i = threadIdx.x; i < NTOK * words; i += kNW * 32) {
-                const int n = i / words, r = i - n * words, xq = r >> 3, w = r & 7;
-                const int tk = all_k ? xq : (tk0 + xq) % p.nTK;
-                const uint32_t v = n < p.N ? __ldg(reinterpret_cast<const uint32_t*>(
-                                                 xg + (int64_t)n * (p.K / 2) + (int64_t)tk * (kTK / 2) + 4 * w))
-                                           : 0u;                  // absent tokens: code 0
-                if (NT) {
-                    *reinterpret_cast<uint32_t*>(xs + ((int64_t)n * xcols + xq) * XROW + 4 * w) = v;
-                } else {
-                    const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;
-                    const uint32_t e0 = __vsub4(__byte_perm(lo, hi, 0x5140) ^ 0x08080808u, 0x08080808u);
-                    const uint32_t e1 = __vsub4(__byte_perm(lo, hi, 0x7362) ^ 0x08080808u, 0x08080808u);
-                    *reinterpret_cast<uint2*>(xs + ((int64_t)n * xcols + xq) * XROW + 8 * w) = make_uint2(e0, e1);
+            // every load of a round is issued before its stores (the first global
+            // round trip after the dependency wait is on the critical path).
+            // dp4a: 4-byte words (8 codes, 8 per K tile) spread over many
+            // threads, each expanded to 8 int8; mma: 16-byte pieces (32 codes, 2
+            // per K tile) copied as they are
+            constexpr int kPieceB = NT ? 16 : 4;
+            constexpr int kPerTile = 32 / kPieceB;
+            const int pieces = ncols * kPerTile;
+            const int total = NTOK * pieces;
+            constexpr int kU = (NT == 1 || NT == 2) ? 8 : 4;
+            for (int i0 = threadIdx.x; i0 < total; i0 += kU * kNW * 32) {
+                uint4 v[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = i0 + u * kNW * 32;
+                    v[u] = make_uint4(0u, 0u, 0u, 0u);              // absent tokens: code 0
+                    if (i < total) {
+                        const int n = i / pieces, r = i - n * pieces, xq = r / kPerTile, hh = r - xq * kPerTile;
+                        const int tk = all_k ? xq : (tk0 + xq) % p.nTK;
+                        const uint8_t* src = xg + (int64_t)n * (p.K / 2) + (int64_t)tk * (kTK / 2) + kPieceB * hh;
+                        if (n < p.N) {
+                            if (NT) v[u] = __ldg(reinterpret_cast<const uint4*>(src));
+                            else v[u].x = __ldg(reinterpret_cast<const uint32_t*>(src));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int i = i0 + u * kNW * 32;
+                    if (i >= total) break;
+                    const int n = i / pieces, r = i - n * pieces, xq = r / kPerTile, hh = r - xq * kPerTile;
+                    if (NT) {
+                        *reinterpret_cast<uint4*>(xs + ((int64_t)n * xcols + xq) * XROW + 16 * hh) = v[u];
+                    } else {
+                        const uint32_t lo = v[u].x & 0x0F0F0F0Fu, hi = (v[u].x >> 4) & 0x0F0F0F0Fu;
+                        const uint32_t e0 = __vsub4(__byte_perm(lo, hi, 0x5140) ^ 0x08080808u, 0x08080808u);
+                        const uint32_t e1 = __vsub4(__byte_perm(lo, hi, 0x7362) ^ 0x08080808u, 0x08080808u);
+                        *reinterpret_cast<uint2*>(xs + ((int64_t)n * xcols + xq) * XROW + 8 * hh) = make_uint2(e0, e1);
+                    }
                 }
             }
         }
