@@ -71,10 +71,23 @@ US_DEV bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Bounded wait for phase `parity` of `bar`.  Returns false (and records
 // US_ERR_TIMEOUT) if the phase did not complete within kWaitLimitNs.
+// As mbar_try_wait, but the thread may sleep up to `ns` for the phase first.
+US_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 US_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             set_status(status, US_ERR_TIMEOUT);
             return false;
@@ -258,6 +271,7 @@ struct UsKParams {
     unsigned* counters; // split-K arrival counters, one per (band, token block)
     unsigned* status;
     // balanced (stream-K) W4A4 kernel only: CTAs, most tiles of one CTA, value
-    // ring bytes, staged activation columns (tiles), most bands one CTA touches
-    int sk_grid, sk_per, sk_ring, sk_xcols, sk_nb;
+    // ring bytes, most tiles of one consumer warp, most bands one CTA touches,
+    // dense decoded-tile slots, tiles decoded before the dependency wait
+    int sk_grid, sk_per, sk_ring, sk_tw, sk_nb, sk_slots, sk_pre;
 };

@@ -1,4 +1,4 @@
-// us_w4a4_sk.cu -- W4A4 bitmap SpMM for 1..8 tokens, the tile sequence spread
+// us_w4a4_sk.cu -- W4A4 bitmap SpMM for 1..32 tokens, the tile sequence spread
 // evenly over the SMs.
 //
 // Y = W . X with W int4 in 64 x 64 bitmap tiles, row-major scan (IE-BME of
@@ -12,22 +12,23 @@
 //    tile sequence t = tm*nTK + tk (one CTA per SM, a second one of the next
 //    launch fits beside it).  A contiguous run of tiles is contiguous in the
 //    bitmap and in the value array, so one chunk of four tiles arrives with two
-//    1-D bulk copies (TMA).  Every chunk is requested as soon as there is room:
-//    the runs are packed into a byte ring by their real length, not their worst
-//    case, so at 50 % density about twice as many tiles are in flight;
-//  * work item = one tile on one warp; lane l decodes rows l and l+32.  Row
-//    bases come from one warp scan of packed popcounts (the word-level part of
-//    UnionSparse's idx_base, section VI-B);
-//  * byte-step decode as in the cluster kernel (selector table + PRMT, dp4a on
-//    16*w); each table entry also carries the mask that empties rank 7's byte
-//    (clear positions read it) unless all eight positions are set;
+//    1-D bulk copies (TMA), packed into a byte ring by their real length;
+//  * decode once into dense tiles: a warp turns a tile into 64 x 64 packed int4
+//    in shared memory (lane l: rows l and l + 32; row bases from one warp scan
+//    of packed popcounts, the word-level part of UnionSparse's idx_base,
+//    section VI-B; a byte-step per eight positions: selector table + PRMT).
+//    Weights flagged static are decoded this way BEFORE the dependency wait,
+//    while the previous launch still runs; after it only the multiply is left
+//    (dp4a for up to 7 tokens, mma.sync in 8-token blocks above that).  Tiles
+//    beyond the dense slots, and all tiles of non-static weights, are decoded
+//    after the wait into the warp's own slot;
+//  * after the wait each warp fetches the activation slices of its own tiles
+//    and goes on by itself;
 //  * a band split between CTAs is finished by the CTA holding its first tile:
 //    the others post their partial sums as 64-bit {value, tag} words (one
 //    relaxed store each, no fence, no counter: the tag arrives with its value)
 //    and the owner waits for the tags (bounded), adds, and clears them for the
-//    next call.  Partials are integers, so the sum is exact in any order;
-//  * programmatic stream serialisation: barrier and table set-up (and, for
-//    weights flagged static, the weight copies) overlap the previous launch.
+//    next call.  Partials are integers, so the sum is exact in any order.
 #include "us_common.cuh"
 #include "us_internal.h"
 
@@ -48,10 +49,11 @@ __host__ __device__ constexpr int nw_for(int N, int NT) {
 __host__ __device__ constexpr int threads_for(int N, int NT) { return (nw_for(N, NT) + 1) * 32; }
 __host__ __device__ constexpr int ntok_for(int N, int NT) { return NT ? 8 * NT : N; }   // token slots
 __host__ __device__ constexpr int xrow_for(int NT) { return NT ? 32 : 64; }            // staged bytes per K tile
-constexpr int kLutRep = 16;                 // selector table replicas (bank spreading)
+constexpr int kLutRep = 8;                  // selector table replicas (bank spreading)
 constexpr int kHeader = 512;
 constexpr int kLutBytes = 256 * kLutRep * 8;   // {selector pair, odd-rank mask} per entry
-constexpr int kMinRing = 3 * kC * (kBm + kValCap);   // at least three worst-case chunks
+constexpr int kSlot = kTM * kTK / 2;        // one decoded tile: 64 x 64 packed int4
+constexpr int kMinRing = 2 * kC * (kBm + kValCap);   // at least two worst-case chunks
 
 struct SkSmem {
     uint64_t full[kR], empty[kR];
@@ -75,17 +77,19 @@ w4a4_sk_kernel(const UsKParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     SkSmem& S = *reinterpret_cast<SkSmem*>(smem);
     uint2* lut = reinterpret_cast<uint2*>(smem + kHeader);
-    uint8_t* ring = smem + kHeader + kLutBytes;
+    // dense tiles (sk_slots x kSlot) follow the table, then the byte ring
+    uint8_t* ring = smem + kHeader + kLutBytes + (size_t)p.sk_slots * kSlot;
     const uint32_t D = (uint32_t)p.sk_ring;
     const int nT = p.nTM * p.nTK, G = p.sk_grid;
     const int cta = blockIdx.x;
     const int t0 = sk_start(cta, G, nT), t1 = sk_start(cta + 1, G, nT);
     const int per = t1 - t0;
     uint32_t* offs = reinterpret_cast<uint32_t*>(ring + D);                       // per + 1
-    // activations: NTOK x xcols x XROW bytes (int8 per position for dp4a, the
-    // packed int4 codes for mma)
+    // activations, one region per consumer warp: its j-th tile's K slice for
+    // every token, XROW bytes each (int8 per position for dp4a, the packed int4
+    // codes for mma); sk_tw tiles per warp at most
     int8_t* xs = reinterpret_cast<int8_t*>(offs + ((p.sk_per + 1 + 3) & ~3));
-    int* accs = reinterpret_cast<int*>(xs + NTOK * p.sk_xcols * XROW);           // bands x NTOK x 64
+    int* accs = reinterpret_cast<int*>(xs + kNW * p.sk_tw * NTOK * XROW);       // bands x NTOK x 64
     uint16_t* sws = reinterpret_cast<uint16_t*>(accs + p.sk_nb * NTOK * kTM);     // bands x 64 row scales
     uint16_t* sxs = sws + p.sk_nb * kTM;                                          // NTOK token scales
     const int band0 = t0 / p.nTK;
@@ -109,8 +113,13 @@ w4a4_sk_kernel(const UsKParams p) {
     if (warp == kNW) {
         // ------------------------------------------------------------ producer
         if (!early) us::pdl_wait();
+        // the whole range heads for L2 at once; the ring then refills from there
+        if (early && lane == 0) us::bulk_prefetch_l2(p.bitmap + (int64_t)t0 * (kBm / 8), (uint32_t)per * kBm);
         for (int i = lane; i <= per; i += 32) offs[i] = p.tile_off[t0 + i];
         __syncwarp();
+        if (early && lane == 0 && offs[per] > offs[0] && (offs[0] & 31u) == 0 && (offs[per] & 31u) == 0 &&
+            (uint64_t)offs[per] * 4u <= p.values_bytes * 8ull)
+            us::bulk_prefetch_l2(p.values + offs[0] / 2u, (offs[per] - offs[0]) / 2u);
         const int nch = (per + kC - 1) / kC;
         uint32_t pos = 0;                                     // end of the newest chunk in the ring
         bool waited = !early;
@@ -143,9 +152,10 @@ w4a4_sk_kernel(const UsKParams p) {
                             break;
                         }
                     }
-                    // the consumers start only after the previous launch has finished:
-                    // wait for that too before a bounded wait on them
-                    if (!waited) {
+                    // the consumers release a chunk before the previous launch has
+                    // finished only if all its tiles are decoded early: else wait
+                    // for that launch too before a bounded wait on them
+                    if (!waited && min((tail + 1) * kC, per) > p.sk_pre) {
                         us::pdl_wait();
                         waited = true;
                     }
@@ -178,181 +188,261 @@ w4a4_sk_kernel(const UsKParams p) {
     }
     else {
         // ----------------------------------------------------------- consumers
+        // selector table, 16 w form for every consumer: the dp4a one keeps the
+        // positions in order (bytes p0..p3 | p4..p7); the mma one asks for
+        // (p0 p4 p1 p5 | p2 p6 p3 p7), which packs into the nibble order that
+        // the fp16 conversion below pairs up
         for (int e = threadIdx.x; e < 256; e += kNW * 32) {
-            // clear positions take rank 7's byte, which must then be empty (dp4a:
-            // 16 w = 0; mma: w + 8 = 8): the odd-rank mask drops rank 7 unless all
-            // eight positions are set
-            const uint32_t full = NT ? 0x0F0F0F0Fu : 0xF0F0F0F0u, part = NT ? 0x000F0F0Fu : 0x00F0F0F0u;
-            const uint2 ent = make_uint2(us::make_sel((uint32_t)e), e == 255 ? full : part);
+            uint32_t sel = us::make_sel((uint32_t)e);
+            if (NT) {
+                uint32_t ps = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    constexpr int kTo[8] = {0, 2, 4, 6, 1, 3, 5, 7};   // position -> selector nibble
+                    ps |= ((sel >> (4 * i)) & 0xFu) << (4 * kTo[i]);
+                }
+                sel = ps;
+            }
+            // clear positions take rank 7's byte, which the odd-rank mask empties
+            // unless all eight positions are set
+            const uint2 ent = make_uint2(sel, e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u);
 #pragma unroll
             for (int r = 0; r < kLutRep; ++r) lut[e * kLutRep + r] = ent;
         }
+        // static weights: their row scales are fixed too
+        if (p.Y && early)
+            for (int i = threadIdx.x; i < nb * kTM; i += kNW * 32) sws[i] = p.s_w[band0 * kTM + i];
+        us::named_bar_sync(1, kNW * 32);
+
+        const uint32_t lut_lane = (uint32_t)(lane % kLutRep);
+        const int P = early ? p.sk_pre : 0;                   // tiles decoded before the wait
+        // Decode tile q of the range into the dense packed-int4 tile dst: lane l
+        // takes rows l and l + 32; row bases come from one warp scan of packed
+        // popcounts (the word-level part of UnionSparse's idx_base, section
+        // VI-B); a byte-step turns eight positions into one word of eight
+        // nibbles.  False when the wait for the tile's chunk gave up.
+        auto decode_tile = [&](int q, uint8_t* dst) -> bool {
+            const int ch = q / kC, slot = ch % kR;
+            if (!us::mbar_wait(&S.full[slot], (uint32_t)(ch / kR) & 1u, p.status)) {
+                S.abort = 1;
+                return false;
+            }
+            const int ct = min(kC, per - ch * kC);
+            const uint8_t* base = ring + S.pos[slot];
+            const uint64_t* bm = reinterpret_cast<const uint64_t*>(base + (q - ch * kC) * kBm);
+            const uint64_t wA = bm[lane], wB = bm[lane + 32];
+            const uint32_t packed = (uint32_t)__popcll(wA) | ((uint32_t)__popcll(wB) << 16);
+            uint32_t incl = packed;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += o;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            const uint32_t ex = incl - packed;
+            const uint32_t totA = tot & 0xFFFFu;
+            const bool good = S.bad[slot] == 0 && totA + (tot >> 16) <= offs[q + 1] - offs[q];
+            if (!good && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
+            const uint32_t* vw = reinterpret_cast<const uint32_t*>(base + ct * kBm + (offs[q] - offs[ch * kC]) / 2u);
+            const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vw);
+            // rows lane (h = 0) and lane + 32 (h = 1) step by step side by side;
+            // each keeps a three-word window over its run: a step consumes at
+            // most one word, and the word a step loads (predicated, only by the
+            // lanes whose window moved on) is needed one step later
+            uint32_t ob[2], wi[2], cur[2], nxt[2], nn[2], lo[2], hi[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint64_t w = good ? (h ? wB : wA) : 0ull;        // a bad tile decodes as zeros
+                lo[h] = (uint32_t)w;
+                hi[h] = (uint32_t)(w >> 32);
+                ob[h] = h ? totA + (ex >> 16) : (ex & 0xFFFFu);         // nibble index of the row's first value
+                wi[h] = ob[h] >> 3;
+                cur[h] = vw[wi[h]];
+                nxt[h] = vw[wi[h] + 1];
+                nn[h] = vw[wi[h] + 2];
+            }
+            uint32_t pw[2][8];
+#pragma unroll
+            for (int bt = 0; bt < 8; ++bt) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t bb = __byte_perm(bt < 4 ? lo[h] : hi[h], 0u, 0x4440u | (uint32_t)(bt & 3));
+                    if (bt > 0) {
+                        const uint32_t nwi = ob[h] >> 3;
+                        const uint32_t adv = nwi != wi[h];
+                        cur[h] = adv ? nxt[h] : cur[h];
+                        nxt[h] = adv ? nn[h] : nxt[h];
+                        us::lds_u32_if(nn[h], adv, vbase + 4u * (nwi + 2u));
+                        wi[h] = nwi;
+                    }
+                    const uint32_t win = __funnelshift_r(cur[h], nxt[h], ob[h] << 2);
+                    const uint2 ent = lut[bb * kLutRep + lut_lane];
+                    const uint32_t odd = win & ent.y;                       // 16 w, ranks 1,3,5,(7)
+                    const uint32_t even = (win << 4) & 0xF0F0F0F0u;         // 16 w, ranks 0,2,4,6
+                    const uint32_t d0 = __byte_perm(even, odd, ent.x);
+                    const uint32_t d1 = __byte_perm(even, odd, ent.x >> 16);
+                    // byte i = d0's nibble i | d1's nibble i << 4; the mma consumer
+                    // keeps w + 8 (unsigned) for its fp16 conversion
+                    pw[h][bt] = (((d0 >> 4) & 0x0F0F0F0Fu) | (d1 & 0xF0F0F0F0u)) ^ (NT ? 0x88888888u : 0u);
+                    ob[h] += (uint32_t)__popc(bb);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int r = lane + 32 * h;
+                if constexpr (NT == 0) {
+                    // row r: 32 bytes, its two 16-byte halves swapped on every
+                    // other group of four rows (no bank conflicts either way)
+                    const int sw = (r >> 2) & 1;
+                    *reinterpret_cast<uint4*>(dst + r * 32 + 16 * sw) =
+                        make_uint4(pw[h][0], pw[h][1], pw[h][2], pw[h][3]);
+                    *reinterpret_cast<uint4*>(dst + r * 32 + 16 * (sw ^ 1)) =
+                        make_uint4(pw[h][4], pw[h][5], pw[h][6], pw[h][7]);
+                } else {
+                    // fragment order: the 16 bytes thread (g, tig) of 16-row block
+                    // mb reads are rows g and g + 8, words 2 tig and 2 tig + 1
+                    const int mb = r >> 4, g = r & 7, hr = (r >> 3) & 1;
+#pragma unroll
+                    for (int tig = 0; tig < 4; ++tig) {
+                        const int sg = mb * 32 + g * 4 + tig;
+                        const int ph = sg ^ ((sg >> 3) & 3);
+                        *reinterpret_cast<uint2*>(dst + ph * 16 + hr * 8) = make_uint2(pw[h][2 * tig], pw[h][2 * tig + 1]);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) us::mbar_arrive(&S.empty[slot]);
+            return true;
+        };
+
+        uint8_t* dense = smem + kHeader + kLutBytes;
+        bool ok = true;
+        // static weights: decode this CTA's first P tiles while the previous
+        // launch still runs
+        for (int q = warp; q < P && ok; q += kNW) ok = decode_tile(q, dense + q * kSlot);
         us::pdl_wait();
-        // activations: column block xq of token n holds K tile tk, where xq = tk when
-        // the CTA spans a whole band width, else xq = the tile's place in the range
+        // activations: each warp fetches the K slices of its own tiles (all its
+        // loads in flight before the first store) and goes on by itself; no
+        // warp waits for another one here
+        int8_t* xw = xs + (int64_t)warp * p.sk_tw * NTOK * XROW;
         {
             const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.X);
-            const int xcols = p.sk_xcols;
-            const bool all_k = xcols == p.nTK;
-            const int tk0 = t0 % p.nTK;
-            const int ncols = all_k ? p.nTK : per;
-            // every load of a round is issued before its stores (the first global
-            // round trip after the dependency wait is on the critical path).
-            // dp4a: 4-byte words (8 codes, 8 per K tile) spread over many
-            // threads, each expanded to 8 int8; mma: 16-byte pieces (32 codes, 2
-            // per K tile) copied as they are
+            // dp4a: 4-byte words (8 codes, 8 per K tile), each expanded to 8 int8;
+            // mma: 16-byte pieces (32 codes, 2 per K tile) copied as they are
             constexpr int kPieceB = NT ? 16 : 4;
             constexpr int kPerTile = 32 / kPieceB;
-            const int pieces = ncols * kPerTile;
-            const int total = NTOK * pieces;
-            constexpr int kU = (NT == 1 || NT == 2) ? 8 : 4;
-            for (int i0 = threadIdx.x; i0 < total; i0 += kU * kNW * 32) {
+            constexpr int kPerJ = NTOK * kPerTile;
+            const int T = per > warp ? (per - warp + kNW - 1) / kNW : 0;
+            const int total = T * kPerJ;
+            constexpr int kU = NT == 4 ? 4 : 8;
+            // the token scales travel in the same round trip
+            uint16_t sxv = 0;
+            if (p.Y && threadIdx.x < NTOK && threadIdx.x < p.N) sxv = p.s_x[threadIdx.x];
+            for (int i0 = lane; i0 < total; i0 += kU * 32) {
                 uint4 v[kU];
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
-                    const int i = i0 + u * kNW * 32;
+                    const int i = i0 + u * 32;
                     v[u] = make_uint4(0u, 0u, 0u, 0u);              // absent tokens: code 0
-                    if (i < total) {
-                        const int n = i / pieces, r = i - n * pieces, xq = r / kPerTile, hh = r - xq * kPerTile;
-                        const int tk = all_k ? xq : (tk0 + xq) % p.nTK;
+                    const int j = i / kPerJ, r = i - j * kPerJ, n = r / kPerTile, hh = r - n * kPerTile;
+                    if (i < total && n < p.N) {
+                        const int tk = (t0 + warp + j * kNW) % p.nTK;
                         const uint8_t* src = xg + (int64_t)n * (p.K / 2) + (int64_t)tk * (kTK / 2) + kPieceB * hh;
-                        if (n < p.N) {
-                            if (NT) v[u] = __ldg(reinterpret_cast<const uint4*>(src));
-                            else v[u].x = __ldg(reinterpret_cast<const uint32_t*>(src));
-                        }
+                        if (NT) v[u] = __ldg(reinterpret_cast<const uint4*>(src));
+                        else v[u].x = __ldg(reinterpret_cast<const uint32_t*>(src));
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < kU; ++u) {
-                    const int i = i0 + u * kNW * 32;
+                    const int i = i0 + u * 32;
                     if (i >= total) break;
-                    const int n = i / pieces, r = i - n * pieces, xq = r / kPerTile, hh = r - xq * kPerTile;
+                    const int j = i / kPerJ, r = i - j * kPerJ, n = r / kPerTile, hh = r - n * kPerTile;
+                    int8_t* dst = xw + (int64_t)(j * NTOK + n) * XROW;
                     if (NT) {
-                        *reinterpret_cast<uint4*>(xs + ((int64_t)n * xcols + xq) * XROW + 16 * hh) = v[u];
+                        *reinterpret_cast<uint4*>(dst + 16 * hh) = v[u];
                     } else {
                         const uint32_t lo = v[u].x & 0x0F0F0F0Fu, hi = (v[u].x >> 4) & 0x0F0F0F0Fu;
                         const uint32_t e0 = __vsub4(__byte_perm(lo, hi, 0x5140) ^ 0x08080808u, 0x08080808u);
                         const uint32_t e1 = __vsub4(__byte_perm(lo, hi, 0x7362) ^ 0x08080808u, 0x08080808u);
-                        *reinterpret_cast<uint2*>(xs + ((int64_t)n * xcols + xq) * XROW + 8 * hh) = make_uint2(e0, e1);
+                        *reinterpret_cast<uint2*>(dst + 8 * hh) = make_uint2(e0, e1);
                     }
                 }
             }
+            if (p.Y && threadIdx.x < NTOK) sxs[threadIdx.x] = sxv;
         }
-        if (p.Y) {
+        // the epilogue reads the row scales after the block-wide barrier
+        if (p.Y && !early)
             for (int i = threadIdx.x; i < nb * kTM; i += kNW * 32) sws[i] = p.s_w[band0 * kTM + i];
-            for (int i = threadIdx.x; i < NTOK; i += kNW * 32) sxs[i] = i < p.N ? p.s_x[i] : (uint16_t)0;
-        }
-        us::named_bar_sync(1, kNW * 32);
+        __syncwarp();
 
+        // After the wait: tile q < P is read from its dense tile; a later one is
+        // decoded now into this warp's own slot (slot w held tile w, done by
+        // then) and read back from there.
+        int cur_b = -1;
         if constexpr (NT == 0) {
-            const uint32_t lut_lane = (uint32_t)(lane % kLutRep);
-            const bool all_k = p.sk_xcols == p.nTK;
             int acc[2][N];
-    #pragma unroll
+#pragma unroll
             for (int h = 0; h < 2; ++h)
-    #pragma unroll
+#pragma unroll
                 for (int n = 0; n < N; ++n) acc[h][n] = 0;
-            int cur_b = -1;
             auto flush = [&]() {
                 if (cur_b < 0) return;
-    #pragma unroll
+#pragma unroll
                 for (int h = 0; h < 2; ++h)
-    #pragma unroll
+#pragma unroll
                     for (int n = 0; n < N; ++n) {
                         atomicAdd(&accs[(cur_b * N + n) * kTM + h * 32 + lane], acc[h][n]);
                         acc[h][n] = 0;
                     }
             };
-            // one tile per warp at a time; lane l decodes rows l and l + 32
-            for (int q = warp; q < per; q += kNW) {
-                const int ch = q / kC, slot = ch % kR;
-                if (!us::mbar_wait(&S.full[slot], (uint32_t)(ch / kR) & 1u, p.status)) {
-                    S.abort = 1;
-                    break;
-                }
+            for (int q = warp; q < per && ok; q += kNW) {
                 const int t = t0 + q;
                 const int brel = t / p.nTK - band0;
                 if (brel != cur_b) {
                     flush();
                     cur_b = brel;
                 }
-                const int ct = min(kC, per - ch * kC);
-                const uint8_t* base = ring + S.pos[slot];
-                const uint64_t* bm = reinterpret_cast<const uint64_t*>(base + (q - ch * kC) * kBm);
-                const uint64_t wA = bm[lane], wB = bm[lane + 32];
-                const uint32_t packed = (uint32_t)__popcll(wA) | ((uint32_t)__popcll(wB) << 16);
-                uint32_t incl = packed;
-    #pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += o;
+                const uint8_t* src = dense + q * kSlot;
+                if (q >= P) {
+                    src = dense + warp * kSlot;
+                    if (!(ok = decode_tile(q, dense + warp * kSlot))) break;
                 }
-                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-                const uint32_t ex = incl - packed;
-                const uint32_t totA = tot & 0xFFFFu;
-                const bool good = S.bad[slot] == 0 && totA + (tot >> 16) <= offs[q + 1] - offs[q];
-                if (!good) {
-                    if (lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-                } else {
-                    const uint32_t* vw = reinterpret_cast<const uint32_t*>(base + ct * kBm + (offs[q] - offs[ch * kC]) / 2u);
-                    const int8_t* xt = xs + (all_k ? t % p.nTK : q) * kTK;
-                    const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vw);
-    #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint64_t w = h ? wB : wA;
-                        const uint32_t lo = (uint32_t)w, hi = (uint32_t)(w >> 32);
-                        uint32_t ob = h ? totA + (ex >> 16) : (ex & 0xFFFFu);   // nibble index of the row's first value
-                        // two-word window over the row's run; a step consumes at most one
-                        // word, so a new word is loaded only by the lanes whose window
-                        // moved on (predicated, no branch): fewer bank conflicts
-                        uint32_t wi = ob >> 3;
-                        uint32_t cur = vw[wi], nxt = vw[wi + 1];
-    #pragma unroll
-                        for (int bt = 0; bt < 8; ++bt) {
-                            const uint32_t bb = __byte_perm(bt < 4 ? lo : hi, 0u, 0x4440u | (uint32_t)(bt & 3));
-                            if (bt > 0) {
-                                const uint32_t nwi = ob >> 3;
-                                const uint32_t adv = nwi != wi;
-                                cur = adv ? nxt : cur;
-                                us::lds_u32_if(nxt, adv, vbase + 4u * (nwi + 1u));
-                                wi = nwi;
-                            }
-                            const uint32_t win = __funnelshift_r(cur, nxt, ob << 2);
-                            const uint2 ent = lut[bb * kLutRep + lut_lane];
-                            const uint32_t odd = win & ent.y;                       // 16 w, ranks 1,3,5,(7)
-                            const uint32_t even = (win << 4) & 0xF0F0F0F0u;         // 16 w, ranks 0,2,4,6
-                            const int d0 = (int)__byte_perm(even, odd, ent.x);
-                            const int d1 = (int)__byte_perm(even, odd, ent.x >> 16);
-    #pragma unroll
-                            for (int n = 0; n < N; ++n) {
-                                const uint2 xv =
-                                    *reinterpret_cast<const uint2*>(xt + (int64_t)n * p.sk_xcols * kTK + 8 * bt);
-                                acc[h][n] = __dp4a(d0, (int)xv.x, acc[h][n]);
-                                acc[h][n] = __dp4a(d1, (int)xv.y, acc[h][n]);
-                            }
-                            ob += (uint32_t)__popc(bb);
+                // rows lane and lane + 32, eight words each: byte i of word k holds
+                // positions 8k + i (low nibble) and 8k + 4 + i (high nibble)
+                uint32_t pw[2][8];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int r = lane + 32 * h, sw = (r >> 2) & 1;
+                    const uint4 a = *reinterpret_cast<const uint4*>(src + r * 32 + 16 * sw);
+                    const uint4 b = *reinterpret_cast<const uint4*>(src + r * 32 + 16 * (sw ^ 1));
+                    pw[h][0] = a.x; pw[h][1] = a.y; pw[h][2] = a.z; pw[h][3] = a.w;
+                    pw[h][4] = b.x; pw[h][5] = b.y; pw[h][6] = b.z; pw[h][7] = b.w;
+                }
+                __syncwarp();                                 // the slot may be refilled next
+                const int8_t* xt = xw + (int64_t)((q - warp) / kNW) * N * kTK;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+#pragma unroll
+                    for (int n = 0; n < N; ++n) {
+                        const uint2 xv = *reinterpret_cast<const uint2*>(xt + n * kTK + 8 * k);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            acc[h][n] = __dp4a((int)((pw[h][k] << 4) & 0xF0F0F0F0u), (int)xv.x, acc[h][n]);   // 16 w
+                            acc[h][n] = __dp4a((int)(pw[h][k] & 0xF0F0F0F0u), (int)xv.y, acc[h][n]);
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) us::mbar_arrive(&S.empty[slot]);
             }
             flush();
         } else {
-            // mma.sync consumer: one tile per warp at a time.  Thread (g, tig) =
-            // (lane / 4, lane % 4) decodes, for rows g and g + 8 of each 16-row
-            // block, the 16 consecutive positions 16 tig .. 16 tig + 15 (two
-            // byte-steps) as fp16.  K is a reduction index, so it may be permuted
-            // as long as A and B agree: position 16 tig + 4 kk + c is the K16 block
-            // kk's column {2 tig, 2 tig + 1, 8 + 2 tig, 9 + 2 tig}[c], which makes the
-            // decoded halves exactly the thread's A fragment registers of
+            // mma.sync: thread (g, tig) = (lane / 4, lane % 4) holds, for rows g
+            // and g + 8 of each 16-row block, the positions 16 tig .. 16 tig + 15.
+            // K is a reduction index, so it may be permuted as long as A and B
+            // agree: position 16 tig + 4 kk + c is the K16 block kk's column
+            // {2 tig, 2 tig + 1, 8 + 2 tig, 9 + 2 tig}[c], which makes the thread's
+            // eight position pairs exactly its A fragment registers of
             // mma.m16n8k16 and its B fragment one 8-byte load per token.
             const int g = lane >> 2, tig = lane & 3;
-            const uint32_t lut_lane = (uint32_t)(lane % kLutRep);
-            const bool all_k = p.sk_xcols == p.nTK;
-            const uint32_t m_lo = tig == 0 ? 0u : (tig == 1 ? 0xFFFFu : 0xFFFFFFFFu);   // bits below 16 tig
-            const uint32_t m_hi = tig == 3 ? 0xFFFFu : 0u;
-            const uint32_t sh16 = 16u * (uint32_t)(tig & 1);
             float acc[4][NT][4];
 #pragma unroll
             for (int mb = 0; mb < 4; ++mb)
@@ -360,7 +450,6 @@ w4a4_sk_kernel(const UsKParams p) {
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) acc[mb][nt][c] = 0.f;
-            int cur_b = -1;
             auto flush = [&]() {
                 if (cur_b < 0) return;
 #pragma unroll
@@ -374,103 +463,74 @@ w4a4_sk_kernel(const UsKParams p) {
                             acc[mb][nt][c] = 0.f;
                         }
             };
-            for (int q = warp; q < per; q += kNW) {
-                const int ch = q / kC, slot = ch % kR;
-                if (!us::mbar_wait(&S.full[slot], (uint32_t)(ch / kR) & 1u, p.status)) {
-                    S.abort = 1;
-                    break;
+            // word of eight nibbles u = w + 8, nibbles (0,4), (1,5), (2,6), (3,7)
+            // paired -> four fp16 pairs.  0x6400 | u is 1024 + u; 0x6400 | 16 u is
+            // 1024 + 16 u, which (x / 16) - 72 maps to u - 8 exactly
+            auto cvt = [](uint32_t pw, uint32_t* o) {
+                const __half2 b0 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
+                const __half2 s1 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
+                const __half2 b1 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));   // -72
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const uint32_t v = j ? pw >> 8 : pw;
+                    uint32_t l = (v & 0x000F000Fu) | 0x64006400u, h = (v & 0x00F000F0u) | 0x64006400u;
+                    const __half2 fl = __hsub2(*reinterpret_cast<const __half2*>(&l), b0);
+                    const __half2 fh = __hfma2(*reinterpret_cast<const __half2*>(&h), s1, b1);
+                    o[2 * j] = *reinterpret_cast<const uint32_t*>(&fl);
+                    o[2 * j + 1] = *reinterpret_cast<const uint32_t*>(&fh);
                 }
+            };
+            for (int q = warp; q < per && ok; q += kNW) {
                 const int t = t0 + q;
                 const int brel = t / p.nTK - band0;
                 if (brel != cur_b) {
                     flush();
                     cur_b = brel;
                 }
-                const int ct = min(kC, per - ch * kC);
-                const uint8_t* base = ring + S.pos[slot];
-                const uint64_t* bm = reinterpret_cast<const uint64_t*>(base + (q - ch * kC) * kBm);
-                const uint64_t wA = bm[lane], wB = bm[lane + 32];
-                const uint32_t packed = (uint32_t)__popcll(wA) | ((uint32_t)__popcll(wB) << 16);
-                uint32_t incl = packed;
-#pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += o;
+                const uint8_t* src = dense + q * kSlot;
+                if (q >= P) {
+                    src = dense + warp * kSlot;
+                    if (!(ok = decode_tile(q, dense + warp * kSlot))) break;
                 }
-                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-                const uint32_t ex = incl - packed;
-                const uint32_t totA = tot & 0xFFFFu;
-                const bool good = S.bad[slot] == 0 && totA + (tot >> 16) <= offs[q + 1] - offs[q];
-                if (!good) {
-                    if (lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-                } else {
-                    const uint32_t* vw = reinterpret_cast<const uint32_t*>(base + ct * kBm + (offs[q] - offs[ch * kC]) / 2u);
-                    const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vw);
-                    // B fragments: token 8 nt + g, positions 16 tig .. 16 tig + 15 as fp16
-                    uint32_t bf[NT][8];
-                    const int xq = all_k ? t % p.nTK : q;
+                // B fragments: token 8 nt + g, positions 16 tig .. 16 tig + 15 as fp16
+                uint32_t bf[NT][8];
+                const int8_t* xt = xw + (int64_t)((q - warp) / kNW) * NTOK * XROW;
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const uint2 v = *reinterpret_cast<const uint2*>(
-                            xs + ((int64_t)(8 * nt + g) * p.sk_xcols + xq) * XROW + 8 * tig);
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint2 v = *reinterpret_cast<const uint2*>(xt + (8 * nt + g) * XROW + 8 * tig);
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const uint32_t w = hh ? v.y : v.x;
-                            // w + 8 per element: element 2i in byte i of lo, 2i + 1 in byte i of hi
-                            const uint4 h = us::u8x8_to_f16x8((w & 0x0F0F0F0Fu) ^ 0x08080808u,
-                                                             ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x73625140u);
-                            bf[nt][4 * hh + 0] = h.x;
-                            bf[nt][4 * hh + 1] = h.y;
-                            bf[nt][4 * hh + 2] = h.z;
-                            bf[nt][4 * hh + 3] = h.w;
-                        }
-                    }
-#pragma unroll
-                    for (int mb = 0; mb < 4; ++mb) {
-                        uint32_t af[2][8];                        // rows g, g + 8: 16 positions as fp16 pairs
-#pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {
-                            const int r = 16 * mb + g + 8 * hr;
-                            const uint64_t word = bm[r];
-                            const uint32_t e = __shfl_sync(0xffffffffu, ex, r & 31);
-                            const uint32_t rowbase = r < 32 ? (e & 0xFFFFu) : totA + (e >> 16);
-                            const uint32_t lo = (uint32_t)word, hi = (uint32_t)(word >> 32);
-                            const uint32_t w16 = ((tig < 2 ? lo : hi) >> sh16) & 0xFFFFu;
-                            uint32_t ob = rowbase + (uint32_t)__popc(lo & m_lo) + (uint32_t)__popc(hi & m_hi);
-                            uint32_t wi = ob >> 3;
-                            uint32_t cur = vw[wi], nxt = vw[wi + 1];
-#pragma unroll
-                            for (int s2 = 0; s2 < 2; ++s2) {
-                                const uint32_t bb = s2 ? (w16 >> 8) : (w16 & 0xFFu);
-                                if (s2) {
-                                    const uint32_t nwi = ob >> 3;
-                                    const uint32_t adv = nwi != wi;
-                                    cur = adv ? nxt : cur;
-                                    us::lds_u32_if(nxt, adv, vbase + 4u * (nwi + 1u));
-                                    wi = nwi;
-                                }
-                                const uint32_t win = __funnelshift_r(cur, nxt, ob << 2);
-                                const uint2 ent = lut[bb * kLutRep + lut_lane];
-                                const uint32_t even = (win & 0x0F0F0F0Fu) ^ 0x08080808u;        // w + 8, ranks 0,2,4,6
-                                const uint32_t odd = ((win >> 4) & ent.y) ^ 0x08080808u;        // w + 8, ranks 1,3,5,(7)
-                                const uint4 h = us::u8x8_to_f16x8(even, odd, ent.x);
-                                af[hr][4 * s2 + 0] = h.x;
-                                af[hr][4 * s2 + 1] = h.y;
-                                af[hr][4 * s2 + 2] = h.z;
-                                af[hr][4 * s2 + 3] = h.w;
-                                ob += (uint32_t)__popc(bb);
-                            }
-                        }
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                us::mma_m16n8k16_f16(acc[mb][nt], af[0][2 * kk], af[1][2 * kk], af[0][2 * kk + 1],
-                                                     af[1][2 * kk + 1], bf[nt][2 * kk], bf[nt][2 * kk + 1]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const uint32_t w = hh ? v.y : v.x;
+                        // w + 8 per element: element 2i in byte i of lo, 2i + 1 in byte i of hi
+                        const uint4 h = us::u8x8_to_f16x8((w & 0x0F0F0F0Fu) ^ 0x08080808u,
+                                                         ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x73625140u);
+                        bf[nt][4 * hh + 0] = h.x;
+                        bf[nt][4 * hh + 1] = h.y;
+                        bf[nt][4 * hh + 2] = h.z;
+                        bf[nt][4 * hh + 3] = h.w;
                     }
                 }
-                __syncwarp();
-                if (lane == 0) us::mbar_arrive(&S.empty[slot]);
+                uint4 av[4];
+#pragma unroll
+                for (int mb = 0; mb < 4; ++mb) {
+                    const int sg = mb * 32 + lane;
+                    av[mb] = *reinterpret_cast<const uint4*>(src + (sg ^ ((sg >> 3) & 3)) * 16);
+                }
+                __syncwarp();                                 // the slot may be refilled next
+#pragma unroll
+                for (int mb = 0; mb < 4; ++mb) {
+                    uint32_t af[2][8];                        // rows g, g + 8: position pairs 0..7
+                    cvt(av[mb].x, &af[0][0]);
+                    cvt(av[mb].y, &af[0][4]);
+                    cvt(av[mb].z, &af[1][0]);
+                    cvt(av[mb].w, &af[1][4]);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            us::mma_m16n8k16_f16(acc[mb][nt], af[0][2 * kk], af[1][2 * kk], af[0][2 * kk + 1],
+                                                 af[1][2 * kk + 1], bf[nt][2 * kk], bf[nt][2 * kk + 1]);
+                }
             }
             flush();
         }
@@ -516,36 +576,52 @@ w4a4_sk_kernel(const UsKParams p) {
             for (int i = threadIdx.x; i < NTOK * kTM; i += kThreads) store(br, i, a[i]);
             continue;
         }
-        // owned, continued by CTAs cta+1 .. c_hi, whose first band it is
+        // owned, continued by CTAs cta+1 .. c_hi, whose first band it is.  A
+        // thread's loads of up to kE elements x 4 CTAs are all in flight before
+        // the first is used: usually one L2 round trip for the whole band
         const int c_hi = sk_cta_of((int64_t)(b + 1) * p.nTK - 1, G, nT);
-        for (int i = threadIdx.x; i < NTOK * kTM; i += kThreads) {
-            int v = a[i];
+        constexpr int kAll = NTOK * kTM;
+        constexpr int kE = (kAll + kThreads - 1) / kThreads < 4 ? (kAll + kThreads - 1) / kThreads : 4;
+        for (int i0 = threadIdx.x; i0 < kAll; i0 += kE * kThreads) {
+            int v[kE];
+#pragma unroll
+            for (int e = 0; e < kE; ++e) v[e] = i0 + e * kThreads < kAll ? a[i0 + e * kThreads] : 0;
             for (int c0 = cta + 1; c0 <= c_hi; c0 += 4) {
-                uint64_t w[4];
+                uint64_t w[kE][4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    w[u] = c0 + u <= c_hi ? us::ld_relaxed_gpu_u64(post + (int64_t)(c0 + u) * NTOK * kTM + i)
-                                          : (1ull << 32);
+                for (int e = 0; e < kE; ++e)
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    if (c0 + u > c_hi) continue;
-                    uint64_t* src = post + (int64_t)(c0 + u) * NTOK * kTM + i;
-                    if ((w[u] >> 32) != 1ull) {
-                        // not posted yet: wait for it, bounded
-                        const uint64_t tw = us::globaltimer_ns();
-                        while (((w[u] = us::ld_relaxed_gpu_u64(src)) >> 32) != 1ull) {
-                            if (us::globaltimer_ns() - tw > us::kWaitLimitNs) {
-                                us::set_status(p.status, US_ERR_TIMEOUT);
-                                w[u] = 0;
-                                break;
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + e * kThreads;
+                        w[e][u] = c0 + u <= c_hi && i < kAll
+                                      ? us::ld_relaxed_gpu_u64(post + (int64_t)(c0 + u) * kAll + i)
+                                      : (1ull << 32);
+                    }
+#pragma unroll
+                for (int e = 0; e < kE; ++e)
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + e * kThreads;
+                        if (c0 + u > c_hi || i >= kAll) continue;
+                        uint64_t* src = post + (int64_t)(c0 + u) * kAll + i;
+                        if ((w[e][u] >> 32) != 1ull) {
+                            // not posted yet: wait for it, bounded
+                            const uint64_t tw = us::globaltimer_ns();
+                            while (((w[e][u] = us::ld_relaxed_gpu_u64(src)) >> 32) != 1ull) {
+                                if (us::globaltimer_ns() - tw > us::kWaitLimitNs) {
+                                    us::set_status(p.status, US_ERR_TIMEOUT);
+                                    w[e][u] = 0;
+                                    break;
+                                }
                             }
                         }
+                        v[e] += (int)(uint32_t)w[e][u];
+                        us::st_relaxed_gpu_u64(src, 0ull);           // ready for the next call
                     }
-                    v += (int)(uint32_t)w[u];
-                    us::st_relaxed_gpu_u64(src, 0ull);               // ready for the next call
-                }
             }
-            store(br, i, v);
+#pragma unroll
+            for (int e = 0; e < kE; ++e)
+                if (i0 + e * kThreads < kAll) store(br, i0 + e * kThreads, v[e]);
         }
     }
 }
@@ -554,14 +630,16 @@ w4a4_sk_kernel(const UsKParams p) {
 
 namespace {
 
-// Shared-memory plan of one launch; false when it does not fit.
+// Shared-memory plan of one launch; false when it does not fit.  `pre`: the
+// weights are static, so tiles may be decoded before the dependency wait.
 struct SkPlan {
-    int NT, G, per, xcols, nb, ring;
+    int NT, G, per, tw, nb, ring, slots, pre;
     size_t smem;
 };
 
 constexpr size_t kSmemTwoPerSm = 112 * 1024;   // two CTAs of this size share one SM
 constexpr size_t kSmemMax = 200 * 1024;
+constexpr size_t kRingMax = 64 * 1024;
 
 #ifndef US_W4A4_DP4A_MAX_N
 #define US_W4A4_DP4A_MAX_N 7         // more tokens than this: the mma.sync consumer
@@ -569,29 +647,36 @@ constexpr size_t kSmemMax = 200 * 1024;
 
 int nt_for_tokens(int N) { return N <= US_W4A4_DP4A_MAX_N ? 0 : (N <= 8 ? 1 : (N <= 16 ? 2 : 4)); }
 
-bool sk_plan(int nTM, int nTK, int N, SkPlan& pl) {
+bool sk_plan(int nTM, int nTK, int N, bool pre, SkPlan& pl) {
     if (N < 1 || N > 32) return false;
     pl.NT = nt_for_tokens(N);
     if (pl.NT == 0 && N > 8) return false;
     if (pl.NT && nTK * kTK > (1 << 18)) return false;       // fp32 sums of int4 products stay exact
     const int ntok = ntok_for(N, pl.NT), xrow = xrow_for(pl.NT);
+    const int nw = nw_for(N, pl.NT);
     const int nT = nTM * nTK;
     pl.G = us::num_sms() < nT ? us::num_sms() : nT;
     pl.per = (nT + pl.G - 1) / pl.G;
-    pl.xcols = pl.per < nTK ? pl.per : nTK;
+    pl.tw = (pl.per + nw - 1) / nw;
     pl.nb = (pl.per + nTK - 1) / nTK + 1;
     const size_t fixed = kHeader + kLutBytes + (size_t)((pl.per + 1 + 3) & ~3) * 4 +
-                         (size_t)ntok * pl.xcols * xrow + (size_t)pl.nb * ntok * kTM * 4 +
+                         (size_t)nw * pl.tw * ntok * xrow + (size_t)pl.nb * ntok * kTM * 4 +
                          (((size_t)pl.nb * kTM + ntok) * 2 + 15) / 16 * 16;
-    const size_t ring_max = 64 * 1024;
-    size_t ring = fixed < kSmemTwoPerSm ? kSmemTwoPerSm - fixed : 0;
-    if (ring < kMinRing) ring = fixed < kSmemMax ? kSmemMax - fixed : 0;   // then one CTA per SM
-    if (ring > ring_max) ring = ring_max;
-    ring &= ~(size_t)15;
-    if (ring < kMinRing) return false;
-    pl.ring = (int)ring;
-    pl.smem = fixed + ring;
-    return pl.smem <= kSmemMax;
+    // every warp needs a slot of its own; static weights want one per tile
+    const int want = pre ? (pl.per > nw ? pl.per : nw) : nw;
+    for (size_t budget : {kSmemTwoPerSm, kSmemMax}) {
+        if (fixed + kMinRing + (size_t)nw * kSlot > budget) continue;
+        const size_t cap = (budget - fixed - kMinRing) / kSlot;
+        pl.slots = (int)((size_t)want < cap ? (size_t)want : cap);
+        pl.pre = pre ? (pl.per < pl.slots ? pl.per : pl.slots) : 0;
+        size_t ring = budget - fixed - (size_t)pl.slots * kSlot;
+        if (ring > kRingMax) ring = kRingMax;
+        ring &= ~(size_t)15;
+        pl.ring = (int)ring;
+        pl.smem = fixed + (size_t)pl.slots * kSlot + ring;
+        return true;
+    }
+    return false;
 }
 
 template <int N, int NT>
@@ -599,7 +684,8 @@ us_status launch_sk_n(UsKParams p, const SkPlan& pl, cudaStream_t st) {
     auto kern = w4a4_sk_kernel<N, NT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) != cudaSuccess)
         return US_ERR_CUDA;
-    p.sk_grid = pl.G; p.sk_per = pl.per; p.sk_ring = pl.ring; p.sk_xcols = pl.xcols; p.sk_nb = pl.nb;
+    p.sk_grid = pl.G; p.sk_per = pl.per; p.sk_ring = pl.ring; p.sk_tw = pl.tw; p.sk_nb = pl.nb;
+    p.sk_slots = pl.slots; p.sk_pre = pl.pre;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.G);
     cfg.blockDim = dim3(threads_for(N, NT));
@@ -620,12 +706,12 @@ namespace us {
 bool w4a4_sk_supported(int TM, int TK, int M, int K, int N) {
     if (TM != kTM || TK != kTK) return false;
     SkPlan pl;
-    return sk_plan(M / TM, K / TK, N, pl);
+    return sk_plan(M / TM, K / TK, N, false, pl);
 }
 
 size_t w4a4_sk_ws(int M, int K, int N) {
     SkPlan pl;
-    if (!sk_plan(M / kTM, K / kTK, N, pl)) return 0;
+    if (!sk_plan(M / kTM, K / kTK, N, false, pl)) return 0;
     return (size_t)pl.G * ntok_for(N, pl.NT) * kTM * 8;   // one posted partial per CTA
 }
 
@@ -635,7 +721,7 @@ int w4a4_sk_variant(int N) { return nt_for_tokens(N); }
 // first call and left zero by every call.
 us_status launch_w4a4_sk(UsKParams p, cudaStream_t st) {
     SkPlan pl;
-    if (!sk_plan(p.nTM, p.nTK, p.N, pl)) return US_ERR_UNSUPPORTED;
+    if (!sk_plan(p.nTM, p.nTK, p.N, (p.flags & US_BITMAP_STATIC) != 0, pl)) return US_ERR_UNSUPPORTED;
     switch (pl.NT) {
         case 1: return launch_sk_n<8, 1>(p, pl, st);
         case 2: return launch_sk_n<16, 2>(p, pl, st);

@@ -85,11 +85,12 @@ typedef enum {
  * parameters; the caller owns the three arrays.  values_bytes is the
  * readable length of `values` (at least tile_off[nT] * bits / 8).
  * flags: 0, or US_BITMAP_STATIC.  US_BITMAP_STATIC promises that no work
- * enqueued earlier on the same stream writes bitmap, tile_off or values (the
- * usual case for inference weights).  Kernels then start fetching them before
- * the preceding kernel has finished (programmatic dependent launch); the
- * activations and outputs are still touched only after it has.  Leave it 0
- * when the matrix may still be in the making, e.g. right after us_encode. */
+ * enqueued earlier on the same stream writes bitmap, tile_off or values, nor,
+ * in us_spmm_w4a4, the row scales s_w (the usual case for inference weights).
+ * Kernels then start fetching and decoding them before the preceding kernel
+ * has finished (programmatic dependent launch); the activations, their scales
+ * and the outputs are still touched only after it has.  Leave it 0 when the
+ * matrix may still be in the making, e.g. right after us_encode. */
 #define US_BITMAP_STATIC 1u
 typedef struct {
     int32_t M, K, TM, TK;

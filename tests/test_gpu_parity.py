@@ -177,20 +177,26 @@ SK_SHAPES = [
     (64 * 37, 64 * 13, 5, 0.3),    # 481 tiles: ranges of 3-4 tiles crossing band edges
     (64 * 9, 64 * 61, 2, 0.9),     # dense runs: the value ring wraps many times
     (64 * 3, 64 * 5, 7, 0.0),      # all tiles empty
+    (64 * 40, 64 * 200, 1, 0.5),   # 53 tiles per CTA: more than the dense slots hold
+    (64 * 40, 64 * 200, 6, 0.5),
 ]
 
 
+@pytest.mark.parametrize("static", [0, 1])
 @pytest.mark.parametrize("M,K,N,dens", SK_SHAPES)
-def test_w4a4_balanced_partition(us, orc, M, K, N, dens):
+def test_w4a4_balanced_partition(us, orc, M, K, N, dens, static):
     """Automatic W4A4 path for few tokens against the oracle, three times in a
     row (the posted partial sums of shared bands must be cleared for the next
-    call), and against an explicit K split, which takes the cluster kernel."""
+    call), and against an explicit K split, which takes the cluster kernel.
+    Static weights are decoded before the dependency wait (as many tiles as the
+    dense slots hold, the rest after it); others after it."""
     rng = np.random.default_rng(M + K + N)
     W = rand_i4(rng, M, K, dens)
     Xq = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
     s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
     s_x = (rng.random(N) * 0.5 + 0.05).astype(np.float16)
     E = encode_gpu(us, W, 64, 64, I4, ROW)
+    E.flags = us.US_BITMAP_STATIC if static else 0
     assert us.us_pick_split_k(us.US_OP_SPMM_W4A4, E, N) == 0
     Xp = wl.pack_int4(Xq)
     dev = "cuda"
@@ -223,19 +229,24 @@ TC_SHAPES = [
     (128 * 3, 64 * 5, 20, 0.3),    # 30 tiles, 20 tokens padded to 32
     (128 * 7, 64 * 33, 32, 0.6),   # 462 tiles, 32 tokens
     (192, 64 * 6, 9, 0.0),         # all tiles empty, 9 tokens padded to 16
+    (64 * 64, 64 * 64, 16, 0.5),   # 27 tiles per CTA, 26 dense slots when static
+    (64 * 40, 64 * 200, 32, 0.5),  # 53 tiles per CTA, one CTA per SM
 ]
 
 
+@pytest.mark.parametrize("static", [0, 1])
 @pytest.mark.parametrize("M,K,N,dens", TC_SHAPES)
-def test_w4a4_tensor_cores_balanced(us, orc, M, K, N, dens):
+def test_w4a4_tensor_cores_balanced(us, orc, M, K, N, dens, static):
     """Automatic W4A4 path with the mma.sync consumer against the oracle, three
-    calls in a row on one workspace (posted partials must be cleared each time)."""
+    calls in a row on one workspace (posted partials must be cleared each time),
+    with and without the static-weights flag."""
     rng = np.random.default_rng(M * 7 + K + N)
     W = rand_i4(rng, M, K, dens)
     Xq = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
     s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
     s_x = (rng.random(N) * 0.5 + 0.05).astype(np.float16)
     E = encode_gpu(us, W, 64, 64, I4, ROW)
+    E.flags = us.US_BITMAP_STATIC if static else 0
     dev = "cuda"
     X = torch.from_numpy(wl.pack_int4(Xq)).to(dev)
     sw = torch.from_numpy(s_w.view(np.int16)).to(dev)
