@@ -87,7 +87,7 @@ void fill_common(UsKParams& p, const us_bitmap* W, int N) {
     p.values_bytes = W->values_bytes;
     p.X = nullptr; p.s_w = nullptr; p.s_x = nullptr; p.Yacc = nullptr; p.Y = nullptr;
     p.tau = 0.f; p.ws = nullptr; p.counters = nullptr;
-    p.sk_grid = p.sk_per = p.sk_ring = p.sk_tw = p.sk_nb = p.sk_slots = p.sk_pre = 0;
+    p.sk_grid = p.sk_per = p.sk_ring = p.sk_xcols = p.sk_nb = p.sk_slots = p.sk_pre = 0;
     p.flags = W->flags;
     p.status = status_ptr();
 }

@@ -271,7 +271,7 @@ struct UsKParams {
     unsigned* counters; // split-K arrival counters, one per (band, token block)
     unsigned* status;
     // balanced (stream-K) W4A4 kernel only: CTAs, most tiles of one CTA, value
-    // ring bytes, most tiles of one consumer warp, most bands one CTA touches,
+    // ring bytes, staged activation columns (tiles), most bands one CTA touches,
     // dense decoded-tile slots, tiles decoded before the dependency wait
-    int sk_grid, sk_per, sk_ring, sk_tw, sk_nb, sk_slots, sk_pre;
+    int sk_grid, sk_per, sk_ring, sk_xcols, sk_nb, sk_slots, sk_pre;
 };

@@ -46,10 +46,10 @@ constexpr int kR = 16;                      // chunks in flight at most (mbarrie
 __host__ __device__ constexpr int nw_for(int N, int NT) {
     return NT ? (NT == 1 ? 12 : (NT == 2 ? 8 : 6)) : (N == 1 ? 16 : (N <= 3 ? 12 : 8));
 }
-__host__ __device__ constexpr int threads_for(int N, int NT) { return (nw_for(N, NT) + 1) * 32; }
+// consumer warps, then the weight producer warp, then the activation warp
+__host__ __device__ constexpr int threads_for(int N, int NT) { return (nw_for(N, NT) + 2) * 32; }
 __host__ __device__ constexpr int ntok_for(int N, int NT) { return NT ? 8 * NT : N; }   // token slots
-__host__ __device__ constexpr int xrow_for(int NT) { return NT ? 32 : 64; }            // staged bytes per K tile
-constexpr int kLutRep = 8;                  // selector table replicas (bank spreading)
+constexpr int kLutRep = 4;                  // selector table replicas (bank spreading)
 constexpr int kHeader = 512;
 constexpr int kLutBytes = 256 * kLutRep * 8;   // {selector pair, odd-rank mask} per entry
 constexpr int kSlot = kTM * kTK / 2;        // one decoded tile: 64 x 64 packed int4
@@ -57,6 +57,7 @@ constexpr int kMinRing = 2 * kC * (kBm + kValCap);   // at least two worst-case 
 
 struct SkSmem {
     uint64_t full[kR], empty[kR];
+    uint64_t xfull;                         // the activation copies have landed
     uint32_t pos[kR];                       // ring offset of the chunk in slot s
     uint32_t bad[kR];                       // its offsets failed the checks
     uint32_t abort;
@@ -73,7 +74,7 @@ w4a4_sk_kernel(const UsKParams p) {
     constexpr int kNW = nw_for(N, NT);
     constexpr int kThreads = threads_for(N, NT);
     constexpr int NTOK = ntok_for(N, NT);
-    constexpr int XROW = xrow_for(NT);
+    constexpr int XROW = kTK / 2;               // staged activation bytes per K tile (packed int4)
     extern __shared__ __align__(128) uint8_t smem[];
     SkSmem& S = *reinterpret_cast<SkSmem*>(smem);
     uint2* lut = reinterpret_cast<uint2*>(smem + kHeader);
@@ -85,11 +86,11 @@ w4a4_sk_kernel(const UsKParams p) {
     const int t0 = sk_start(cta, G, nT), t1 = sk_start(cta + 1, G, nT);
     const int per = t1 - t0;
     uint32_t* offs = reinterpret_cast<uint32_t*>(ring + D);                       // per + 1
-    // activations, one region per consumer warp: its j-th tile's K slice for
-    // every token, XROW bytes each (int8 per position for dp4a, the packed int4
-    // codes for mma); sk_tw tiles per warp at most
+    // activations as given (packed int4): NTOK x xcols x XROW bytes; column xq of
+    // token n holds K tile tk, where xq = tk when the CTAs span whole band
+    // widths (xcols == nTK), else xq = the tile's place in the CTA's range
     int8_t* xs = reinterpret_cast<int8_t*>(offs + ((p.sk_per + 1 + 3) & ~3));
-    int* accs = reinterpret_cast<int*>(xs + kNW * p.sk_tw * NTOK * XROW);       // bands x NTOK x 64
+    int* accs = reinterpret_cast<int*>(xs + NTOK * p.sk_xcols * XROW);          // bands x NTOK x 64
     uint16_t* sws = reinterpret_cast<uint16_t*>(accs + p.sk_nb * NTOK * kTM);     // bands x 64 row scales
     uint16_t* sxs = sws + p.sk_nb * kTM;                                          // NTOK token scales
     const int band0 = t0 / p.nTK;
@@ -102,6 +103,7 @@ w4a4_sk_kernel(const UsKParams p) {
             us::mbar_init(&S.full[i], 1);
             us::mbar_init(&S.empty[i], kC);                  // one arrival per tile
         }
+        us::mbar_init(&S.xfull, 1);
         S.abort = 0;
         us::fence_mbar_init();
     }
@@ -185,29 +187,55 @@ w4a4_sk_kernel(const UsKParams p) {
             }
         }
         if (!waited) us::pdl_wait();                          // idle now: take it off the epilogue's path
+    } else if (warp == kNW + 1) {
+        // ---------------------------------------------------------- activations
+        // copied in as soon as the previous launch has finished, whatever the
+        // weight producer and the consumers are still busy with
+        us::pdl_wait();
+        const bool all_k = p.sk_xcols == p.nTK;
+        const int ncols = all_k ? p.nTK : per;
+        const uint32_t row = (uint32_t)ncols * XROW;
+        if (lane == 0) us::mbar_arrive_expect_tx(&S.xfull, (uint32_t)p.N * row);
+        __syncwarp();
+        const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.X);
+        const int tk0 = all_k ? 0 : t0 % p.nTK;
+        const int len1 = min(ncols, p.nTK - tk0);            // the range may wrap past the band's end
+        for (int n = lane; n < p.N; n += 32) {
+            const uint8_t* src = xg + (int64_t)n * (p.K / 2);
+            int8_t* dst = xs + (int64_t)n * p.sk_xcols * XROW;
+            us::bulk_g2s(dst, src + (int64_t)tk0 * XROW, (uint32_t)len1 * XROW, &S.xfull);
+            if (len1 < ncols) us::bulk_g2s(dst + len1 * XROW, src, (uint32_t)(ncols - len1) * XROW, &S.xfull);
+            if (p.Y) sxs[n] = p.s_x[n];
+        }
     }
     else {
         // ----------------------------------------------------------- consumers
-        // selector table, 16 w form for every consumer: the dp4a one keeps the
-        // positions in order (bytes p0..p3 | p4..p7); the mma one asks for
-        // (p0 p4 p1 p5 | p2 p6 p3 p7), which packs into the nibble order that
-        // the fp16 conversion below pairs up
+        // selector table, 16 w form: d0's bytes become the low nibbles of a
+        // packed word, d1's the high ones.  The dp4a consumer asks for
+        // (p0 p2 p4 p6 | p1 p3 p5 p7), which packs the positions in the order of
+        // the packed activations (position 2i low, 2i + 1 high in byte i); the
+        // mma one for (p0 p4 p1 p5 | p2 p6 p3 p7), the nibble order that the fp16
+        // conversion below pairs up
         for (int e = threadIdx.x; e < 256; e += kNW * 32) {
-            uint32_t sel = us::make_sel((uint32_t)e);
-            if (NT) {
-                uint32_t ps = 0;
+            const uint32_t sel = us::make_sel((uint32_t)e);
+            uint32_t ps = 0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    constexpr int kTo[8] = {0, 2, 4, 6, 1, 3, 5, 7};   // position -> selector nibble
-                    ps |= ((sel >> (4 * i)) & 0xFu) << (4 * kTo[i]);
-                }
-                sel = ps;
+            for (int i = 0; i < 8; ++i) {
+                // position i -> selector nibble
+                const int to = NT ? ((i & 3) * 2 + (i >> 2)) : ((i & 1) * 4 + (i >> 1));
+                ps |= ((sel >> (4 * i)) & 0xFu) << (4 * to);
             }
             // clear positions take rank 7's byte, which the odd-rank mask empties
             // unless all eight positions are set
-            const uint2 ent = make_uint2(sel, e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u);
+            const uint2 ent = make_uint2(ps, e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u);
 #pragma unroll
             for (int r = 0; r < kLutRep; ++r) lut[e * kLutRep + r] = ent;
+        }
+        // the padding tokens of the mma consumer multiply as zeros
+        if (NTOK > p.N) {
+            uint4* z = reinterpret_cast<uint4*>(xs + (int64_t)p.N * p.sk_xcols * XROW);
+            const int nz = (NTOK - p.N) * p.sk_xcols * XROW / 16;
+            for (int i = threadIdx.x; i < nz; i += kNW * 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
         }
         // static weights: their row scales are fixed too
         if (p.Y && early)
@@ -320,60 +348,18 @@ w4a4_sk_kernel(const UsKParams p) {
         // static weights: decode this CTA's first P tiles while the previous
         // launch still runs
         for (int q = warp; q < P && ok; q += kNW) ok = decode_tile(q, dense + q * kSlot);
+        // the activations are copied in by the producer warp once the previous
+        // launch has finished; wait for that launch first (the wait below is
+        // bounded), then for the copies
         us::pdl_wait();
-        // activations: each warp fetches the K slices of its own tiles (all its
-        // loads in flight before the first store) and goes on by itself; no
-        // warp waits for another one here
-        int8_t* xw = xs + (int64_t)warp * p.sk_tw * NTOK * XROW;
-        {
-            const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.X);
-            // dp4a: 4-byte words (8 codes, 8 per K tile), each expanded to 8 int8;
-            // mma: 16-byte pieces (32 codes, 2 per K tile) copied as they are
-            constexpr int kPieceB = NT ? 16 : 4;
-            constexpr int kPerTile = 32 / kPieceB;
-            constexpr int kPerJ = NTOK * kPerTile;
-            const int T = per > warp ? (per - warp + kNW - 1) / kNW : 0;
-            const int total = T * kPerJ;
-            constexpr int kU = NT == 4 ? 4 : 8;
-            // the token scales travel in the same round trip
-            uint16_t sxv = 0;
-            if (p.Y && threadIdx.x < NTOK && threadIdx.x < p.N) sxv = p.s_x[threadIdx.x];
-            for (int i0 = lane; i0 < total; i0 += kU * 32) {
-                uint4 v[kU];
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int i = i0 + u * 32;
-                    v[u] = make_uint4(0u, 0u, 0u, 0u);              // absent tokens: code 0
-                    const int j = i / kPerJ, r = i - j * kPerJ, n = r / kPerTile, hh = r - n * kPerTile;
-                    if (i < total && n < p.N) {
-                        const int tk = (t0 + warp + j * kNW) % p.nTK;
-                        const uint8_t* src = xg + (int64_t)n * (p.K / 2) + (int64_t)tk * (kTK / 2) + kPieceB * hh;
-                        if (NT) v[u] = __ldg(reinterpret_cast<const uint4*>(src));
-                        else v[u].x = __ldg(reinterpret_cast<const uint32_t*>(src));
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int i = i0 + u * 32;
-                    if (i >= total) break;
-                    const int j = i / kPerJ, r = i - j * kPerJ, n = r / kPerTile, hh = r - n * kPerTile;
-                    int8_t* dst = xw + (int64_t)(j * NTOK + n) * XROW;
-                    if (NT) {
-                        *reinterpret_cast<uint4*>(dst + 16 * hh) = v[u];
-                    } else {
-                        const uint32_t lo = v[u].x & 0x0F0F0F0Fu, hi = (v[u].x >> 4) & 0x0F0F0F0Fu;
-                        const uint32_t e0 = __vsub4(__byte_perm(lo, hi, 0x5140) ^ 0x08080808u, 0x08080808u);
-                        const uint32_t e1 = __vsub4(__byte_perm(lo, hi, 0x7362) ^ 0x08080808u, 0x08080808u);
-                        *reinterpret_cast<uint2*>(dst + 8 * hh) = make_uint2(e0, e1);
-                    }
-                }
-            }
-            if (p.Y && threadIdx.x < NTOK) sxs[threadIdx.x] = sxv;
+        if (ok && !us::mbar_wait(&S.xfull, 0u, p.status)) {
+            S.abort = 1;
+            ok = false;
         }
         // the epilogue reads the row scales after the block-wide barrier
         if (p.Y && !early)
             for (int i = threadIdx.x; i < nb * kTM; i += kNW * 32) sws[i] = p.s_w[band0 * kTM + i];
-        __syncwarp();
+        const bool all_k = p.sk_xcols == p.nTK;
 
         // After the wait: tile q < P is read from its dense tile; a later one is
         // decoded now into this warp's own slot (slot w held tile w, done by
@@ -408,7 +394,8 @@ w4a4_sk_kernel(const UsKParams p) {
                     if (!(ok = decode_tile(q, dense + warp * kSlot))) break;
                 }
                 // rows lane and lane + 32, eight words each: byte i of word k holds
-                // positions 8k + i (low nibble) and 8k + 4 + i (high nibble)
+                // positions 8k + 2i (low nibble) and 8k + 2i + 1 (high nibble), as
+                // the packed activations do
                 uint32_t pw[2][8];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -419,16 +406,18 @@ w4a4_sk_kernel(const UsKParams p) {
                     pw[h][4] = b.x; pw[h][5] = b.y; pw[h][6] = b.z; pw[h][7] = b.w;
                 }
                 __syncwarp();                                 // the slot may be refilled next
-                const int8_t* xt = xw + (int64_t)((q - warp) / kNW) * N * kTK;
+                const int8_t* xt = xs + (int64_t)(all_k ? t % p.nTK : q) * XROW;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
 #pragma unroll
                     for (int n = 0; n < N; ++n) {
-                        const uint2 xv = *reinterpret_cast<const uint2*>(xt + n * kTK + 8 * k);
+                        // even and odd positions as 16 x, against 16 w: 256 w x
+                        const uint32_t xv = *reinterpret_cast<const uint32_t*>(xt + (int64_t)n * p.sk_xcols * XROW + 4 * k);
+                        const int xe = (int)((xv << 4) & 0xF0F0F0F0u), xo = (int)(xv & 0xF0F0F0F0u);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            acc[h][n] = __dp4a((int)((pw[h][k] << 4) & 0xF0F0F0F0u), (int)xv.x, acc[h][n]);   // 16 w
-                            acc[h][n] = __dp4a((int)(pw[h][k] & 0xF0F0F0F0u), (int)xv.y, acc[h][n]);
+                            acc[h][n] = __dp4a((int)((pw[h][k] << 4) & 0xF0F0F0F0u), xe, acc[h][n]);
+                            acc[h][n] = __dp4a((int)(pw[h][k] & 0xF0F0F0F0u), xo, acc[h][n]);
                         }
                     }
                 }
@@ -494,10 +483,10 @@ w4a4_sk_kernel(const UsKParams p) {
                 }
                 // B fragments: token 8 nt + g, positions 16 tig .. 16 tig + 15 as fp16
                 uint32_t bf[NT][8];
-                const int8_t* xt = xw + (int64_t)((q - warp) / kNW) * NTOK * XROW;
+                const int8_t* xt = xs + (int64_t)(all_k ? t % p.nTK : q) * XROW;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const uint2 v = *reinterpret_cast<const uint2*>(xt + (8 * nt + g) * XROW + 8 * tig);
+                    const uint2 v = *reinterpret_cast<const uint2*>(xt + (int64_t)(8 * nt + g) * p.sk_xcols * XROW + 8 * tig);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint32_t w = hh ? v.y : v.x;
@@ -540,13 +529,14 @@ w4a4_sk_kernel(const UsKParams p) {
         // a wait gave up: let the copies still in flight land (bounded); this
         // call's outputs are not valid (US_ERR_TIMEOUT is recorded)
         for (int ch = tail; ch < issued; ++ch) us::mbar_wait(&S.full[ch % kR], (uint32_t)(ch / kR) & 1u, nullptr);
+        us::mbar_wait(&S.xfull, 0u, nullptr);
     }
     us::pdl_wait();                                           // before the first global write
 
     // ------------------------------------------------------------- epilogue
-    // dp4a accumulators hold 16 * sum (weights sit in the high nibble): >> 4 is
-    // exact; the mma ones hold the sum itself
-    constexpr int kShift = NT ? 0 : 4;
+    // dp4a accumulators hold 256 * sum (weights and activations sit in high
+    // nibbles): >> 8 is exact; the mma ones hold the sum itself
+    constexpr int kShift = NT ? 0 : 8;
     auto store = [&](int br, int i, int a16) {
         const int n = i / kTM, r = i - n * kTM;
         if (n >= p.N) return;                                 // padding tokens of the mma consumer
@@ -633,7 +623,7 @@ namespace {
 // Shared-memory plan of one launch; false when it does not fit.  `pre`: the
 // weights are static, so tiles may be decoded before the dependency wait.
 struct SkPlan {
-    int NT, G, per, tw, nb, ring, slots, pre;
+    int NT, G, per, xcols, nb, ring, slots, pre;
     size_t smem;
 };
 
@@ -652,15 +642,16 @@ bool sk_plan(int nTM, int nTK, int N, bool pre, SkPlan& pl) {
     pl.NT = nt_for_tokens(N);
     if (pl.NT == 0 && N > 8) return false;
     if (pl.NT && nTK * kTK > (1 << 18)) return false;       // fp32 sums of int4 products stay exact
-    const int ntok = ntok_for(N, pl.NT), xrow = xrow_for(pl.NT);
+    if (!pl.NT && nTK * kTK > (1 << 17)) return false;      // int32 sums of 256 w x do not overflow
+    const int ntok = ntok_for(N, pl.NT);
     const int nw = nw_for(N, pl.NT);
     const int nT = nTM * nTK;
     pl.G = us::num_sms() < nT ? us::num_sms() : nT;
     pl.per = (nT + pl.G - 1) / pl.G;
-    pl.tw = (pl.per + nw - 1) / nw;
+    pl.xcols = pl.per < nTK ? pl.per : nTK;
     pl.nb = (pl.per + nTK - 1) / nTK + 1;
     const size_t fixed = kHeader + kLutBytes + (size_t)((pl.per + 1 + 3) & ~3) * 4 +
-                         (size_t)nw * pl.tw * ntok * xrow + (size_t)pl.nb * ntok * kTM * 4 +
+                         (size_t)ntok * pl.xcols * (kTK / 2) + (size_t)pl.nb * ntok * kTM * 4 +
                          (((size_t)pl.nb * kTM + ntok) * 2 + 15) / 16 * 16;
     // every warp needs a slot of its own; static weights want one per tile
     const int want = pre ? (pl.per > nw ? pl.per : nw) : nw;
@@ -684,7 +675,7 @@ us_status launch_sk_n(UsKParams p, const SkPlan& pl, cudaStream_t st) {
     auto kern = w4a4_sk_kernel<N, NT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) != cudaSuccess)
         return US_ERR_CUDA;
-    p.sk_grid = pl.G; p.sk_per = pl.per; p.sk_ring = pl.ring; p.sk_tw = pl.tw; p.sk_nb = pl.nb;
+    p.sk_grid = pl.G; p.sk_per = pl.per; p.sk_ring = pl.ring; p.sk_xcols = pl.xcols; p.sk_nb = pl.nb;
     p.sk_slots = pl.slots; p.sk_pre = pl.pre;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.G);
