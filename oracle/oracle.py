@@ -19,7 +19,9 @@ What each call restates:
   scales.
 * ``spmm_f16`` / ``spmspv_f16``: Y = W.X in fp64, rounded once to fp16; the
   spMspV form skips columns whose activation fails |x_k| > tau (SPDP section 2,
-  dynamic pruning W (.) M(x)).
+  dynamic pruning W (.) M(x)); ``spmspv_f16_batched`` applies it per token.
+* ``colinfo``: the ColInfo array of SPDP section 4.1 (per tile column: its
+  offset in the tile's value run and its nonzero count).
 """
 from __future__ import annotations
 
@@ -88,9 +90,10 @@ def _load():
         lib.or_spmm_f16_at.argtypes = [P, P, i32, i32, i32, P, P, i64, P, P]
         lib.or_spmspv_f16.argtypes = [P, P, ctypes.c_float, i32, i32, P, P, i32]
         lib.or_quantize_x.argtypes = [P, i32, i32, P, P]
+        lib.or_colinfo.argtypes = [P, i32, i32, i32, i32, P]
         lib.or_max_threads.argtypes = []
         for name in ("or_num_tiles", "or_encode", "or_decode", "or_spmm_w4a4", "or_spmm_w4a4_at",
-                     "or_spmm_f16", "or_spmm_f16_at", "or_spmspv_f16", "or_max_threads"):
+                     "or_spmm_f16", "or_spmm_f16_at", "or_spmspv_f16", "or_colinfo", "or_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -251,6 +254,25 @@ def spmspv_f16(Wd: np.ndarray, x: np.ndarray, tau: float = 0.0, nthreads: int = 
     _check(_load().or_spmspv_f16(_ptr(Wd), _ptr(x), float(tau), M, K, _ptr(y), _ptr(ex), nthreads),
            "spmspv_f16")
     return y.view(np.float16), ex
+
+
+def spmspv_f16_batched(Wd: np.ndarray, X: np.ndarray, tau: float = 0.0, nthreads: int = 1):
+    """Batched dynamic pruning: token n keeps X[n][k] iff |X[n][k]| > tau, so
+    each token's row of the result is its own spMspV.  Wd: M x K fp16, X: N x K
+    fp16.  Returns (Y fp16 N x M, exact fp64 sums N x M)."""
+    X = np.atleast_2d(X)
+    ys, exs = zip(*(spmspv_f16(Wd, X[n], tau, nthreads) for n in range(X.shape[0])))
+    return np.stack(ys), np.stack(exs)
+
+
+def colinfo(bitmap: np.ndarray, M: int, K: int, TM: int, TK: int) -> np.ndarray:
+    """ColInfo of a COL-order bitmap (SPDP section 4.1): uint32 per column of
+    every tile, tile-major, (offset within the tile's run << 16) | nnz."""
+    bitmap = np.ascontiguousarray(bitmap, dtype=np.uint64)
+    nT = num_tiles(M, K, TM, TK)
+    out = np.zeros(nT * TK, np.uint32)
+    _check(_load().or_colinfo(_ptr(bitmap), M, K, TM, TK, _ptr(out)), "colinfo")
+    return out
 
 
 def quantize_x(X: np.ndarray):

@@ -345,6 +345,34 @@ int or_spmspv_f16(const uint16_t* Wd, const uint16_t* x, float tau, int M, int K
     return OR_OK;
 }
 
+/* ColInfo ([SPDP] section 4.1, Tiled-CBC storage structure): for a COL-order
+ * matrix, one 32-bit word per column of every tile, tile-major
+ * (colinfo[t*TK + j]); the upper 16 bits hold the column's starting offset
+ * inside the tile's value run (TileOffset_Col: the nonzeros of the columns
+ * before it in the same tile), the lower 16 bits its number of nonzeros
+ * (NNZ_Column).  Read off the bitmap one position at a time. */
+int or_colinfo(const uint64_t* bitmap, int M, int K, int TM, int TK, uint32_t* colinfo) {
+    int64_t nT;
+    int rc = or_num_tiles(M, K, TM, TK, &nT);
+    if (rc != OR_OK) return rc;
+    if (!bitmap || !colinfo) return OR_BAD_ARG;
+    const int64_t words = (int64_t)TM * TK / 64;
+    for (int64_t t = 0; t < nT; ++t) {
+        const uint64_t* bm = bitmap + t * words;
+        uint32_t offset = 0;
+        for (int j = 0; j < TK; ++j) {
+            uint32_t nnz = 0;
+            for (int i = 0; i < TM; ++i) {
+                const int64_t pos = (int64_t)j * TM + i;          /* COL scan: p = j*TM + i */
+                if ((bm[pos / 64] >> (pos % 64)) & 1u) ++nnz;
+            }
+            colinfo[t * TK + j] = (offset << 16) | nnz;
+            offset += nnz;
+        }
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------- activation quantisation ---- */
 /* Per-token symmetric int4 quantisation of fp16 activations ([UnionSparse]
  * Fig. 2, the "Quant" step between FP16 X and INT4 X; the page fixes the

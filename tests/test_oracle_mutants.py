@@ -32,6 +32,11 @@ MUTANTS = {
     "quant_truncates": ("float q = rintf(v / s);", "float q = truncf(v / s);"),
     "quant_rounds_half_up": ("float q = rintf(v / s);", "float q = floorf(v / s + 0.5f);"),
     "quant_signed_max": ("const float a = fabsf(or_half_to_float(x[k]));", "const float a = or_half_to_float(x[k]);"),
+    "colinfo_row_scan": ("const int64_t pos = (int64_t)j * TM + i;          /* COL scan: p = j*TM + i */",
+                         "const int64_t pos = (int64_t)i * TK + j;          /* COL scan: p = j*TM + i */"),
+    "colinfo_offset_inclusive": ("            colinfo[t * TK + j] = (offset << 16) | nnz;\n            offset += nnz;",
+                                 "            offset += nnz;\n            colinfo[t * TK + j] = (offset << 16) | nnz;"),
+    "colinfo_fields_swapped": ("colinfo[t * TK + j] = (offset << 16) | nnz;", "colinfo[t * TK + j] = (nnz << 16) | offset;"),
     "tile_numbering_colmajor": ("            const int64_t t = (int64_t)tm * nTK + tk;\n            uint64_t* words = bitmap",
                                 "            const int64_t t = (int64_t)tk * nTM + tm;\n            uint64_t* words = bitmap"),
 }

@@ -375,3 +375,86 @@ def test_quantize_invariants(orc):
     assert np.all(err <= sf[:, None] * (0.5 + 1e-3))
     c4, s4 = orc.quantize_x((X.astype(np.float32) * 4).astype(np.float16))
     assert np.array_equal(c4, codes) and np.array_equal(s4.astype(np.float32), s.astype(np.float32) * 4)
+
+
+# ------------------------------------------------------------------ ColInfo --
+def _colinfo_from_dense(W: np.ndarray, TM: int, TK: int) -> np.ndarray:
+    """ColInfo counted on the dense matrix itself (no bitmap): per tile, per
+    column, its nonzeros and the nonzeros of the columns before it."""
+    M, K = W.shape
+    out = []
+    for tm in range(M // TM):
+        for tk in range(K // TK):
+            blk = W[tm * TM:(tm + 1) * TM, tk * TK:(tk + 1) * TK]
+            nnz = np.count_nonzero(blk.astype(np.float32) != 0, axis=0)
+            off = np.concatenate([[0], np.cumsum(nnz)[:-1]])
+            out.append((off.astype(np.uint32) << 16) | nnz.astype(np.uint32))
+    return np.concatenate(out)
+
+
+def test_colinfo_worked_example(orc):
+    """Column j of the only tile holds j nonzeros (rows 0..j-1): NNZ_Column = j
+    and TileOffset_Col = 0 + 1 + ... + (j - 1) = j (j - 1) / 2."""
+    TM, TK = 64, 16
+    W = np.zeros((TM, TK), np.float16)
+    for j in range(TK):
+        W[:j, j] = 1.0 + j
+    bm, off, vals = orc.encode(W, TM, TK, F16, COL)
+    ci = orc.colinfo(bm, TM, TK, TM, TK)
+    assert [int(v) & 0xFFFF for v in ci] == list(range(TK))
+    assert [int(v) >> 16 for v in ci] == [j * (j - 1) // 2 for j in range(TK)]
+
+
+@pytest.mark.parametrize("shape", [(128, 256, 64, 64), (256, 64, 256, 16), (192, 384, 64, 128), (128, 96, 128, 32)])
+def test_colinfo_matches_dense_counts(orc, shape):
+    M, K, TM, TK = shape
+    rng = np.random.default_rng(M + K)
+    W = _rand_f16(rng, M, K, 0.45)
+    W[:, 5] = 0                                     # an empty column
+    W[: TM, K - 1] = 1.0                            # a full column
+    bm, off, vals = orc.encode(W, TM, TK, F16, COL)
+    ci = orc.colinfo(bm, M, K, TM, TK)
+    assert np.array_equal(ci, _colinfo_from_dense(W, TM, TK))
+
+
+def test_colinfo_addresses_each_column_run(orc):
+    """TileOffset_Col points at the column's first value in the tile's run and
+    NNZ_Column values follow: they are that column's nonzeros in row order."""
+    M, K, TM, TK = 128, 128, 64, 32
+    rng = np.random.default_rng(3)
+    W = _rand_f16(rng, M, K, 0.5)
+    bm, off, vals = orc.encode(W, TM, TK, F16, COL)
+    ci = orc.colinfo(bm, M, K, TM, TK)
+    v16 = vals.view(np.float16)
+    nTK = K // TK
+    for t in range((M // TM) * nTK):
+        tm, tk = divmod(t, nTK)
+        for j in range(TK):
+            o, n = int(ci[t * TK + j]) >> 16, int(ci[t * TK + j]) & 0xFFFF
+            col = W[tm * TM:(tm + 1) * TM, tk * TK + j]
+            want = col[col.astype(np.float32) != 0]
+            got = v16[int(off[t]) + o: int(off[t]) + o + n]
+            assert np.array_equal(got.view(np.uint16), want.view(np.uint16)), (t, j)
+
+
+def test_batched_spmspv_pins(orc):
+    """Per-token dynamic pruning: with tau = 0 and no zero activations the
+    batched spMspV is the dense fp16 product; a token whose activations all
+    fail the test gives zeros; every row equals that token's own spMspV."""
+    rng = np.random.default_rng(8)
+    M, K, N = 96, 128, 4
+    W = _rand_f16(rng, M, K, 0.5)
+    X = rng.standard_normal((N, K)).astype(np.float16)
+    X[X == 0] = np.float16(0.5)
+    Y0, ex0 = orc.spmspv_f16_batched(W, X, 0.0)
+    Yd = orc.spmm_f16(W, X)
+    assert np.array_equal(Y0.view(np.uint16), Yd.view(np.uint16))
+    X[2] = np.clip(X[2], -0.25, 0.25)
+    Y1, ex1 = orc.spmspv_f16_batched(W, X, 0.25)
+    assert not Y1[2].view(np.uint16).any()
+    for n in range(N):
+        y, e = orc.spmspv_f16(W, X[n], 0.25)
+        assert np.array_equal(Y1[n].view(np.uint16), y.view(np.uint16))
+    # the pruned product equals the dense product of the pruned activations
+    Xp = np.where(np.abs(X.astype(np.float32)) > 0.25, X, np.float16(0))
+    assert np.allclose(ex1, Xp.astype(np.float64) @ W.astype(np.float64).T, rtol=0, atol=1e-9)
