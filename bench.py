@@ -490,6 +490,26 @@ def measure_extras(us, torch, wl, dev, stream):
         sp[f"zeros_{int(zf * 100)}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
                                         "GB/s": round(alg / (t * 1e-6) / 1e9, 1)}
     out["spmspv_f16_14336x4096"] = sp
+    # the same with ColInfo (per tile column: offset and count), N = 1 and a batch of 8
+    cis = [us.us_colinfo(E, None, stream) for E in cps]
+    stream.synchronize()
+    nTM_s = 14336 // 64
+    sci = {}
+    for zf, N in ((0.5, 1), (0.7, 1), (0.9, 1), (0.9, 8), (0.7, 8)):
+        X = np.stack([wl.relu_threshold(rng.standard_normal(4096).astype(np.float32), zf) for _ in range(N)])
+        X = X.astype(np.float16)
+        Xt = torch.from_numpy(X.view(np.int16)).to(dev)
+        Yt = torch.empty(N, 14336, dtype=torch.int16, device=dev)
+        active = (np.abs(X.astype(np.float32)) > 0).any(axis=0)
+        alg = (4 * nTM_s * 4096 + 4 * (nTM_s * 64 + 1) + nTM_s * int(active.sum()) * 8 +
+               int(Wnz[:, active].sum()) * 2 + N * 4096 * 2 + N * 14336 * 2)
+        ms = time_graph(torch, stream,
+                        lambda: [us.us_spmspv_f16_ci(E, c, Xt, N, 0.0, Yt, None, stream) for E, c in zip(cps, cis)])
+        t = ms * 1e3 / n_cp
+        sci[f"zeros_{int(zf * 100)}_N{N}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
+                                              "active_columns": round(float(active.mean()), 3),
+                                              "GB/s": round(alg / (t * 1e-6) / 1e9, 1)}
+    out["spmspv_colinfo_f16_14336x4096"] = sci
     # encoder, W4A4 4096^2 (dense int8 codes in): count + scan + pack
     d = wl.w4a4(4096, 4096, 1, 0.5, seed=0)
     Wd = torch.from_numpy(d["Wq"]).to(dev)

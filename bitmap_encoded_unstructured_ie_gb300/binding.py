@@ -6,7 +6,8 @@ library has not been built, the first call raises ``LibraryMissing``: there is
 no CPU fallback.
 
 Function names follow the C ABI: ``us_encode``, ``us_spmm_w4a4``,
-``us_spmm_f16``, ``us_spmspv_f16``, ``us_quantize_x``, ``us_workspace_bytes``, ``us_pick_split_k``,
+``us_spmm_f16``, ``us_spmspv_f16``, ``us_colinfo``, ``us_spmspv_f16_ci``, ``us_quantize_x``,
+``us_workspace_bytes``, ``us_pick_split_k``,
 ``us_validate``, ``us_get_last_device_status``.
 """
 from __future__ import annotations
@@ -29,7 +30,7 @@ US_OP_ENCODE, US_OP_SPMM_W4A4, US_OP_SPMM_F16, US_OP_SPMSPV_F16 = 0, 1, 2, 3
 US_BITMAP_STATIC = 1
 
 EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmm_f16_noalloc", "us_spmspv_f16",
-            "us_quantize_x",
+            "us_colinfo", "us_spmspv_f16_ci", "us_quantize_x",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
             "us_status_string", "us_version")
 
@@ -74,6 +75,8 @@ def load(path: str = LIB_PATH):
         lib.us_spmm_f16.argtypes = [pbm, P, i32, P, P, sz, i32, P]
         lib.us_spmm_f16_noalloc.argtypes = [pbm, P, i32, P, i32, P]
         lib.us_spmspv_f16.argtypes = [pbm, P, ctypes.c_float, P, P, sz, P]
+        lib.us_colinfo.argtypes = [pbm, P, P]
+        lib.us_spmspv_f16_ci.argtypes = [pbm, P, P, i32, ctypes.c_float, P, P, sz, P]
         lib.us_quantize_x.argtypes = [P, i32, i32, P, P, P]
         lib.us_workspace_bytes.argtypes = [i32, pbm, i32, i32, psz]
         lib.us_pick_split_k.argtypes = [i32, pbm, i32, ctypes.POINTER(ctypes.c_int)]
@@ -227,6 +230,30 @@ def us_spmspv_f16(E: Encoded, x: torch.Tensor, tau: float, y: torch.Tensor, ws: 
     d = E.desc()
     _check("us_spmspv_f16", load().us_spmspv_f16(ctypes.byref(d), _dptr(x), float(tau), _dptr(y), _dptr(ws),
                                                  ws.numel(), _stream(stream)))
+
+
+def colinfo_words(E: Encoded) -> int:
+    """Number of uint32 ColInfo words of a COL-order matrix (one per tile column)."""
+    return (E.M // E.TM) * E.K
+
+
+def us_colinfo(E: Encoded, colinfo: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """ColInfo of a COL-order matrix: int32 tensor (bit pattern of uint32) of
+    (M / TM) * K words, tile-major, (offset << 16) | nnz per tile column."""
+    if colinfo is None:
+        colinfo = torch.empty(colinfo_words(E), dtype=torch.int32, device=E.bitmap.device)
+    d = E.desc()
+    _check("us_colinfo", load().us_colinfo(ctypes.byref(d), _dptr(colinfo), _stream(stream)))
+    return colinfo
+
+
+def us_spmspv_f16_ci(E: Encoded, colinfo: torch.Tensor, X: torch.Tensor, N: int, tau: float, Y: torch.Tensor,
+                     ws: torch.Tensor | None = None, stream=None):
+    """Batched spMspV through ColInfo: X N x K fp16 (bit pattern), Y N x M."""
+    d = E.desc()
+    _check("us_spmspv_f16_ci", load().us_spmspv_f16_ci(ctypes.byref(d), _dptr(colinfo), _dptr(X), N, float(tau),
+                                                       _dptr(Y), _dptr(ws), ws.numel() if ws is not None else 0,
+                                                       _stream(stream)))
 
 
 def us_quantize_x(X: torch.Tensor, N: int, K: int, Xq: torch.Tensor, s_x: torch.Tensor, stream=None):

@@ -364,6 +364,31 @@ us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16
     return us::launch_spmspv(p, static_cast<cudaStream_t>(stream));
 }
 
+us_status us_colinfo(const us_bitmap* W, uint32_t* colinfo, void* stream) {
+    if (!W) return US_ERR_INVALID_ARG;
+    us_status s = check_bitmap(W, W->elem, US_ORDER_COL);
+    if (s != US_OK) return s;
+    if (!colinfo || !aligned16(colinfo)) return US_ERR_INVALID_ARG;
+    const int64_t nT = (int64_t)(W->M / W->TM) * (W->K / W->TK);
+    return us::launch_colinfo(W->bitmap, W->TM, W->TK, nT, colinfo, static_cast<cudaStream_t>(stream));
+}
+
+us_status us_spmspv_f16_ci(const us_bitmap* W, const uint32_t* colinfo, const uint16_t* X, int N, float tau,
+                           uint16_t* Y, void* ws, size_t ws_bytes, void* stream) {
+    us_status s = check_bitmap(W, US_F16, US_ORDER_COL);
+    if (s != US_OK) return s;
+    if (N < 1 || !colinfo || !X || !Y || !aligned16(colinfo) || !aligned16(X) || !aligned16(Y) || !(tau >= 0.f))
+        return US_ERR_INVALID_ARG;
+    if ((int64_t)N * W->K >= ((int64_t)1 << 31) || (int64_t)N * W->M >= ((int64_t)1 << 31)) return US_ERR_TOO_LARGE;
+    const Plan pl = plan_spmspv(W);
+    if (pl.ws && (!ws || ws_bytes < pl.ws || !aligned16(ws))) return US_ERR_WORKSPACE;
+    UsKParams p;
+    fill_common(p, W, N);
+    p.X = X; p.Y = Y; p.tau = tau;
+    p.split = pl.split; p.tok_block = 1;
+    return us::launch_spmspv_ci(p, colinfo, static_cast<cudaStream_t>(stream));
+}
+
 us_status us_quantize_x(const uint16_t* X, int N, int K, uint8_t* Xq, uint16_t* s_x, void* stream) {
     if (N < 1 || K < 32 || K % 32 || (int64_t)N * K >= ((int64_t)1 << 32)) return US_ERR_INVALID_ARG;
     if (!X || !Xq || !s_x || !aligned16(X) || !aligned16(Xq)) return US_ERR_INVALID_ARG;

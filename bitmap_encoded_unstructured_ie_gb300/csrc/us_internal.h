@@ -48,6 +48,8 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
 
 // spMspV (us_spmspv.cu)
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st);
+us_status launch_colinfo(const uint64_t* bitmap, int TM, int TK, int64_t nT, uint32_t* colinfo, cudaStream_t st);
+us_status launch_spmspv_ci(const UsKParams& p, const uint32_t* colinfo, cudaStream_t st);
 size_t spmspv_ws(int M, int TM, int split);
 int spmspv_max_split();
 

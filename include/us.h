@@ -173,6 +173,31 @@ us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint
 us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* ColInfo of a COL-order matrix ("Unified Static-Dynamic Pruning for
+ * Efficient LLM Inference", section 4.1, Tiled-CBC storage structure): one
+ * uint32 per column of every tile, tile-major (colinfo[t * TK + j] for tile t,
+ * column j), holding (offset << 16) | nnz: nnz is the number of nonzeros of
+ * the column, offset the number of nonzeros of the columns before it in the
+ * same tile, i.e. where the column's values start in the tile's value run.
+ * Derived from the bitmap alone, for either element type.  colinfo: device,
+ * nT * TK * 4 bytes, 16-byte aligned, written in full.  W->order must be
+ * US_ORDER_COL (US_ERR_UNSUPPORTED otherwise). */
+us_status us_colinfo(const us_bitmap* W, uint32_t* colinfo, void* stream);
+
+/* Batched fp16 spMspV with column metadata (SPDP section 4.2, dynamic pruning
+ * per token):  Y[n][m] = fp16(sum over k with |X[n][k]| > tau of
+ * W[m][k] * X[n][k]), fp32 accumulation.  A column is fetched only if some
+ * token keeps its activation; it is found through colinfo (us_colinfo of the
+ * same W), so an inactive column costs 4 bytes of metadata and neither bitmap
+ * words nor values.  W: elem US_F16, order US_ORDER_COL.  X: N x K fp16
+ * token-major, Y: N x M fp16 token-major, N >= 1, tau >= 0.  ws may be NULL
+ * (us_workspace_bytes for US_OP_SPMSPV_F16 gives the size, currently 0).
+ * colinfo that disagrees with the bitmap or overruns a tile's run records
+ * US_ERR_CORRUPT (us_get_last_device_status); such a column contributes only
+ * the values inside its run. */
+us_status us_spmspv_f16_ci(const us_bitmap* W, const uint32_t* colinfo, const uint16_t* X, int N, float tau,
+                           uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
+
 /* Per-token int4 quantisation of fp16 activations (UnionSparse Fig. 2, the
  * "Quant" step from FP16 X to INT4 X with a per-token scale; the page does not
  * fix the rounding, this is the plain symmetric reading):

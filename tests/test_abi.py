@@ -129,3 +129,15 @@ def test_bad_arguments_rejected_without_launch(lib):
     assert L.us_quantize_x(None, 4, 64, Y, P(0x40000), None) == 1
     assert L.us_quantize_x(P(0x20008), 4, 64, Y, P(0x40000), None) == 1
     assert L.us_quantize_x(X, 4, 64, Y, P(0x40001), None) == 1
+    # ColInfo and batched spMspV: COL order only, N >= 1, tau >= 0, aligned pointers
+    CI = P(0x60000)
+    assert L.us_colinfo(ctypes.byref(f16), CI, None) == 2                          # ROW order
+    assert L.us_colinfo(ctypes.byref(fcol), None, None) == 1
+    assert L.us_colinfo(ctypes.byref(fcol), P(0x60004), None) == 1
+    assert L.us_colinfo(None, CI, None) == 1
+    assert L.us_spmspv_f16_ci(ctypes.byref(f16), CI, X, 1, ctypes.c_float(0.0), Y, None, 0, None) == 2
+    assert L.us_spmspv_f16_ci(ctypes.byref(good), CI, X, 1, ctypes.c_float(0.0), Y, None, 0, None) == 1  # I4
+    assert L.us_spmspv_f16_ci(ctypes.byref(fcol), CI, X, 0, ctypes.c_float(0.0), Y, None, 0, None) == 1
+    assert L.us_spmspv_f16_ci(ctypes.byref(fcol), CI, X, 2, ctypes.c_float(-1.0), Y, None, 0, None) == 1
+    assert L.us_spmspv_f16_ci(ctypes.byref(fcol), None, X, 2, ctypes.c_float(0.0), Y, None, 0, None) == 1
+    assert L.us_spmspv_f16_ci(ctypes.byref(fcol), CI, P(0x20002), 2, ctypes.c_float(0.0), Y, None, 0, None) == 1
