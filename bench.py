@@ -530,6 +530,16 @@ def measure_extras(us, torch, wl, dev, stream):
         fl = 2 * 4096 * 4096 * N
         pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_4096_s60"] = pf
+    # the same on COL tiles: the format spMspV reads serves prefill too
+    Efc = us.us_encode(torch.from_numpy(f["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_COL)
+    pfc = {}
+    for N in (256, 1024, 2048):
+        Yf = torch.empty(N, 4096, dtype=torch.int16, device=dev)
+        wsf = us.workspace(us.US_OP_SPMM_F16, Efc, N)
+        ms = time_graph(torch, stream, lambda: us.us_spmm_f16(Efc, Xf[:N], N, Yf, wsf, 0, stream), 3)
+        fl = 2 * 4096 * 4096 * N
+        pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
+    out["prefill_f16_col_tiles_4096_s60"] = pfc
     # per-token activation quantisation, fp16 -> int4 + scale (reads 2NK, writes NK/2 + 2N bytes)
     qz = {}
     for N in (16, 2048):

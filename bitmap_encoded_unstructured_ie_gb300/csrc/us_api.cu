@@ -89,6 +89,7 @@ void fill_common(UsKParams& p, const us_bitmap* W, int N) {
     p.tau = 0.f; p.ws = nullptr; p.counters = nullptr;
     p.sk_grid = p.sk_per = p.sk_ring = p.sk_xcols = p.sk_nb = p.sk_slots = p.sk_pre = 0;
     p.flags = W->flags;
+    p.order = W->order;
     p.status = status_ptr();
 }
 
@@ -272,7 +273,8 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
 
 us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y, void* ws, size_t ws_bytes,
                       int split_k, void* stream) {
-    us_status s = check_bitmap(W, US_F16, US_ORDER_ROW);
+    // either scan order: ROW (IE-BME) or COL (Tiled-CBC, the spMspV format)
+    us_status s = check_bitmap(W, US_F16, W && W->order == US_ORDER_COL ? US_ORDER_COL : US_ORDER_ROW);
     if (s != US_OK) return s;
     if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
     if (!X || !Y || !aligned16(X) || !aligned16(Y)) return US_ERR_INVALID_ARG;
@@ -323,7 +325,7 @@ uint8_t* noalloc_scratch_ptr() {
 }  // namespace
 
 us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y, int split_k, void* stream) {
-    us_status s = check_bitmap(W, US_F16, US_ORDER_ROW);
+    us_status s = check_bitmap(W, US_F16, W && W->order == US_ORDER_COL ? US_ORDER_COL : US_ORDER_ROW);
     if (s != US_OK) return s;
     if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
     if (!X || !Y || !aligned16(X) || !aligned16(Y)) return US_ERR_INVALID_ARG;

@@ -267,6 +267,7 @@ struct UsKParams {
     uint16_t* Y;
     float tau;
     uint32_t flags;     // US_BITMAP_* flags of the weight descriptor
+    int order;          // US_ORDER_ROW or US_ORDER_COL scan inside a tile
     void* ws;           // split-K partials (after the counters)
     unsigned* counters; // split-K arrival counters, one per (band, token block)
     unsigned* status;

@@ -171,7 +171,9 @@ spmm_generic_kernel(const UsKParams p) {
         for (int pos = threadIdx.x; pos < npos; pos += kThreads) {
             const int w = pos >> 6, b = pos & 63;
             const uint64_t word = words[w];
-            const int i = pos / TK, j = pos - i * TK;
+            // ROW scan p = i TK + j (IE-BME); COL scan p = j TM + i (Tiled-CBC)
+            const int i = p.order == US_ORDER_COL ? pos % TM : pos / TK;
+            const int j = p.order == US_ORDER_COL ? pos / TM : pos - i * TK;
             const bool set = tile_ok && ((word >> b) & 1ull);
             uint32_t rank = 0;
             if (set) rank = wpre[w] + (uint32_t)__popcll(word & ((1ull << b) - 1ull));

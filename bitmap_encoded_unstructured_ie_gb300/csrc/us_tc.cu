@@ -70,6 +70,7 @@ struct TcParams {
     int n_tiles;          // ceil(N / kBN)
 };
 
+template <int ORDER>
 __global__ void __launch_bounds__(kThreads, 1)
 spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) {
     const UsKParams& p = tp.p;
@@ -170,65 +171,142 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         }
     } else {
         // ------------------------------------------------------------ decoders
-        const int d = warp - 2;                            // 0..7: rows 16d .. 16d+15
-        const int row = 16 * d + (lane >> 1);              // 0..127 within the block
-        const int hb = lane & 1;                           // which 32 positions of the row
-        const int band_h = row >> 6, i_in_band = row & 63;
-        for (int q = 0; q < nk; ++q) {
-            const int rs = q % kRawStages, s = q % kStages;
-            if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
-                failed = true;
-                break;
-            }
-            const uint8_t* r = raw + rs * kRawBytes;
-            const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
-            // row base: popcounts of the earlier rows of this band (warp scan)
-            const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
-            const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
-            uint32_t incl = packed;
-#pragma unroll
-            for (int dd = 1; dd < 32; dd <<= 1) {
-                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
-                if (lane >= dd) incl += o;
-            }
-            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-            const uint32_t ex = incl - packed;
-            const uint32_t exr = __shfl_sync(0xffffffffu, ex, i_in_band & 31);
-            const uint32_t rowbase = (i_in_band < 32) ? (exr & 0xFFFFu) : (tot & 0xFFFFu) + (exr >> 16);
-            const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
-            const bool ok = P <= S.raw_len[rs][band_h];
-            if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-            const uint64_t word = bm[i_in_band];
-            const uint32_t bits = hb ? (uint32_t)(word >> 32) : (uint32_t)word;
-            uint32_t rank = rowbase + (hb ? (uint32_t)__popc((uint32_t)word) : 0u);
-            const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
-            // wait for the A stage to be free (the MMA of step q - kStages finished)
-            if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
-                failed = true;
-                break;
-            }
-            uint8_t* arow = a_st + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {                  // 8 positions per 16-byte chunk
-                uint32_t h2[4];
-#pragma unroll
-                for (int j = 0; j < 8; j += 2) {
-                    const uint32_t b0 = ok ? (bits >> (8 * c + j)) & 1u : 0u;
-                    const uint32_t b1 = ok ? (bits >> (8 * c + j + 1)) & 1u : 0u;
-                    const uint32_t v0 = b0 ? run[rank] : 0u;
-                    rank += b0;
-                    const uint32_t v1 = b1 ? run[rank] : 0u;
-                    rank += b1;
-                    h2[j >> 1] = v0 | (v1 << 16);
+        if constexpr (ORDER == US_ORDER_ROW) {
+            const int d = warp - 2;                            // 0..7: rows 16d .. 16d+15
+            const int row = 16 * d + (lane >> 1);              // 0..127 within the block
+            const int hb = lane & 1;                           // which 32 positions of the row
+            const int band_h = row >> 6, i_in_band = row & 63;
+            for (int q = 0; q < nk; ++q) {
+                const int rs = q % kRawStages, s = q % kStages;
+                if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
+                    failed = true;
+                    break;
                 }
-                const int chunk = 4 * hb + c;
-                *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                const uint8_t* r = raw + rs * kRawBytes;
+                const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
+                // row base: popcounts of the earlier rows of this band (warp scan)
+                const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
+                const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
+                uint32_t incl = packed;
+    #pragma unroll
+                for (int dd = 1; dd < 32; dd <<= 1) {
+                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
+                    if (lane >= dd) incl += o;
+                }
+                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+                const uint32_t ex = incl - packed;
+                const uint32_t exr = __shfl_sync(0xffffffffu, ex, i_in_band & 31);
+                const uint32_t rowbase = (i_in_band < 32) ? (exr & 0xFFFFu) : (tot & 0xFFFFu) + (exr >> 16);
+                const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
+                const bool ok = P <= S.raw_len[rs][band_h];
+                if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
+                const uint64_t word = bm[i_in_band];
+                const uint32_t bits = hb ? (uint32_t)(word >> 32) : (uint32_t)word;
+                uint32_t rank = rowbase + (hb ? (uint32_t)__popc((uint32_t)word) : 0u);
+                const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
+                // wait for the A stage to be free (the MMA of step q - kStages finished)
+                if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
+                    failed = true;
+                    break;
+                }
+                uint8_t* arow = a_st + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
+    #pragma unroll
+                for (int c = 0; c < 4; ++c) {                  // 8 positions per 16-byte chunk
+                    uint32_t h2[4];
+    #pragma unroll
+                    for (int j = 0; j < 8; j += 2) {
+                        const uint32_t b0 = ok ? (bits >> (8 * c + j)) & 1u : 0u;
+                        const uint32_t b1 = ok ? (bits >> (8 * c + j + 1)) & 1u : 0u;
+                        const uint32_t v0 = b0 ? run[rank] : 0u;
+                        rank += b0;
+                        const uint32_t v1 = b1 ? run[rank] : 0u;
+                        rank += b1;
+                        h2[j >> 1] = v0 | (v1 << 16);
+                    }
+                    const int chunk = 4 * hb + c;
+                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                }
+                us::fence_proxy_async_smem();                  // generic writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) {
+                    us::mbar_arrive(&S.a_full[s]);
+                    us::mbar_arrive(&S.raw_empty[rs]);
+                }
             }
-            us::fence_proxy_async_smem();                  // generic writes -> visible to the tensor core
-            __syncwarp();
-            if (lane == 0) {
-                us::mbar_arrive(&S.a_full[s]);
-                us::mbar_arrive(&S.raw_empty[rs]);
+        } else {
+            // COL tiles (Tiled-CBC of "Unified Static-Dynamic Pruning for
+            // Efficient LLM Inference", section 4.1: one bitmap word per column,
+            // the values column after column).  A thread rebuilds 4 adjacent
+            // columns x 8 rows: per column, rank = column base (warp scan of the
+            // band's column popcounts) + popcount of the rows above + running
+            // count; per row it stores the 4 values as one 8-byte piece of the
+            // K-major swizzled A stage - the layout alignment of that page's
+            // section 4.3 done by the decoder's own stores.  Sixteen lanes (one
+            // 8-row group, all 16 column quads) fill 128 bytes of a row per step.
+            const int d = warp - 2;                        // 0..7
+            const int band_h = d >> 2;
+            const int quad = lane & 15;                    // columns 4 quad .. 4 quad + 3
+            const int rg = ((d & 3) << 1) | (lane >> 4);   // rows 8 rg .. 8 rg + 7 of the band
+            for (int q = 0; q < nk; ++q) {
+                const int rs = q % kRawStages, s = q % kStages;
+                if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
+                    failed = true;
+                    break;
+                }
+                const uint8_t* r = raw + rs * kRawBytes;
+                const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
+                const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
+                const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
+                uint32_t incl = packed;
+#pragma unroll
+                for (int dd = 1; dd < 32; dd <<= 1) {
+                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
+                    if (lane >= dd) incl += o;
+                }
+                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+                const uint32_t ex = incl - packed;
+                const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
+                const bool ok = P <= S.raw_len[rs][band_h];
+                if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
+                // the four columns' words, bases (lane j % 32 holds column j's) and
+                // first ranks at row 8 rg
+                uint32_t bits[4], rank[4];
+                const uint64_t below = rg ? (~0ull >> (64 - 8 * rg)) : 0ull;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = 4 * quad + c;
+                    const uint32_t e = __shfl_sync(0xffffffffu, ex, j & 31);
+                    const uint32_t base = j < 32 ? (e & 0xFFFFu) : (tot & 0xFFFFu) + (e >> 16);
+                    const uint64_t word = ok ? bm[j] : 0ull;
+                    rank[c] = base + (uint32_t)__popcll(word & below);
+                    bits[c] = (uint32_t)(word >> (8 * rg)) & 0xFFu;
+                }
+                const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
+                if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
+                    failed = true;
+                    break;
+                }
+                // row m = 64 band_h + 8 rg + i: 128 bytes at m * 128, chunk
+                // (4 quad >> 3) ^ (i), half (quad & 1) of it
+                uint8_t* arow = a_st + s * kABytes + (64 * band_h + 8 * rg) * 128 + (quad & 1) * 8;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t v[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t b = (bits[c] >> i) & 1u;
+                        v[c] = b ? run[rank[c]] : 0u;
+                        rank[c] += b;
+                    }
+                    *reinterpret_cast<uint2*>(arow + i * 128 + (((quad >> 1) ^ i) << 4)) =
+                        make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+                }
+                us::fence_proxy_async_smem();              // generic writes -> visible to the tensor core
+                __syncwarp();
+                if (lane == 0) {
+                    us::mbar_arrive(&S.a_full[s]);
+                    us::mbar_arrive(&S.raw_empty[rs]);
+                }
             }
         }
     }
@@ -370,11 +448,11 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     TcParams tp;
     tp.p = p;
     tp.n_tiles = (p.N + kBN - 1) / kBN;
-    if (cudaFuncSetAttribute(spmm_f16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
+    auto kern = p.order == US_ORDER_COL ? spmm_f16_tc_kernel<US_ORDER_COL> : spmm_f16_tc_kernel<US_ORDER_ROW>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
         return US_ERR_CUDA;
     dim3 grid((unsigned)(p.M / kBM), (unsigned)(tp.n_tiles * p.split));
-    spmm_f16_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(tp, map);
+    kern<<<grid, kThreads, kSmemBytes, st>>>(tp, map);
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }
 
