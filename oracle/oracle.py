@@ -20,6 +20,10 @@ What each call restates:
 * ``spmm_f16`` / ``spmspv_f16``: Y = W.X in fp64, rounded once to fp16; the
   spMspV form skips columns whose activation fails |x_k| > tau (SPDP section 2,
   dynamic pruning W (.) M(x)); ``spmspv_f16_batched`` applies it per token.
+* ``encode_ie`` / ``decode_ie`` / ``reorder_rows``: IE-BME with Q = RA*CA
+  areas (UnionSparse V-A, Fig. 7: one union mask, Q aligned value streams
+  CV[o_t + q P_t + rho]) and the bitmap-aware row reordering of V-B (exact
+  grouped subset DP, canonical permutation).
 * ``colinfo``: the ColInfo array of SPDP section 4.1 (per tile column: its
   offset in the tile's value run and its nonzero count).
 """
@@ -91,9 +95,14 @@ def _load():
         lib.or_spmspv_f16.argtypes = [P, P, ctypes.c_float, i32, i32, P, P, i32]
         lib.or_quantize_x.argtypes = [P, i32, i32, P, P]
         lib.or_colinfo.argtypes = [P, i32, i32, i32, i32, P]
+        lib.or_encode_ie.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, i32, P, P, P, P, u64,
+                                     ctypes.POINTER(u64)]
+        lib.or_decode_ie.argtypes = [P, P, P, u64, i32, i32, i32, i32, i32, i32, i32, P, P, i64]
+        lib.or_reorder_rows.argtypes = [P, i32, i32, i32, i32, P, ctypes.POINTER(ctypes.c_int)]
         lib.or_max_threads.argtypes = []
         for name in ("or_num_tiles", "or_encode", "or_decode", "or_spmm_w4a4", "or_spmm_w4a4_at",
-                     "or_spmm_f16", "or_spmm_f16_at", "or_spmspv_f16", "or_colinfo", "or_max_threads"):
+                     "or_spmm_f16", "or_spmm_f16_at", "or_spmspv_f16", "or_colinfo", "or_encode_ie",
+                     "or_decode_ie", "or_reorder_rows", "or_max_threads"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -273,6 +282,63 @@ def colinfo(bitmap: np.ndarray, M: int, K: int, TM: int, TK: int) -> np.ndarray:
     out = np.zeros(nT * TK, np.uint32)
     _check(_load().or_colinfo(_ptr(bitmap), M, K, TM, TK, _ptr(out)), "colinfo")
     return out
+
+
+def encode_ie(W: np.ndarray, TM: int, TK: int, RA: int, CA: int, elem: int, perm: np.ndarray | None = None):
+    """IE-BME with Q = RA*CA areas (UnionSparse V-A, Fig. 7): one union mask
+    per tile over (TM/RA) x (TK/CA) logical positions, Q aligned value streams.
+    perm: uint8, TM per tile (tile-major), row p of the reordered tile is
+    original row perm[t*TM + p]; None = identity.  Returns (bitmap, tile_off,
+    values)."""
+    W = np.ascontiguousarray(_dense_view(W, elem))
+    M, K = W.shape
+    nT = (M // TM) * (K // TK)
+    bitmap = np.zeros(max(nT * TM * TK // (64 * RA * CA), 1), dtype=np.uint64)
+    tile_off = np.zeros(nT + 1, dtype=np.uint32)
+    bits = 16 if elem == F16 else 4
+    cap = (M * K + nT * 32) * bits // 8 + 16
+    values = np.zeros(cap, dtype=np.uint8)
+    used = ctypes.c_uint64(0)
+    pp = None if perm is None else np.ascontiguousarray(perm, dtype=np.uint8)
+    _check(_load().or_encode_ie(_ptr(W), K, M, K, TM, TK, RA, CA, elem, None if pp is None else _ptr(pp),
+                                _ptr(bitmap), _ptr(tile_off), _ptr(values), cap, ctypes.byref(used)), "encode_ie")
+    return bitmap[: nT * TM * TK // (64 * RA * CA)], tile_off, values[: used.value]
+
+
+def decode_ie(bitmap, tile_off, values, M, K, TM, TK, RA, CA, elem, perm=None) -> np.ndarray:
+    bitmap = np.ascontiguousarray(bitmap, dtype=np.uint64)
+    tile_off = np.ascontiguousarray(tile_off, dtype=np.uint32)
+    values = np.ascontiguousarray(values, dtype=np.uint8)
+    out = np.zeros((M, K), dtype=np.uint16 if elem == F16 else np.int8)
+    pp = None if perm is None else np.ascontiguousarray(perm, dtype=np.uint8)
+    vp = _ptr(values) if values.size else None
+    _check(_load().or_decode_ie(_ptr(bitmap), _ptr(tile_off), vp, values.size, M, K, TM, TK, RA, CA, elem,
+                                None if pp is None else _ptr(pp), _ptr(out), K), "decode_ie")
+    return out.view(np.float16) if elem == F16 else out
+
+
+def reorder_rows(mask: np.ndarray, RA: int, CA: int):
+    """Bitmap-aware row reordering of one local tile (UnionSparse V-B,
+    Algorithm 1): exact grouped subset DP.  mask: HL x KL (nonzero = kept).
+    Returns (perm uint8 HL, minimum union-mask cost)."""
+    m = np.ascontiguousarray(mask != 0, dtype=np.uint8)
+    HL, KL = m.shape
+    perm = np.zeros(HL, np.uint8)
+    cost = ctypes.c_int(0)
+    _check(_load().or_reorder_rows(_ptr(m), HL, KL, RA, CA, _ptr(perm), ctypes.byref(cost)), "reorder_rows")
+    return perm, cost.value
+
+
+def reorder_matrix(W: np.ndarray, TM: int, TK: int, RA: int, CA: int) -> np.ndarray:
+    """Per-tile row permutations of a whole matrix (tile-major, TM bytes each)."""
+    Wv = np.asarray(W)
+    nz = (Wv.view(np.uint16) & 0x7FFF) != 0 if Wv.dtype == np.float16 else Wv != 0
+    M, K = Wv.shape
+    out = []
+    for tm in range(M // TM):
+        for tk in range(K // TK):
+            out.append(reorder_rows(nz[tm * TM:(tm + 1) * TM, tk * TK:(tk + 1) * TK], RA, CA)[0])
+    return np.concatenate(out)
 
 
 def quantize_x(X: np.ndarray):

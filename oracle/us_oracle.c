@@ -13,6 +13,8 @@
  *                 "IE-BME Representation" (Union Bitmaps, Union Value Offsets,
  *                 Compressed Values, Fig. 7) with Q = RA*CA = 1, and Fig. 2
  *                 (INT4 operands, INT32 result, dequantisation to FP16).
+ *                 Section V-A with Q = RA*CA areas and section V-B (bitmap-
+ *                 aware row reordering, Eq. 3-5, the grouped subset DP).
  *  [SPDP]         "Unified Static-Dynamic Pruning for Efficient LLM
  *                 Inference", section 4.1 "Tiled-CBC" (column tiles, values
  *                 in tile-column order, 4-byte TileOffset) and section 4.2.3
@@ -47,6 +49,7 @@
 #include <stddef.h>
 #include <string.h>
 #include <math.h>
+#include <stdlib.h>
 #ifdef _OPENMP
 #include <omp.h>
 #endif
@@ -342,6 +345,255 @@ int or_spmspv_f16(const uint16_t* Wd, const uint16_t* x, float tau, int M, int K
         if (exact_out) exact_out[m] = s;
         y[m] = or_double_to_half(s);
     }
+    return OR_OK;
+}
+
+/* ------------------------------------------------ IE-BME with Q areas ---- */
+/* [UnionSparse] V-A with Q = RA*CA > 1 (Fig. 7).  A local tile (LT) of TM x TK
+ * is split into RA row partitions and CA column partitions; area q = a*CA + c
+ * (a-th row partition, c-th column partition; the page leaves the numbering
+ * of the areas open, this is the row-partition-major reading) covers rows
+ * a*LM .. a*LM+LM-1 and columns c*LK .. c*LK+LK-1, LM = TM/RA, LK = TK/CA.
+ * The logical union mask B_t(i,j) = OR_q [W_t^(q)(i,j) != 0] (LM x LK) is
+ * scanned row-major and packed like the Q = 1 bitmap.  Every set logical
+ * position emits one value per area, zeros included, with the same compact
+ * rank rho: CV[o_t + q*P_t + rho] = W_t^(q)(i,j); the run of Q*P_t elements is
+ * zero-padded to 16 bytes and o_{t+1} = o_t + roundup(Q*P_t).
+ * Row reordering ([UnionSparse] V-B) acts before the areas are cut: perm (TM
+ * bytes per tile, tile-major; NULL = identity) names for each row p of the
+ * reordered tile the original row perm[t*TM + p] of that tile. */
+static int check_ie(int M, int K, int TM, int TK, int RA, int CA, int elem) {
+    if (M <= 0 || K <= 0 || TM <= 0 || TK <= 0 || RA <= 0 || CA <= 0) return OR_BAD_ARG;
+    if (M % TM || K % TK || TM % RA || TK % CA || TM > 256) return OR_BAD_ARG;
+    if (((int64_t)(TM / RA) * (TK / CA)) % 64) return OR_BAD_ARG;
+    if (elem != OR_F16 && elem != OR_I4) return OR_BAD_ARG;
+    if ((uint64_t)M * (uint64_t)K >= ((uint64_t)1 << 32)) return OR_TOO_LARGE;
+    return OR_OK;
+}
+
+static int perm_row(const uint8_t* perm, int64_t t, int TM, int p) {
+    return perm ? (int)perm[t * TM + p] : p;
+}
+
+int or_encode_ie(const void* W, int64_t ldw, int M, int K, int TM, int TK, int RA, int CA, int elem,
+                 const uint8_t* perm, uint64_t* bitmap, uint32_t* tile_off, uint8_t* values,
+                 uint64_t values_cap, uint64_t* values_used) {
+    int rc = check_ie(M, K, TM, TK, RA, CA, elem);
+    if (rc) return rc;
+    if (ldw < K) return OR_BAD_ARG;
+    const int nTM = M / TM, nTK = K / TK, Q = RA * CA, LM = TM / RA, LK = TK / CA;
+    const int64_t lpos = (int64_t)LM * LK, words_per_tile = lpos / 64;
+    const int E = elems_per_16B(elem);
+    if (elem == OR_I4) {
+        for (int r = 0; r < M; ++r)
+            for (int c = 0; c < K; ++c) {
+                int8_t q = ((const int8_t*)W)[(int64_t)r * ldw + c];
+                if (q < -8 || q > 7) return OR_BAD_ARG;
+            }
+    }
+    if (perm) {                                  /* each tile's perm must be a permutation */
+        for (int64_t t = 0; t < (int64_t)nTM * nTK; ++t) {
+            uint8_t seen[256] = {0};
+            for (int p = 0; p < TM; ++p) {
+                if (perm[t * TM + p] >= TM || seen[perm[t * TM + p]]) return OR_BAD_ARG;
+                seen[perm[t * TM + p]] = 1;
+            }
+        }
+    }
+    uint64_t off = 0;
+    tile_off[0] = 0;
+    for (int tm = 0; tm < nTM; ++tm) {
+        for (int tk = 0; tk < nTK; ++tk) {
+            const int64_t t = (int64_t)tm * nTK + tk;
+            uint64_t* words = bitmap + t * words_per_tile;
+            for (int64_t w = 0; w < words_per_tile; ++w) words[w] = 0;
+            /* the union mask and P_t */
+            uint64_t P = 0;
+            for (int64_t p = 0; p < lpos; ++p) {
+                const int i = (int)(p / LK), j = (int)(p % LK);
+                int any = 0;
+                for (int a = 0; a < RA; ++a)
+                    for (int c = 0; c < CA; ++c) {
+                        const int r = tm * TM + perm_row(perm, t, TM, a * LM + i);
+                        any |= dense_nonzero(W, ldw, elem, r, tk * TK + c * LK + j);
+                    }
+                if (any) {
+                    words[p / 64] |= (uint64_t)1 << (p % 64);
+                    ++P;
+                }
+            }
+            /* the Q aligned streams: CV[o_t + q P_t + rho] */
+            uint64_t rho = 0;
+            for (int64_t p = 0; p < lpos; ++p) {
+                if (!((words[p / 64] >> (p % 64)) & 1u)) continue;
+                const int i = (int)(p / LK), j = (int)(p % LK);
+                for (int a = 0; a < RA; ++a)
+                    for (int c = 0; c < CA; ++c) {
+                        const int q = a * CA + c;
+                        const uint64_t e = off + (uint64_t)q * P + rho;
+                        if ((e + 1) * elem_bits(elem) > values_cap * 8) return OR_CAPACITY;
+                        const int r = tm * TM + perm_row(perm, t, TM, a * LM + i);
+                        put_value(values, elem, e, W, ldw, r, tk * TK + c * LK + j);
+                    }
+                ++rho;
+            }
+            const uint64_t len = (uint64_t)Q * P, padded = (len + E - 1) / E * E;
+            for (uint64_t e = off + len; e < off + padded; ++e) {
+                if ((e + 1) * elem_bits(elem) > values_cap * 8) return OR_CAPACITY;
+                if (elem == OR_F16) { values[2 * e] = 0; values[2 * e + 1] = 0; }
+                else if (e & 1) values[e >> 1] &= 0x0F;
+                else values[e >> 1] &= 0xF0;
+            }
+            off += padded;
+            if (off >= ((uint64_t)1 << 32)) return OR_TOO_LARGE;
+            tile_off[t + 1] = (uint32_t)off;
+        }
+    }
+    *values_used = off * elem_bits(elem) / 8;
+    return OR_OK;
+}
+
+/* Decode (exact inverse of or_encode_ie): back to the original row order. */
+int or_decode_ie(const uint64_t* bitmap, const uint32_t* tile_off, const uint8_t* values, uint64_t values_bytes,
+                 int M, int K, int TM, int TK, int RA, int CA, int elem, const uint8_t* perm, void* W,
+                 int64_t ldw) {
+    int rc = check_ie(M, K, TM, TK, RA, CA, elem);
+    if (rc) return rc;
+    const int nTM = M / TM, nTK = K / TK, Q = RA * CA, LM = TM / RA, LK = TK / CA;
+    const int64_t lpos = (int64_t)LM * LK, words_per_tile = lpos / 64;
+    for (int tm = 0; tm < nTM; ++tm) {
+        for (int tk = 0; tk < nTK; ++tk) {
+            const int64_t t = (int64_t)tm * nTK + tk;
+            const uint64_t* words = bitmap + t * words_per_tile;
+            uint64_t P = 0;
+            for (int64_t w = 0; w < words_per_tile; ++w) P += (uint64_t)__builtin_popcountll(words[w]);
+            const uint64_t o0 = tile_off[t], o1 = tile_off[t + 1];
+            if (o1 < o0 || (uint64_t)Q * P > o1 - o0 || o1 * elem_bits(elem) > values_bytes * 8) return OR_CORRUPT;
+            uint64_t rho = 0;
+            for (int64_t p = 0; p < lpos; ++p) {
+                const int i = (int)(p / LK), j = (int)(p % LK);
+                const int set = (words[p / 64] >> (p % 64)) & 1u;
+                for (int a = 0; a < RA; ++a)
+                    for (int c = 0; c < CA; ++c) {
+                        const int r = tm * TM + perm_row(perm, t, TM, a * LM + i);
+                        const int64_t idx = (int64_t)r * ldw + tk * TK + c * LK + j;
+                        const uint64_t e = o0 + (uint64_t)(a * CA + c) * P + rho;
+                        if (elem == OR_F16) ((uint16_t*)W)[idx] = set ? get_f16(values, e) : 0;
+                        else ((int8_t*)W)[idx] = set ? get_i4(values, e) : 0;
+                    }
+                rho += (uint64_t)set;
+            }
+        }
+    }
+    return OR_OK;
+}
+
+/* Bitmap-aware row reordering of one local tile ([UnionSparse] V-B, Eq. 3-5,
+ * Algorithm 1).  mask: HL x KL bytes (nonzero = nonzero weight).  Rows are
+ * partitioned into groups of RA; a group r = (r_0 .. r_{RA-1}) activates, at
+ * grouped column j < KL/CA, phi(r;j) = OR_a OR_c mask[r_a][j + c*KL/CA], and
+ * costs c(r) = sum_j phi(r;j).  F(S) = min over groups r in S holding the
+ * smallest row of S of c(r) + F(S \ r), F(empty) = 0, memoised over row
+ * subsets.  The optimal groups are canonicalised (rows ascending inside a
+ * group, groups in lexicographic order) and the permutation is built
+ * partition-wise: perm[p*(HL/RA) + g] = r_{g,p}.  HL <= 20.  Returns the
+ * minimum cost in *cost. */
+static int group_cost(const uint8_t* mask, int KL, int RA, int CA, const int* rows) {
+    const int LK = KL / CA;
+    int cost = 0;
+    for (int j = 0; j < LK; ++j) {
+        int any = 0;
+        for (int a = 0; a < RA; ++a)
+            for (int c = 0; c < CA; ++c) any |= mask[rows[a] * KL + c * LK + j] != 0;
+        cost += any;
+    }
+    return cost;
+}
+
+typedef struct {
+    const uint8_t* mask;
+    int HL, KL, RA, CA;
+    int32_t* F;                    /* memo, -1 = unknown */
+    uint32_t* choice;              /* best group (as a row set) of each state */
+} reorder_ctx;
+
+static int32_t dp_solve(reorder_ctx* x, uint32_t S) {
+    if (S == 0) return 0;
+    if (x->F[S] >= 0) return x->F[S];
+    int pivot = 0;
+    while (!((S >> pivot) & 1u)) ++pivot;
+    /* the other RA-1 rows of the group: every (RA-1)-subset of S without the pivot */
+    int others[32], no = 0;
+    for (int r = pivot + 1; r < x->HL; ++r)
+        if ((S >> r) & 1u) others[no++] = r;
+    int32_t best = INT32_MAX;
+    uint32_t best_g = 0;
+    int idx[4] = {0, 1, 2, 3};
+    const int need = x->RA - 1;
+    if (need > no) return INT32_MAX;
+    for (;;) {
+        int rows[4];
+        uint32_t g = 1u << pivot;
+        rows[0] = pivot;
+        for (int k = 0; k < need; ++k) {
+            rows[k + 1] = others[idx[k]];
+            g |= 1u << others[idx[k]];
+        }
+        const int32_t rest = dp_solve(x, S & ~g);
+        if (rest != INT32_MAX) {
+            const int32_t v = group_cost(x->mask, x->KL, x->RA, x->CA, rows) + rest;
+            if (v < best) { best = v; best_g = g; }
+        }
+        /* next combination of `need` indices out of `no` */
+        int k = need - 1;
+        while (k >= 0 && idx[k] == no - need + k) --k;
+        if (k < 0) break;
+        ++idx[k];
+        for (int m = k + 1; m < need; ++m) idx[m] = idx[m - 1] + 1;
+    }
+    x->F[S] = best;
+    x->choice[S] = best_g;
+    return best;
+}
+
+int or_reorder_rows(const uint8_t* mask, int HL, int KL, int RA, int CA, uint8_t* perm, int* cost) {
+    if (!mask || !perm || HL <= 0 || HL > 20 || KL <= 0 || RA <= 0 || RA > 4 || CA <= 0) return OR_BAD_ARG;
+    if (HL % RA || KL % CA) return OR_BAD_ARG;
+    reorder_ctx x;
+    x.mask = mask; x.HL = HL; x.KL = KL; x.RA = RA; x.CA = CA;
+    const size_t ns = (size_t)1 << HL;
+    x.F = (int32_t*)malloc(ns * sizeof(int32_t));
+    x.choice = (uint32_t*)malloc(ns * sizeof(uint32_t));
+    if (!x.F || !x.choice) { free(x.F); free(x.choice); return OR_TOO_LARGE; }
+    for (size_t i = 0; i < ns; ++i) x.F[i] = -1;
+    const uint32_t all = (uint32_t)(ns - 1);
+    const int32_t best = dp_solve(&x, all);
+    /* recover the groups, rows ascending inside each (the pivot comes first and
+     * the others were enumerated in increasing order) */
+    const int G = HL / RA;
+    int groups[20][4];
+    uint32_t S = all;
+    for (int g = 0; g < G; ++g) {
+        const uint32_t gs = x.choice[S];
+        int k = 0;
+        for (int r = 0; r < HL; ++r)
+            if ((gs >> r) & 1u) groups[g][k++] = r;
+        S &= ~gs;
+    }
+    /* groups in lexicographic order (insertion sort) */
+    for (int a = 1; a < G; ++a)
+        for (int b = a; b > 0; --b) {
+            int less = 0;
+            for (int k = 0; k < RA; ++k)
+                if (groups[b][k] != groups[b - 1][k]) { less = groups[b][k] < groups[b - 1][k]; break; }
+            if (!less) break;
+            for (int k = 0; k < RA; ++k) { int t = groups[b][k]; groups[b][k] = groups[b - 1][k]; groups[b - 1][k] = t; }
+        }
+    for (int p = 0; p < RA; ++p)
+        for (int g = 0; g < G; ++g) perm[p * G + g] = (uint8_t)groups[g][p];
+    if (cost) *cost = best;
+    free(x.F);
+    free(x.choice);
     return OR_OK;
 }
 

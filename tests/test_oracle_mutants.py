@@ -37,6 +37,10 @@ MUTANTS = {
     "colinfo_offset_inclusive": ("            colinfo[t * TK + j] = (offset << 16) | nnz;\n            offset += nnz;",
                                  "            offset += nnz;\n            colinfo[t * TK + j] = (offset << 16) | nnz;"),
     "colinfo_fields_swapped": ("colinfo[t * TK + j] = (offset << 16) | nnz;", "colinfo[t * TK + j] = (nnz << 16) | offset;"),
+    "ie_stream_offset_dropped": ("const uint64_t e = off + (uint64_t)q * P + rho;", "const uint64_t e = off + rho;"),
+    "ie_areas_column_major": ("const int q = a * CA + c;", "const int q = c * RA + a;"),
+    "reorder_cost_ignores_union": ("        cost += any;", "        cost += 1;"),
+    "reorder_perm_groupwise": ("perm[p * G + g] = (uint8_t)groups[g][p];", "perm[g * RA + p] = (uint8_t)groups[g][p];"),
     "tile_numbering_colmajor": ("            const int64_t t = (int64_t)tm * nTK + tk;\n            uint64_t* words = bitmap",
                                 "            const int64_t t = (int64_t)tk * nTM + tm;\n            uint64_t* words = bitmap"),
 }

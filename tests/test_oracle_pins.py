@@ -458,3 +458,130 @@ def test_batched_spmspv_pins(orc):
     # the pruned product equals the dense product of the pruned activations
     Xp = np.where(np.abs(X.astype(np.float32)) > 0.25, X, np.float16(0))
     assert np.allclose(ex1, Xp.astype(np.float64) @ W.astype(np.float64).T, rtol=0, atol=1e-9)
+
+
+# ------------------------------------------------- IE-BME with Q = RA*CA areas --
+def test_fig7_areas_union_mask_and_offset(orc):
+    """UnionSparse Fig. 7 with its four areas: the printed logical rows are the
+    union of the areas' masks, P_t = 40 active positions, and the LT's payload
+    of Q * P_t = 160 int4 values puts the next offset at 160."""
+    g = json.load(open(os.path.join(GOLD, "fig7_union_bitmap.json")))
+    rows = [int(w, 16) for w in g["row_words"]]
+    LM, LK, RA, CA = 4, g["row_width"], 2, 2
+    W = np.zeros((LM * RA, LK * CA), np.int8)
+    for i, word in enumerate(rows):
+        for j in range(LK):
+            if (word >> j) & 1:
+                q = (i + j) % 4                              # the nonzero sits in any one area
+                a, c = divmod(q, CA)
+                W[a * LM + i, c * LK + j] = 1 + (i + 3 * j) % 7
+    bm, off, vals = orc.encode_ie(W, LM * RA, LK * CA, RA, CA, I4)
+    assert bm.size == 1
+    assert int(bm[0]) == rows[0] | rows[1] << 16 | rows[2] << 32 | rows[3] << 48
+    assert int(_popcount64(bm).sum()) == g["P_t"] == 40
+    assert int(off[1]) == g["next_offset_with_Q"] == 160
+    assert np.array_equal(orc.decode_ie(bm, off, vals, *W.shape, LM * RA, LK * CA, RA, CA, I4), W)
+
+
+def test_fig7_aligned_values_include_zeros(orc):
+    """A set logical position emits one value per area even when some are zero
+    (the red-framed [1, 30, 59, 0] of Fig. 7): CV[o_t + q P_t + rho]."""
+    RA, CA, LM, LK = 2, 2, 4, 16
+    W = np.zeros((LM * RA, LK * CA), np.float16)
+    i, j = 2, 5                                              # one logical position ...
+    for q, v in enumerate([1.0, 30.0, 59.0, 0.0]):           # ... its four area values
+        a, c = divmod(q, CA)
+        W[a * LM + i, c * LK + j] = v
+    W[0, 0] = 7.0                                           # an earlier position: rho = 1
+    bm, off, vals = orc.encode_ie(W, LM * RA, LK * CA, RA, CA, F16)
+    P = int(_popcount64(bm).sum())
+    assert P == 2
+    v16 = vals.view(np.float16)
+    assert [float(v16[q * P + 1]) for q in range(4)] == [1.0, 30.0, 59.0, 0.0]
+    assert [float(v16[q * P + 0]) for q in range(4)] == [7.0, 0.0, 0.0, 0.0]
+
+
+@pytest.mark.parametrize("cfg", [(16, 64, 2, 2), (16, 64, 4, 1), (16, 64, 1, 4), (64, 64, 2, 1), (64, 128, 1, 2),
+                                 (8, 32, 2, 2)])
+@pytest.mark.parametrize("elem", [F16, I4])
+def test_ie_round_trip_with_row_permutations(orc, cfg, elem):
+    TM, TK, RA, CA = cfg
+    rng = np.random.default_rng(TM * 7 + TK + RA + 10 * CA + elem)
+    M, K = TM * 3, TK * 2
+    W = _rand_f16(rng, M, K, 0.35) if elem == F16 else _rand_i4(rng, M, K, 0.35)
+    nT = (M // TM) * (K // TK)
+    perm = np.concatenate([rng.permutation(TM) for _ in range(nT)]).astype(np.uint8)
+    for pm in (None, perm):
+        bm, off, vals = orc.encode_ie(W, TM, TK, RA, CA, elem, pm)
+        D = orc.decode_ie(bm, off, vals, M, K, TM, TK, RA, CA, elem, pm)
+        assert np.array_equal(D.view(np.uint8), W.view(np.uint8))
+        # the run of each tile is Q * P_t padded to 16 bytes
+        Q, E = RA * CA, (8 if elem == F16 else 32)
+        wpt = TM * TK // (64 * Q)
+        P = _popcount64(bm).reshape(nT, wpt).sum(axis=1)
+        assert np.array_equal(np.diff(off.astype(np.int64)), (Q * P + E - 1) // E * E)
+
+
+def test_ie_single_area_is_the_plain_format(orc):
+    """Q = 1 with the identity permutation is the plain row-scan encoding."""
+    rng = np.random.default_rng(1)
+    W = _rand_i4(rng, 128, 128, 0.5)
+    a = orc.encode_ie(W, 64, 64, 1, 1, I4)
+    b = orc.encode(W, 64, 64, I4, ROW)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def _brute_min_cost(mask, RA, CA):
+    """Every partition of the rows into groups of RA, by plain recursion."""
+    HL, KL = mask.shape
+    LK = KL // CA
+
+    def cost(g):
+        return sum(any(mask[r, c * LK + j] for r in g for c in range(CA)) for j in range(LK))
+
+    def rec(rest):
+        if not rest:
+            return 0
+        first, others = rest[0], rest[1:]
+        best = None
+        from itertools import combinations
+        for mates in combinations(others, RA - 1):
+            g = (first,) + mates
+            v = cost(g) + rec([r for r in others if r not in mates])
+            best = v if best is None or v < best else best
+        return best
+
+    return rec(list(range(HL)))
+
+
+@pytest.mark.parametrize("shape", [(4, 8, 2, 1), (6, 8, 2, 2), (8, 16, 2, 2), (8, 8, 4, 1), (8, 16, 4, 2),
+                                   (8, 12, 2, 3)])
+def test_reorder_dp_matches_brute_force(orc, shape):
+    HL, KL, RA, CA = shape
+    rng = np.random.default_rng(HL * 31 + KL + RA + CA)
+    for trial in range(6):
+        mask = rng.random((HL, KL)) < rng.uniform(0.1, 0.6)
+        perm, cost = orc.reorder_rows(mask, RA, CA)
+        assert cost == _brute_min_cost(mask, RA, CA)
+        assert sorted(perm.tolist()) == list(range(HL))
+        # the permutation realises that cost: union bits of the reordered tile
+        G = HL // RA
+        groups = [[int(perm[p * G + g]) for p in range(RA)] for g in range(G)]
+        LK = KL // CA
+        realised = sum(any(mask[r, c * LK + j] for r in grp for c in range(CA)) for grp in groups for j in range(LK))
+        assert realised == cost
+        # canonical: ascending inside a group, groups in lexicographic order
+        assert all(grp == sorted(grp) for grp in groups) and groups == sorted(groups)
+
+
+def test_reordering_never_grows_the_union_mask(orc):
+    rng = np.random.default_rng(6)
+    W = _rand_i4(rng, 64, 128, 0.4)
+    base = orc.encode_ie(W, 16, 64, 2, 2, I4)
+    perm = orc.reorder_matrix(W, 16, 64, 2, 2)
+    re = orc.encode_ie(W, 16, 64, 2, 2, I4, perm)
+    nT = 4 * 2
+    pb = _popcount64(base[0]).reshape(nT, -1).sum(axis=1)
+    pr = _popcount64(re[0]).reshape(nT, -1).sum(axis=1)
+    assert np.all(pr <= pb) and pr.sum() < pb.sum()
