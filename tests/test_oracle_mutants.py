@@ -14,8 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "us_oracle.c")
 
 MUTANTS = {
-    "bit_order_msb_first": ("words[p / 64] |= (uint64_t)1 << (p % 64);",
-                            "words[p / 64] |= (uint64_t)1 << (63 - p % 64);"),
+    "bit_order_msb_first": ("if (!dense_nonzero(W, ldw, elem, r, c)) continue;\n                words[p / 64] |= (uint64_t)1 << (p % 64);",
+                            "if (!dense_nonzero(W, ldw, elem, r, c)) continue;\n                words[p / 64] |= (uint64_t)1 << (63 - p % 64);"),
     "row_scan_transposed": ("if (order == OR_ROW) { *i = (int)(p / TK); *j = (int)(p % TK); }",
                             "if (order == OR_ROW) { *i = (int)(p % TM); *j = (int)(p / TM); }"),
     "col_scan_transposed": ("else                 { *j = (int)(p / TM); *i = (int)(p % TM); }",
