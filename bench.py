@@ -540,6 +540,33 @@ def measure_extras(us, torch, wl, dev, stream):
         fl = 2 * 4096 * 4096 * N
         pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_col_tiles_4096_s60"] = pfc
+    # IE-BME with areas: W4A4 4096^2 at 50 %, 16 x 64 local tiles, 2 x 2 areas, with
+    # and without the offline row reordering; encoded bytes and the SpMM time
+    d = wl.w4a4(4096, 4096, 16, 0.5, seed=0)
+    Wq = torch.from_numpy(d["Wq"]).to(dev)
+    ie = {}
+    E1 = us.us_encode(Wq, 64, 64, us.US_I4, us.US_ORDER_ROW)
+    ie["plain_64x64"] = {"bitmap_bytes": E1.bitmap.numel() * 8, "value_bytes": E1.values_bytes,
+                         "total_bytes": E1.nbytes()}
+    import time as _t
+    t_re = _t.time()
+    perm = us.us_reorder_rows(d["Wq"], 16, 64, 2, 2, us.US_I4)
+    reorder_s = _t.time() - t_re
+    permt = torch.from_numpy(perm).to(dev)
+    for name, pm in (("areas_2x2_16x64", None), ("areas_2x2_16x64_reordered", permt)):
+        Ei = us.us_encode_ie(Wq, 16, 64, 2, 2, us.US_I4, pm)
+        row = {"bitmap_bytes": Ei.E.bitmap.numel() * 8, "value_bytes": Ei.E.values_bytes,
+               "perm_bytes": 0 if pm is None else pm.numel(),
+               "total_bytes": Ei.E.nbytes() + (0 if pm is None else pm.numel())}
+        for N in (1, 8, 16):
+            X = torch.from_numpy(wl.pack_int4(d["Xq"][:N])).to(dev)
+            Ya = torch.empty(N, 4096, dtype=torch.int32, device=dev)
+            wsi = us.workspace_ie(Ei, N)
+            ms = time_graph(torch, stream, lambda: us.us_spmm_w4a4_ie(Ei, X, None, None, N, Ya, None, wsi, 0, stream), 20)
+            row[f"N{N}_us"] = round(ms * 1e3, 2)
+        ie[name] = row
+    ie["reorder_host_s"] = round(reorder_s, 2)
+    out["w4a4_ie_areas_4096"] = ie
     # per-token activation quantisation, fp16 -> int4 + scale (reads 2NK, writes NK/2 + 2N bytes)
     qz = {}
     for N in (16, 2048):

@@ -31,6 +31,7 @@ US_BITMAP_STATIC = 1
 
 EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmm_f16_noalloc", "us_spmspv_f16",
             "us_colinfo", "us_spmspv_f16_ci", "us_quantize_x",
+            "us_encode_ie_sizes", "us_encode_ie", "us_reorder_rows", "us_spmm_w4a4_ie", "us_workspace_bytes_ie",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
             "us_status_string", "us_version")
 
@@ -50,6 +51,10 @@ class us_bitmap(ctypes.Structure):
                 ("elem", ctypes.c_int32), ("order", ctypes.c_int32),
                 ("bitmap", ctypes.c_void_p), ("tile_off", ctypes.c_void_p), ("values", ctypes.c_void_p),
                 ("values_bytes", ctypes.c_uint64), ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class us_bitmap_ie(ctypes.Structure):
+    _fields_ = [("W", us_bitmap), ("RA", ctypes.c_int32), ("CA", ctypes.c_int32), ("perm", ctypes.c_void_p)]
 
 
 _lock = threading.Lock()
@@ -76,6 +81,12 @@ def load(path: str = LIB_PATH):
         lib.us_spmm_f16_noalloc.argtypes = [pbm, P, i32, P, i32, P]
         lib.us_spmspv_f16.argtypes = [pbm, P, ctypes.c_float, P, P, sz, P]
         lib.us_colinfo.argtypes = [pbm, P, P]
+        pie = ctypes.POINTER(us_bitmap_ie)
+        lib.us_encode_ie_sizes.argtypes = [i32, i32, i32, i32, i32, i32, i32, psz, psz, psz, psz]
+        lib.us_encode_ie.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, i32, P, P, P, P, sz, P, sz, P]
+        lib.us_reorder_rows.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, i32, P, i32]
+        lib.us_spmm_w4a4_ie.argtypes = [pie, P, P, P, i32, P, P, P, sz, i32, P]
+        lib.us_workspace_bytes_ie.argtypes = [pie, i32, i32, psz]
         lib.us_spmspv_f16_ci.argtypes = [pbm, P, P, i32, ctypes.c_float, P, P, sz, P]
         lib.us_quantize_x.argtypes = [P, i32, i32, P, P, P]
         lib.us_workspace_bytes.argtypes = [i32, pbm, i32, i32, psz]
@@ -173,6 +184,80 @@ def us_encode_into(W: torch.Tensor, E: Encoded, ws: torch.Tensor, stream=None):
     _check("us_encode", load().us_encode(ctypes.c_void_p(W.data_ptr()), W.stride(0), M, K, E.TM, E.TK, E.elem,
                                          E.order, _dptr(E.bitmap), _dptr(E.tile_off), _dptr(E.values),
                                          E.values.numel(), _dptr(ws), ws.numel(), _stream(stream)))
+
+
+@dataclass
+class EncodedIE:
+    """IE-BME with RA x CA areas: an Encoded (ROW scan, union-mask bitmap) plus
+    the area counts and the per-tile row permutation (device uint8, or None)."""
+    E: Encoded
+    RA: int
+    CA: int
+    perm: torch.Tensor | None = None
+
+    def desc(self) -> us_bitmap_ie:
+        return us_bitmap_ie(self.E.desc(), self.RA, self.CA, self.perm.data_ptr() if self.perm is not None else None)
+
+
+def encode_ie_sizes(M, K, TM, TK, RA, CA, elem):
+    b, o, v, w = (ctypes.c_size_t() for _ in range(4))
+    _check("us_encode_ie_sizes", load().us_encode_ie_sizes(M, K, TM, TK, RA, CA, elem, ctypes.byref(b),
+                                                           ctypes.byref(o), ctypes.byref(v), ctypes.byref(w)))
+    return b.value, o.value, v.value, w.value
+
+
+def us_encode_ie(W: torch.Tensor, TM: int, TK: int, RA: int, CA: int, elem: int, perm: torch.Tensor | None = None,
+                 stream=None) -> EncodedIE:
+    """Encode a dense CUDA matrix as IE-BME with RA x CA areas; perm: device
+    uint8 tensor of TM bytes per tile (tile-major) or None."""
+    lib = load()
+    M, K = W.shape
+    dev = W.device
+    assert W.is_cuda and W.stride(1) == 1, "W must be a CUDA matrix with unit column stride"
+    bb, ob, vcap, wsb = encode_ie_sizes(M, K, TM, TK, RA, CA, elem)
+    bitmap = torch.empty(max(bb // 8, 2), dtype=torch.int64, device=dev)
+    tile_off = torch.empty(ob // 4, dtype=torch.int32, device=dev)
+    values = torch.zeros(max(vcap, 16), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=dev)
+    _check("us_encode_ie", lib.us_encode_ie(ctypes.c_void_p(W.data_ptr()), W.stride(0), M, K, TM, TK, RA, CA, elem,
+                                            _dptr(perm), _dptr(bitmap), _dptr(tile_off), _dptr(values),
+                                            values.numel(), _dptr(ws), ws.numel(), _stream(stream)))
+    used_elems = int(tile_off[-1].item()) & 0xFFFFFFFF
+    used = used_elems * (2 if elem == US_F16 else 1) // (1 if elem == US_F16 else 2)
+    values = values[: max(used, 16)].clone()
+    return EncodedIE(Encoded(M, K, TM, TK, elem, US_ORDER_ROW, bitmap, tile_off, values, used), RA, CA, perm)
+
+
+def us_reorder_rows(W, TM: int, TK: int, RA: int, CA: int, elem: int, nthreads: int = 0):
+    """Bitmap-aware row reordering on the host (offline): numpy W (fp16 or int8
+    codes) -> numpy uint8 permutation, TM bytes per tile, tile-major."""
+    import numpy as np
+    Wh = np.ascontiguousarray(W)
+    M, K = Wh.shape
+    perm = np.zeros((M // TM) * (K // TK) * TM, np.uint8)
+    n = nthreads or max(1, min(32, os.cpu_count() or 1))
+    _check("us_reorder_rows", load().us_reorder_rows(Wh.ctypes.data, K, M, K, TM, TK, RA, CA, elem,
+                                                     perm.ctypes.data, n))
+    return perm
+
+
+def us_workspace_bytes_ie(E: EncodedIE, N: int, split_k: int = 0) -> int:
+    n = ctypes.c_size_t()
+    d = E.desc()
+    _check("us_workspace_bytes_ie", load().us_workspace_bytes_ie(ctypes.byref(d), N, split_k, ctypes.byref(n)))
+    return n.value
+
+
+def workspace_ie(E: EncodedIE, N: int, split_k: int = 0) -> torch.Tensor:
+    return torch.zeros(max(us_workspace_bytes_ie(E, N, split_k), 16), dtype=torch.uint8, device=E.E.bitmap.device)
+
+
+def us_spmm_w4a4_ie(E: EncodedIE, Xq: torch.Tensor, s_w, s_x, N: int, Yacc: torch.Tensor, Y, ws: torch.Tensor,
+                    split_k: int = 0, stream=None):
+    d = E.desc()
+    _check("us_spmm_w4a4_ie", load().us_spmm_w4a4_ie(ctypes.byref(d), _dptr(Xq), _dptr(s_w), _dptr(s_x), N,
+                                                     _dptr(Yacc), _dptr(Y), _dptr(ws), ws.numel(), split_k,
+                                                     _stream(stream)))
 
 
 def from_host(bitmap, tile_off, values, M, K, TM, TK, elem, order, device="cuda") -> Encoded:

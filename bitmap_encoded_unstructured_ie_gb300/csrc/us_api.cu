@@ -90,6 +90,8 @@ void fill_common(UsKParams& p, const us_bitmap* W, int N) {
     p.sk_grid = p.sk_per = p.sk_ring = p.sk_xcols = p.sk_nb = p.sk_slots = p.sk_pre = 0;
     p.flags = W->flags;
     p.order = W->order;
+    p.ie_ra = p.ie_ca = 1;
+    p.perm = nullptr;
     p.status = status_ptr();
 }
 
@@ -364,6 +366,109 @@ us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16
     p.counters = static_cast<unsigned*>(ws);
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, 1);
     return us::launch_spmspv(p, static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------- IE-BME with areas --
+namespace {
+
+us_status check_ie_shape(int M, int K, int TM, int TK, int RA, int CA, int elem) {
+    if (M <= 0 || K <= 0) return US_ERR_INVALID_ARG;
+    if (!(TM == 16 || TM == 64 || TM == 128 || TM == 256) || !(TK == 16 || TK == 32 || TK == 64 || TK == 128))
+        return US_ERR_INVALID_ARG;
+    if (!(RA == 1 || RA == 2 || RA == 4) || !(CA == 1 || CA == 2 || CA == 4) || RA * CA > 4) return US_ERR_INVALID_ARG;
+    if (((TM / RA) * (TK / CA)) % 128) return US_ERR_INVALID_ARG;
+    if (M % TM || K % TK) return US_ERR_INVALID_ARG;
+    if (elem != US_F16 && elem != US_I4) return US_ERR_INVALID_ARG;
+    if ((uint64_t)M * (uint64_t)K >= (1ull << 32)) return US_ERR_TOO_LARGE;
+    return US_OK;
+}
+
+us_status check_bitmap_ie(const us_bitmap_ie* B, int elem) {
+    if (!B) return US_ERR_INVALID_ARG;
+    const us_bitmap* W = &B->W;
+    us_status s = check_ie_shape(W->M, W->K, W->TM, W->TK, B->RA, B->CA, W->elem);
+    if (s != US_OK) return s;
+    if (W->elem != elem || W->order != US_ORDER_ROW) return US_ERR_INVALID_ARG;
+    if (!W->bitmap || !W->tile_off || (!W->values && W->values_bytes)) return US_ERR_INVALID_ARG;
+    if (!aligned16(W->bitmap) || !aligned16(W->tile_off) || !aligned16(W->values) || !aligned16(B->perm))
+        return US_ERR_INVALID_ARG;
+    if ((W->flags & ~US_BITMAP_STATIC) || W->reserved) return US_ERR_INVALID_ARG;
+    return US_OK;
+}
+
+Plan plan_ie(const us_bitmap_ie* B, int N, int split_k) {
+    Plan pl{};
+    const us_bitmap* W = &B->W;
+    const int nTM = W->M / W->TM, nTK = W->K / W->TK;
+    pl.tok_block = us::spmm_generic_tok_block(N);
+    const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
+    // small local tiles make thin bands: slice K deeper so that each CTA walks
+    // fewer tiles (its per-tile work is short and barrier bound)
+    pl.split = split_k > 0 ? split_k : auto_split(nTM, nTK, ntb, 8 * us::num_sms());
+    if (pl.split > nTK) pl.split = nTK;
+    pl.ws = us::spmm_generic_ws(W->M, W->TM, N, pl.split, pl.tok_block);
+    return pl;
+}
+
+}  // namespace
+
+us_status us_encode_ie_sizes(int M, int K, int TM, int TK, int RA, int CA, us_elem elem, size_t* bitmap_bytes,
+                             size_t* tile_off_bytes, size_t* values_cap_bytes, size_t* ws_bytes) {
+    us_status s = check_ie_shape(M, K, TM, TK, RA, CA, elem);
+    if (s != US_OK) return s;
+    const uint64_t nT = (uint64_t)(M / TM) * (K / TK);
+    if (bitmap_bytes) *bitmap_bytes = (size_t)M * K / (8 * RA * CA);
+    if (tile_off_bytes) *tile_off_bytes = (size_t)(nT + 1) * 4;
+    // Q * P_t <= TM * TK per tile, and TM * TK is a multiple of the padding quantum
+    if (values_cap_bytes) *values_cap_bytes = (size_t)M * K * (elem == US_F16 ? 2 : 1) / (elem == US_F16 ? 1 : 2);
+    if (ws_bytes) *ws_bytes = ((size_t)nT * 4 + 255) & ~(size_t)255;
+    return US_OK;
+}
+
+us_status us_encode_ie(const void* W, int64_t ldw, int M, int K, int TM, int TK, int RA, int CA, us_elem elem,
+                       const uint8_t* perm, uint64_t* bitmap, uint32_t* tile_off, void* values, size_t values_cap,
+                       void* ws, size_t ws_bytes, void* stream) {
+    us_status s = check_ie_shape(M, K, TM, TK, RA, CA, elem);
+    if (s != US_OK) return s;
+    if (!W || !bitmap || !tile_off || !values || !ws || ldw < K) return US_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(W) & (elem == US_F16 ? 1u : 0u)) != 0) return US_ERR_INVALID_ARG;
+    if (!aligned16(bitmap) || !aligned16(tile_off) || !aligned16(values) || !aligned16(ws)) return US_ERR_INVALID_ARG;
+    size_t need = 0;
+    us_encode_ie_sizes(M, K, TM, TK, RA, CA, elem, nullptr, nullptr, nullptr, &need);
+    if (ws_bytes < need) return US_ERR_WORKSPACE;
+    return us::launch_encode_ie(W, ldw, M, K, TM, TK, RA, CA, elem, perm, bitmap, tile_off, values, values_cap,
+                                static_cast<uint32_t*>(ws), status_ptr(), static_cast<cudaStream_t>(stream));
+}
+
+us_status us_workspace_bytes_ie(const us_bitmap_ie* B, int N, int split_k, size_t* bytes) {
+    if (!B || !bytes) return US_ERR_INVALID_ARG;
+    us_status s = check_ie_shape(B->W.M, B->W.K, B->W.TM, B->W.TK, B->RA, B->CA, B->W.elem);
+    if (s != US_OK) return s;
+    if (N < 1 || N > 2048 || split_k < 0) return US_ERR_INVALID_ARG;
+    *bytes = plan_ie(B, N, split_k).ws;
+    return US_OK;
+}
+
+us_status us_spmm_w4a4_ie(const us_bitmap_ie* B, const uint8_t* Xq, const uint16_t* s_w, const uint16_t* s_x, int N,
+                          int32_t* Yacc, uint16_t* Y, void* ws, size_t ws_bytes, int split_k, void* stream) {
+    us_status s = check_bitmap_ie(B, US_I4);
+    if (s != US_OK) return s;
+    const us_bitmap* W = &B->W;
+    if (N < 1 || N > 2048 || W->K % 32) return US_ERR_INVALID_ARG;
+    if (!Xq || !Yacc || !aligned16(Xq) || !aligned16(Yacc)) return US_ERR_INVALID_ARG;
+    if (Y && (!s_w || !s_x || !aligned16(Y))) return US_ERR_INVALID_ARG;
+    if (split_k < 0 || split_k > W->K / W->TK) return US_ERR_INVALID_ARG;
+    const Plan pl = plan_ie(B, N, split_k);
+    if (!ws || ws_bytes < pl.ws || !aligned16(ws)) return US_ERR_WORKSPACE;
+    UsKParams p;
+    fill_common(p, W, N);
+    p.X = Xq; p.s_w = s_w; p.s_x = s_x; p.Yacc = Yacc; p.Y = Y;
+    p.split = pl.split; p.tok_block = pl.tok_block;
+    p.ie_ra = B->RA; p.ie_ca = B->CA; p.perm = B->perm;
+    const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
+    p.counters = static_cast<unsigned*>(ws);
+    p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
+    return us::launch_spmm_generic(p, US_I4, static_cast<cudaStream_t>(stream));
 }
 
 us_status us_colinfo(const us_bitmap* W, uint32_t* colinfo, void* stream) {

@@ -268,6 +268,11 @@ struct UsKParams {
     float tau;
     uint32_t flags;     // US_BITMAP_* flags of the weight descriptor
     int order;          // US_ORDER_ROW or US_ORDER_COL scan inside a tile
+    // IE-BME with areas (generic kernel only): RA row x CA column partitions of
+    // each tile, one union mask, Q = RA*CA value streams; perm: per tile, the
+    // original row of each row of the reordered tile (nullptr = identity)
+    int ie_ra, ie_ca;
+    const uint8_t* perm;
     void* ws;           // split-K partials (after the counters)
     unsigned* counters; // split-K arrival counters, one per (band, token block)
     unsigned* status;

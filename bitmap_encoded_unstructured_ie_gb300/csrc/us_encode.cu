@@ -213,6 +213,183 @@ enc_pack_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK
     (void)EB;
 }
 
+// ---------------------------------------------------- IE-BME with areas --
+// UnionSparse section V-A with Q = RA*CA areas (Fig. 7): a TM x TK tile,
+// after its optional row permutation, is cut into RA x CA areas of LM x LK;
+// logical position (i, j) of the union mask is set iff some area holds a
+// nonzero there; each set position emits one value per area, zeros included,
+// at CV[o_t + q P_t + rho] with q = a*CA + c.
+struct IeShape {
+    int TM, TK, RA, CA, nTK;
+};
+
+// original row (within the tile) of row r of the reordered tile
+__device__ __forceinline__ int ie_row(const uint8_t* perm, int64_t t, int TM, int r) {
+    if (!perm) return r;
+    const int v = perm[t * TM + r];
+    return v < TM ? v : r;                  // out-of-range entries were reported by the count kernel
+}
+
+template <int ELEM>
+__global__ void __launch_bounds__(kEncThreads)
+enc_ie_count_kernel(const void* __restrict__ W, int64_t ldw, IeShape sh, const uint8_t* __restrict__ perm,
+                    uint64_t* __restrict__ bitmap, uint32_t* __restrict__ counts, unsigned* status) {
+    const int t = blockIdx.x;
+    const int tm = t / sh.nTK, tk = t - tm * sh.nTK;
+    const int LM = sh.TM / sh.RA, LK = sh.TK / sh.CA;
+    const int nw = LM * LK / 64;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ int warp_sum[kEncThreads / 32];
+    __shared__ uint32_t seen[8];            // rows named by the permutation (TM <= 256)
+    if (threadIdx.x < 8) seen[threadIdx.x] = 0;
+    __syncthreads();
+    if (perm && threadIdx.x < sh.TM) {
+        const int v = perm[(int64_t)t * sh.TM + threadIdx.x];
+        if (v >= sh.TM) us::set_status(status, US_ERR_INVALID_ARG);
+        else atomicOr(&seen[v >> 5], 1u << (v & 31));
+    }
+    __syncthreads();
+    if (perm && threadIdx.x == 0) {
+        int n = 0;
+        for (int i = 0; i < 8; ++i) n += __popc(seen[i]);
+        if (n != sh.TM) us::set_status(status, US_ERR_INVALID_ARG);   // a row named twice
+    }
+    const int64_t row0 = (int64_t)tm * sh.TM;
+    const int64_t col0 = (int64_t)tk * sh.TK;
+    int my = 0;
+    for (int w = warp; w < nw; w += kEncThreads / 32) {
+        uint32_t half[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int lp = w * 64 + h * 32 + lane;
+            const int i = lp / LK, j = lp - i * LK;
+            bool any = false;
+            for (int a = 0; a < sh.RA; ++a) {
+                const int64_t r = row0 + ie_row(perm, t, sh.TM, a * LM + i);
+                for (int c = 0; c < sh.CA; ++c) {
+                    const int64_t idx = r * ldw + col0 + c * LK + j;
+                    any |= is_nonzero<ELEM>(W, idx);
+                    if (ELEM == US_I4) {
+                        const int8_t v = reinterpret_cast<const int8_t*>(W)[idx];
+                        if (v < -8 || v > 7) us::set_status(status, US_ERR_INVALID_ARG);
+                    }
+                }
+            }
+            half[h] = __ballot_sync(0xffffffffu, any);
+        }
+        if (lane == 0) {
+            bitmap[(int64_t)t * nw + w] = (uint64_t)half[0] | ((uint64_t)half[1] << 32);
+            my += __popc(half[0]) + __popc(half[1]);
+        }
+    }
+    if (lane == 0) warp_sum[warp] = my;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int i = 0; i < kEncThreads / 32; ++i) s += warp_sum[i];
+        counts[t] = (uint32_t)(s * sh.RA * sh.CA);              // the run holds Q * P_t values
+    }
+}
+
+template <int ELEM>
+__global__ void __launch_bounds__(kEncThreads)
+enc_ie_pack_kernel(const void* __restrict__ W, int64_t ldw, IeShape sh, const uint8_t* __restrict__ perm,
+                   const uint64_t* __restrict__ bitmap, const uint32_t* __restrict__ tile_off,
+                   uint8_t* __restrict__ values, uint64_t values_cap, unsigned* status) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int t = blockIdx.x;
+    const int tm = t / sh.nTK, tk = t - tm * sh.nTK;
+    const int LM = sh.TM / sh.RA, LK = sh.TK / sh.CA, Q = sh.RA * sh.CA;
+    const int lpos = LM * LK, nw = lpos / 64;
+    uint32_t* wpre = reinterpret_cast<uint32_t*>(smem);
+    uint8_t* cbuf = smem + ((nw * 4 + 15) & ~15);                     // Q * P compacted elements
+    __shared__ uint32_t warp_tot[kEncThreads / 32];
+
+    const uint64_t o0 = tile_off[t], o1 = tile_off[t + 1];
+    const int bits = (ELEM == US_F16) ? 16 : 4;
+    if (o1 < o0 || o1 * bits > values_cap * 8) {
+        if (threadIdx.x == 0) us::set_status(status, US_ERR_WORKSPACE);
+        return;
+    }
+    const uint64_t* words = bitmap + (int64_t)t * nw;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t c0 = 0, c1 = 0;
+    const int w0 = 2 * threadIdx.x, w1 = w0 + 1;
+    if (w0 < nw) c0 = __popcll(words[w0]);
+    if (w1 < nw) c1 = __popcll(words[w1]);
+    uint32_t incl = c0 + c1;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int i = 0; i < warp; ++i) before += warp_tot[i];
+    const uint32_t excl = before + incl - (c0 + c1);
+    if (w0 < nw) wpre[w0] = excl;
+    if (w1 < nw) wpre[w1] = excl + c0;
+    uint32_t P = 0;
+    for (int i = 0; i < kEncThreads / 32; ++i) P += warp_tot[i];
+    __syncthreads();
+    const uint32_t L = P * (uint32_t)Q;                              // values in the run
+    if (L > o1 - o0) {
+        if (threadIdx.x == 0) us::set_status(status, US_ERR_CORRUPT);
+        return;
+    }
+    // each set logical position: one value per area, CV[o_t + q P + rho]
+    const int64_t row0 = (int64_t)tm * sh.TM, col0 = (int64_t)tk * sh.TK;
+    for (int lp = threadIdx.x; lp < lpos; lp += kEncThreads) {
+        const int w = lp >> 6, b = lp & 63;
+        const uint64_t word = words[w];
+        if (!((word >> b) & 1ull)) continue;
+        const uint32_t rank = wpre[w] + __popcll(word & ((1ull << b) - 1ull));
+        const int i = lp / LK, j = lp - i * LK;
+        for (int a = 0; a < sh.RA; ++a) {
+            const int64_t r = row0 + ie_row(perm, t, sh.TM, a * LM + i);
+            for (int c = 0; c < sh.CA; ++c) {
+                const int64_t idx = r * ldw + col0 + c * LK + j;
+                const uint32_t e = (uint32_t)(a * sh.CA + c) * P + rank;
+                if (ELEM == US_F16)
+                    reinterpret_cast<uint16_t*>(cbuf)[e] = reinterpret_cast<const uint16_t*>(W)[idx];
+                else
+                    cbuf[e] = (uint8_t)reinterpret_cast<const int8_t*>(W)[idx] & 0x0Fu;
+            }
+        }
+    }
+    __syncthreads();
+    // the run [o0, o1) with zero padding, 16 bytes per thread-step
+    const uint64_t run_bytes = (o1 - o0) * bits / 8;
+    uint8_t* dst = values + o0 * bits / 8;
+    for (uint64_t q = (uint64_t)threadIdx.x * 16; q < run_bytes; q += (uint64_t)kEncThreads * 16) {
+        uint32_t v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int bsub = 0; bsub < 4; ++bsub) {
+                const uint64_t byte = q + r * 4 + bsub;
+                uint32_t by = 0;
+                if (ELEM == US_F16) {
+                    const uint64_t e = byte >> 1;
+                    if (e < L) {
+                        const uint16_t h = reinterpret_cast<const uint16_t*>(cbuf)[e];
+                        by = (byte & 1) ? (h >> 8) : (h & 0xFF);
+                    }
+                } else {
+                    const uint64_t e0 = byte * 2, e1 = e0 + 1;
+                    if (e0 < L) by |= cbuf[e0];
+                    if (e1 < L) by |= (uint32_t)cbuf[e1] << 4;
+                }
+                word |= (by & 0xFFu) << (8 * bsub);
+            }
+            v[r] = word;
+        }
+        *reinterpret_cast<uint4*>(dst + q) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+}
+
 }  // namespace
 
 namespace us {
@@ -250,6 +427,35 @@ us_status launch_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK
             return US_ERR_CUDA;
         enc_pack_kernel<US_I4><<<(unsigned)nT, kEncThreads, smem, st>>>(
             W, ldw, TM, TK, nTK, order, bitmap, tile_off, (uint8_t*)values, values_cap, status);
+    }
+    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
+}
+
+us_status launch_encode_ie(const void* W, int64_t ldw, int M, int K, int TM, int TK, int RA, int CA, int elem,
+                           const uint8_t* perm, uint64_t* bitmap, uint32_t* tile_off, void* values,
+                           size_t values_cap, uint32_t* counts, unsigned* status, cudaStream_t st) {
+    IeShape sh{TM, TK, RA, CA, K / TK};
+    const int64_t nT = (int64_t)(M / TM) * (K / TK);
+    const size_t smem = encode_pack_smem(TM, TK, elem);             // Q * P <= TM * TK elements
+    if (elem == US_F16)
+        enc_ie_count_kernel<US_F16><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, sh, perm, bitmap, counts, status);
+    else
+        enc_ie_count_kernel<US_I4><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, sh, perm, bitmap, counts, status);
+    if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
+    enc_scan_kernel<<<1, 1024, 0, st>>>(counts, nT, elem == US_F16 ? 8 : 32, tile_off, status);
+    if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
+    if (elem == US_F16) {
+        if (cudaFuncSetAttribute(enc_ie_pack_kernel<US_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return US_ERR_CUDA;
+        enc_ie_pack_kernel<US_F16><<<(unsigned)nT, kEncThreads, smem, st>>>(W, ldw, sh, perm, bitmap, tile_off,
+                                                                            (uint8_t*)values, values_cap, status);
+    } else {
+        if (cudaFuncSetAttribute(enc_ie_pack_kernel<US_I4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem) != cudaSuccess)
+            return US_ERR_CUDA;
+        enc_ie_pack_kernel<US_I4><<<(unsigned)nT, kEncThreads, smem, st>>>(W, ldw, sh, perm, bitmap, tile_off,
+                                                                           (uint8_t*)values, values_cap, status);
     }
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }

@@ -48,6 +48,9 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
 
 // spMspV (us_spmspv.cu)
 us_status launch_spmspv(const UsKParams& p, cudaStream_t st);
+us_status launch_encode_ie(const void* W, int64_t ldw, int M, int K, int TM, int TK, int RA, int CA, int elem,
+                           const uint8_t* perm, uint64_t* bitmap, uint32_t* tile_off, void* values,
+                           size_t values_cap, uint32_t* counts, unsigned* status, cudaStream_t st);
 us_status launch_colinfo(const uint64_t* bitmap, int TM, int TK, int64_t nT, uint32_t* colinfo, cudaStream_t st);
 us_status launch_spmspv_ci(const UsKParams& p, const uint32_t* colinfo, cudaStream_t st);
 size_t spmspv_ws(int M, int TM, int split);

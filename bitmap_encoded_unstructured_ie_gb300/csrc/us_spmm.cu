@@ -62,7 +62,10 @@ spmm_generic_kernel(const UsKParams p) {
     using acc_t = typename std::conditional<ELEM == US_F16, float, int>::type;
 
     const int TK = p.TK;
-    const int nw = TM * TK / 64;
+    const int Q = p.ie_ra * p.ie_ca;                  // value streams per tile (1: plain format)
+    const int LM = TM / p.ie_ra, LK = TK / p.ie_ca;   // logical union-mask rows and columns
+    const bool ie = Q > 1 || p.perm != nullptr;
+    const int nw = TM * TK / (64 * Q);
     const int npos = TM * TK;
     const int band = blockIdx.x % p.nTM;
     const int slice = blockIdx.x / p.nTM;
@@ -77,7 +80,7 @@ spmm_generic_kernel(const UsKParams p) {
     uint32_t off = 32;
     uint32_t* offs = reinterpret_cast<uint32_t*>(smem + off);
     off = align16(off + (uint32_t)(nk + 1) * 4u);
-    const uint32_t bm_bytes = (uint32_t)npos / 8u;
+    const uint32_t bm_bytes = (uint32_t)npos / (8u * (uint32_t)Q);
     const uint32_t val_cap = (uint32_t)npos * BITS / 8u;
     uint8_t* stage_ptr[2];
     stage_ptr[0] = smem + off; off += align16(bm_bytes + val_cap);
@@ -87,6 +90,7 @@ spmm_generic_kernel(const UsKParams p) {
     uint8_t* xs = smem + off;    // kTB x TK (float for F16, int8 for I4)
     __shared__ uint32_t warp_tot[kThreads / 32];
     __shared__ int flag_s;
+    __shared__ uint8_t perm_s[TM];                    // the tile's row permutation (IE-BME)
 
     const int64_t tile0 = (int64_t)band * p.nTK + kt0;
     for (int q = threadIdx.x; q <= nk; q += kThreads) offs[q] = p.tile_off[tile0 + q];
@@ -163,11 +167,49 @@ spmm_generic_kernel(const UsKParams p) {
                 reinterpret_cast<int8_t*>(xs)[idx] = v;
             }
         }
+        if (ie && threadIdx.x < TM) {
+            uint32_t r = p.perm ? p.perm[(tile0 + q) * TM + threadIdx.x] : (uint32_t)threadIdx.x;
+            if (r >= (uint32_t)TM) {                  // not a row of the tile: refuse it, stay in bounds
+                us::set_status(p.status, US_ERR_CORRUPT);
+                r = threadIdx.x;
+            }
+            perm_s[threadIdx.x] = (uint8_t)r;
+        }
         __syncthreads();
-        const bool tile_ok = P <= len;
+        const bool tile_ok = (uint64_t)P * Q <= len;
         if (!tile_ok && threadIdx.x == 0) us::set_status(p.status, US_ERR_CORRUPT);
 
         // 2. decode every position into the k-major dense tile
+        if (ie) {
+            // IE-BME with areas ("UnionSparse: An Index-Efficient Sparsity
+            // Framework for Low-Bit Sparse LLM Inference on Edge", section V-A,
+            // Fig. 7): position (r, k) of the reordered tile lies in area
+            // q = (r / LM) * CA + k / LK at logical position (r % LM, k % LK);
+            // its value is CV[o_t + q P_t + rho] if that union-mask bit is set.
+            // Row r of the reordered tile is row perm[r] of the original tile.
+            for (int pos = threadIdx.x; pos < npos; pos += kThreads) {
+                const int r = pos / TK, k = pos - r * TK;
+                const int a = r / LM, i = r - a * LM, c = k / LK, j = k - c * LK;
+                const int lp = i * LK + j;
+                const uint64_t word = words[lp >> 6];
+                const int b = lp & 63;
+                const bool set = tile_ok && ((word >> b) & 1ull);
+                uint32_t e = 0;
+                if (set) e = (uint32_t)(a * p.ie_ca + c) * P + wpre[lp >> 6] + (uint32_t)__popcll(word & ((1ull << b) - 1ull));
+                const int row = perm_s[r];
+                if (ELEM == US_F16) {
+                    const uint16_t h = set ? reinterpret_cast<const uint16_t*>(run)[e] : (uint16_t)0;
+                    reinterpret_cast<uint16_t*>(dense)[k * TM + row] = h;
+                } else {
+                    int8_t v = 0;
+                    if (set) {
+                        const uint8_t by = run[e >> 1];
+                        v = (int8_t)us::sext4((e & 1) ? (by >> 4) : by);
+                    }
+                    reinterpret_cast<int8_t*>(dense)[k * TM + row] = v;
+                }
+            }
+        } else
         for (int pos = threadIdx.x; pos < npos; pos += kThreads) {
             const int w = pos >> 6, b = pos & 63;
             const uint64_t word = words[w];
@@ -300,12 +342,14 @@ size_t spmm_generic_ws(int M, int TM, int N, int split, int tok_block) {
 us_status launch_spmm_generic(const UsKParams& p, int elem, cudaStream_t st) {
     if (elem == US_F16) {
         switch (p.TM) {
+            case 16: return launch_t<US_F16, 16>(p, st);
             case 64: return launch_t<US_F16, 64>(p, st);
             case 128: return launch_t<US_F16, 128>(p, st);
             case 256: return launch_t<US_F16, 256>(p, st);
         }
     } else {
         switch (p.TM) {
+            case 16: return launch_t<US_I4, 16>(p, st);
             case 64: return launch_t<US_I4, 64>(p, st);
             case 128: return launch_t<US_I4, 128>(p, st);
             case 256: return launch_t<US_I4, 256>(p, st);

@@ -173,6 +173,68 @@ us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint
 us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y,
                         void* ws, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * IE-BME with areas ("UnionSparse: An Index-Efficient Sparsity Framework for
+ * Low-Bit Sparse LLM Inference on Edge", section V-A with Q = RA*CA > 1,
+ * Fig. 7, and the bitmap-aware row reordering of section V-B).
+ *
+ * A TM x TK tile is the page's local tile.  Its rows are first permuted by
+ * perm (row p of the reordered tile is row perm[t*TM + p] of the original
+ * tile; NULL = identity).  The reordered tile is cut into RA row partitions
+ * and CA column partitions: area q = a*CA + c holds rows a*LM .. a*LM+LM-1
+ * and columns c*LK .. c*LK+LK-1, with LM = TM/RA and LK = TK/CA.
+ *
+ * One union mask per tile: logical position (i, j), scanned row-major
+ * (p = i*LK + j, bit p%64 of word p/64, earlier = less significant), is set
+ * iff some area holds a nonzero there.  TM*TK/(64*Q) words per tile,
+ * tile-major.
+ *
+ * Values: each set position emits one value per area, zeros included, at
+ * CV[tile_off[t] + q*P_t + rho], rho = set positions before it.  The run of
+ * Q*P_t values is zero-padded to 16 bytes:
+ * tile_off[t+1] = tile_off[t] + roundup(Q*P_t).
+ *
+ * Shapes: TM in {16, 64, 128, 256}; TK in {16, 32, 64, 128}; RA, CA in
+ * {1, 2, 4}; RA*CA <= 4; (TM/RA)*(TK/CA) a multiple of 128 (whole 16-byte
+ * bitmap runs); M % TM == K % TK == 0.  Scan order is ROW.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    us_bitmap W;              /* W.order = US_ORDER_ROW; W.bitmap holds the union masks */
+    int32_t RA, CA;           /* row and column partitions, Q = RA * CA */
+    const uint8_t* perm;      /* device, TM bytes per tile (tile-major), or NULL */
+} us_bitmap_ie;
+
+/* Buffer sizes of us_encode_ie (bitmap M*K/(8*Q), offsets, worst-case values,
+ * workspace). */
+us_status us_encode_ie_sizes(int M, int K, int TM, int TK, int RA, int CA, us_elem elem, size_t* bitmap_bytes,
+                             size_t* tile_off_bytes, size_t* values_cap_bytes, size_t* ws_bytes);
+
+/* Dense -> IE-BME with areas, on the GPU (same dense input as us_encode, ROW
+ * scan).  perm: device, TM bytes per tile or NULL; each tile's entries must be
+ * a permutation of 0..TM-1 (an entry >= TM or a repeated row records
+ * US_ERR_INVALID_ARG in the device status).  ws: us_encode_ie_sizes' ws_bytes. */
+us_status us_encode_ie(const void* W, int64_t ldw, int M, int K, int TM, int TK, int RA, int CA, us_elem elem,
+                       const uint8_t* perm, uint64_t* bitmap, uint32_t* tile_off, void* values, size_t values_cap,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Bitmap-aware row reordering (UnionSparse V-B, Eq. 3-5, Algorithm 1), offline
+ * on the host: for every TM x TK tile of the HOST matrix W, the exact minimum
+ * of active union-mask positions over all groupings of its rows into groups of
+ * RA, canonicalised (rows ascending inside a group, groups lexicographic) and
+ * laid out partition-wise.  perm: HOST, TM bytes per tile, tile-major, ready
+ * for us_encode_ie.  The search is exponential in TM: TM <= 20
+ * (US_ERR_UNSUPPORTED otherwise).  nthreads host threads share the tiles. */
+us_status us_reorder_rows(const void* W, int64_t ldw, int M, int K, int TM, int TK, int RA, int CA, us_elem elem,
+                          uint8_t* perm, int nthreads);
+
+/* W4A4 SpMM on IE-BME with areas: the results of us_spmm_w4a4 (int32
+ * accumulators, optional fp16 epilogue) for the matrix W encodes, outputs in
+ * the original row order.  W->W.elem must be US_I4.  Workspace: query
+ * us_workspace_bytes_ie, zero it once.  split_k as in us_spmm_w4a4. */
+us_status us_spmm_w4a4_ie(const us_bitmap_ie* W, const uint8_t* Xq, const uint16_t* s_w, const uint16_t* s_x, int N,
+                          int32_t* Yacc, uint16_t* Y, void* ws, size_t ws_bytes, int split_k, void* stream);
+us_status us_workspace_bytes_ie(const us_bitmap_ie* W, int N, int split_k, size_t* bytes);
+
 /* ColInfo of a COL-order matrix ("Unified Static-Dynamic Pruning for
  * Efficient LLM Inference", section 4.1, Tiled-CBC storage structure): one
  * uint32 per column of every tile, tile-major (colinfo[t * TK + j] for tile t,
