@@ -36,7 +36,7 @@ import threading
 
 import numpy as np
 
-F16, I4 = 0, 1
+F16, I4, I2 = 0, 1, 2
 ROW, COL = 0, 1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -148,7 +148,7 @@ def _dense_view(W: np.ndarray, elem: int) -> np.ndarray:
             W = W.view(np.uint16)
         assert W.dtype == np.uint16, "fp16 weights are passed as float16 or uint16 bit patterns"
     else:
-        assert W.dtype == np.int8, "int4 weights are passed as int8 codes in [-8, 7]"
+        assert W.dtype == np.int8, "int4 / int2 weights are passed as int8 codes in [-8, 7] / [-2, 1]"
     return np.ascontiguousarray(W)
 
 

@@ -55,7 +55,7 @@
 #endif
 
 enum { OR_OK = 0, OR_BAD_ARG = 1, OR_TOO_LARGE = 3, OR_CAPACITY = 4, OR_CORRUPT = 7 };
-enum { OR_F16 = 0, OR_I4 = 1 };
+enum { OR_F16 = 0, OR_I4 = 1, OR_I2 = 2 };
 enum { OR_ROW = 0, OR_COL = 1 };
 
 /* ---------------------------------------------------------------- fp16 ---- */
@@ -80,15 +80,15 @@ uint16_t or_double_to_half(double d) {
 }
 
 /* ------------------------------------------------------------- format ---- */
-static int elem_bits(int elem) { return elem == OR_F16 ? 16 : 4; }
+static int elem_bits(int elem) { return elem == OR_F16 ? 16 : (elem == OR_I4 ? 4 : 2); }
 /* elements per 16-byte padding quantum */
-static int elems_per_16B(int elem) { return elem == OR_F16 ? 8 : 32; }
+static int elems_per_16B(int elem) { return 128 / elem_bits(elem); }
 
 static int check_shape(int M, int K, int TM, int TK, int elem, int order) {
     if (M <= 0 || K <= 0 || TM <= 0 || TK <= 0) return OR_BAD_ARG;
     if (M % TM || K % TK) return OR_BAD_ARG;
     if (((int64_t)TM * TK) % 64) return OR_BAD_ARG;
-    if (elem != OR_F16 && elem != OR_I4) return OR_BAD_ARG;
+    if (elem != OR_F16 && elem != OR_I4 && elem != OR_I2) return OR_BAD_ARG;
     if (order != OR_ROW && order != OR_COL) return OR_BAD_ARG;
     if ((uint64_t)M * (uint64_t)K >= ((uint64_t)1 << 32)) return OR_TOO_LARGE;
     return OR_OK;
@@ -121,12 +121,25 @@ static void put_value(uint8_t* values, int elem, uint64_t e, const void* W, int6
         uint16_t h = ((const uint16_t*)W)[(int64_t)r * ldw + c];
         values[2 * e] = (uint8_t)(h & 0xFF);
         values[2 * e + 1] = (uint8_t)(h >> 8);
-    } else {
+    } else if (elem == OR_I4) {
         int8_t q = ((const int8_t*)W)[(int64_t)r * ldw + c];
         uint8_t nib = (uint8_t)q & 0x0F;
         if (e & 1) values[e >> 1] = (uint8_t)((values[e >> 1] & 0x0F) | (nib << 4));
         else       values[e >> 1] = (uint8_t)((values[e >> 1] & 0xF0) | nib);
+    } else {
+        /* int2 (W2A4, a reading of UnionSparse Fig. 11): element e in bits
+         * 2(e%4) .. 2(e%4)+1 of byte e/4, two's complement in [-2, 1] */
+        int8_t q = ((const int8_t*)W)[(int64_t)r * ldw + c];
+        const int sh = 2 * (int)(e & 3);
+        values[e >> 2] = (uint8_t)((values[e >> 2] & ~(3u << sh)) | (((uint8_t)q & 3u) << sh));
     }
+}
+
+/* zero element e of the packed stream (padding) */
+static void zero_value(uint8_t* values, int elem, uint64_t e) {
+    if (elem == OR_F16) { values[2 * e] = 0; values[2 * e + 1] = 0; }
+    else if (elem == OR_I4) values[e >> 1] &= (e & 1) ? 0x0F : 0xF0;
+    else values[e >> 2] &= (uint8_t)~(3u << (2 * (e & 3)));
 }
 
 /*
@@ -152,11 +165,12 @@ int or_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem
     const int64_t tile_pos = (int64_t)TM * TK;
     const int64_t words_per_tile = tile_pos / 64;
     const int E = elems_per_16B(elem);
-    if (elem == OR_I4) {
+    if (elem != OR_F16) {
+        const int lo = elem == OR_I4 ? -8 : -2, hi = elem == OR_I4 ? 7 : 1;
         for (int r = 0; r < M; ++r)
             for (int c = 0; c < K; ++c) {
                 int8_t q = ((const int8_t*)W)[(int64_t)r * ldw + c];
-                if (q < -8 || q > 7) return OR_BAD_ARG;
+                if (q < lo || q > hi) return OR_BAD_ARG;
             }
     }
     uint64_t off = 0;                      /* in elements */
@@ -182,9 +196,7 @@ int or_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem
             uint64_t padded = (P + E - 1) / E * E;
             for (uint64_t e = off + P; e < off + padded; ++e) {
                 if ((e + 1) * elem_bits(elem) > values_cap * 8) return OR_CAPACITY;
-                if (elem == OR_F16) { values[2 * e] = 0; values[2 * e + 1] = 0; }
-                else if (e & 1) values[e >> 1] &= 0x0F;
-                else values[e >> 1] &= 0xF0;
+                zero_value(values, elem, e);
             }
             off += padded;
             if (off >= ((uint64_t)1 << 32)) return OR_TOO_LARGE;
@@ -198,6 +210,10 @@ int or_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem
 /* value with element index e of the packed stream, as fp16 bits or int4 code */
 static uint16_t get_f16(const uint8_t* values, uint64_t e) {
     return (uint16_t)(values[2 * e] | (values[2 * e + 1] << 8));
+}
+static int8_t get_i2(const uint8_t* values, uint64_t e) {
+    const unsigned c = (values[e >> 2] >> (2 * (e & 3))) & 3u;
+    return (int8_t)(c >= 2 ? (int)c - 4 : (int)c);
 }
 static int8_t get_i4(const uint8_t* values, uint64_t e) {
     uint8_t nib = (e & 1) ? (values[e >> 1] >> 4) : (values[e >> 1] & 0x0F);
@@ -235,7 +251,8 @@ int or_decode(const uint64_t* bitmap, const uint32_t* tile_off, const uint8_t* v
                 if (set) {
                     if (o_t + rho >= o_next) return OR_CORRUPT;
                     if (elem == OR_F16) ((uint16_t*)W)[idx] = get_f16(values, o_t + rho);
-                    else ((int8_t*)W)[idx] = get_i4(values, o_t + rho);
+                    else if (elem == OR_I4) ((int8_t*)W)[idx] = get_i4(values, o_t + rho);
+                    else ((int8_t*)W)[idx] = get_i2(values, o_t + rho);
                     ++rho;
                 } else {
                     if (elem == OR_F16) ((uint16_t*)W)[idx] = 0;

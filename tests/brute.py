@@ -7,7 +7,8 @@ column tiles and the 16-byte padding of its section 4.2.3):
 tile t = tm*nTK + tk; scan row-major (ROW) or column-major (COL) inside the tile;
 bit for scan position p is bit p%64 of word p//64, earlier positions in lower
 bits; nonzeros appended in scan order; each tile's run padded with zeros to a
-multiple of 8 fp16 or 32 int4 elements; offsets count elements.
+multiple of 8 fp16, 32 int4 or 64 int2 elements (int2: four per byte, the
+earlier element in the lower bits, two's complement); offsets count elements.
 """
 from fractions import Fraction
 
@@ -23,7 +24,7 @@ def scan_positions(TM, TK, order):
 def encode(W, TM, TK, elem, order):
     """W: list of lists of ints (int4 codes) or of uint16 fp16 bit patterns."""
     M, K = len(W), len(W[0])
-    quantum = 8 if elem == 0 else 32
+    quantum = {0: 8, 1: 32, 2: 64}[elem]
     words, offsets, stream = [], [0], []
     for tm in range(M // TM):
         for tk in range(K // TK):
@@ -44,9 +45,12 @@ def encode(W, TM, TK, elem, order):
             offsets.append(len(stream))
     if elem == 0:
         data = b"".join(int(v).to_bytes(2, "little") for v in stream)
-    else:
+    elif elem == 1:
         nib = [(v + 16) % 16 for v in stream]
         data = bytes(nib[k] + 16 * nib[k + 1] for k in range(0, len(nib), 2))
+    else:
+        cr = [(v + 4) % 4 for v in stream]
+        data = bytes(cr[k] + 4 * cr[k + 1] + 16 * cr[k + 2] + 64 * cr[k + 3] for k in range(0, len(cr), 4))
     return words, offsets, data
 
 

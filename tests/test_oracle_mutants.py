@@ -41,6 +41,8 @@ MUTANTS = {
     "ie_areas_column_major": ("const int q = a * CA + c;", "const int q = c * RA + a;"),
     "reorder_cost_ignores_union": ("        cost += any;", "        cost += 1;"),
     "reorder_perm_groupwise": ("perm[p * G + g] = (uint8_t)groups[g][p];", "perm[g * RA + p] = (uint8_t)groups[g][p];"),
+    "int2_sign_wrong": ("return (int8_t)(c >= 2 ? (int)c - 4 : (int)c);", "return (int8_t)(c >= 2 ? (int)c - 2 : (int)c);"),
+    "int2_crumb_order_swapped": ("const int sh = 2 * (int)(e & 3);", "const int sh = 6 - 2 * (int)(e & 3);"),
     "tile_numbering_colmajor": ("            const int64_t t = (int64_t)tm * nTK + tk;\n            uint64_t* words = bitmap + t * words_per_tile;\n"
                                 "            for (int64_t w = 0; w < words_per_tile; ++w) words[w] = 0;\n            uint64_t P = 0; ",
                                 "            const int64_t t = (int64_t)tk * nTM + tm;\n            uint64_t* words = bitmap + t * words_per_tile;\n"

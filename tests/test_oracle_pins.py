@@ -18,6 +18,7 @@ from tests import brute
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 F16, I4, ROW, COL = 0, 1, 0, 1
+I2 = 2
 
 
 def _popcount64(a: np.ndarray) -> np.ndarray:
@@ -27,6 +28,12 @@ def _popcount64(a: np.ndarray) -> np.ndarray:
 
 def _rand_i4(rng, M, K, density):
     q = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
+    q[rng.random((M, K)) >= density] = 0
+    return q
+
+
+def _rand_i2(rng, M, K, density):
+    q = rng.integers(-2, 2, size=(M, K)).astype(np.int8)
     q[rng.random((M, K)) >= density] = 0
     return q
 
@@ -105,14 +112,19 @@ def test_tiled_cbc_storage_formula(orc):
 
 
 # ------------------------------------------------------------ brute force --
-@pytest.mark.parametrize("elem", [F16, I4])
+@pytest.mark.parametrize("elem", [F16, I4, I2])
 @pytest.mark.parametrize("order", [ROW, COL])
 @pytest.mark.parametrize("shape", [(8, 16, 8, 8), (16, 24, 8, 8), (4, 32, 4, 16), (64, 8, 64, 1)])
 def test_encode_matches_brute_force(orc, elem, order, shape):
     M, K, TM, TK = shape
     rng = np.random.default_rng(M * 31 + K + elem * 7 + order)
     for density in (0.0, 0.3, 0.7, 1.0):
-        W = _rand_f16(rng, M, K, density).view(np.uint16) if elem == F16 else _rand_i4(rng, M, K, density)
+        if elem == F16:
+            W = _rand_f16(rng, M, K, density).view(np.uint16)
+        elif elem == I4:
+            W = _rand_i4(rng, M, K, density)
+        else:
+            W = _rand_i2(rng, M, K, density)
         bm, off, vals = orc.encode(W, TM, TK, elem, order)
         words, offsets, data = brute.encode(brute.to_lists(W), TM, TK, elem, order)
         assert [int(v) for v in bm] == words
@@ -585,3 +597,36 @@ def test_reordering_never_grows_the_union_mask(orc):
     pb = _popcount64(base[0]).reshape(nT, -1).sum(axis=1)
     pr = _popcount64(re[0]).reshape(nT, -1).sum(axis=1)
     assert np.all(pr <= pb) and pr.sum() < pb.sum()
+
+
+# ---------------------------------------------------------------- W2A4 --
+def test_int2_packing_worked_example(orc):
+    """The int2 reading: four values per byte, the earlier element in the lower
+    bits, two's complement.  Row [1, -1, -2, 0, 1, 1, -2, -1]: the seven
+    nonzeros pack to 0b01_10_11_01 = 0x6D and 0b00_11_10_01 = 0x39, then zero
+    padding to 64 elements (16 bytes)."""
+    W = np.zeros((1, 64), np.int8)
+    W[0, :8] = [1, -1, -2, 0, 1, 1, -2, -1]
+    bm, off, vals = orc.encode(W, 1, 64, I2, ROW)
+    assert int(bm[0]) == 0b11110111
+    assert int(off[1]) == 64 and vals.size == 16
+    assert vals[0] == 0x6D and vals[1] == 0x39 and not vals[2:].any()
+    assert np.array_equal(orc.decode(bm, off, vals, 1, 64, 1, 64, I2, ROW), W)
+
+
+def test_w2a4_dense_equals_numpy_gemm_and_refuses_range(orc):
+    rng = np.random.default_rng(12)
+    M, K, N = 64, 192, 5
+    W = rng.integers(-2, 2, size=(M, K)).astype(np.int8)      # every code, zeros included
+    X = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
+    bm, off, vals = orc.encode(W, 64, 64, I2, ROW)
+    Wd = orc.decode(bm, off, vals, M, K, 64, 64, I2, ROW)
+    assert np.array_equal(Wd, W)
+    one = np.ones(M, np.float16)
+    acc, _ = orc.spmm_w4a4(Wd, X, one, np.ones(N, np.float16))
+    assert np.array_equal(acc.astype(np.int64), X.astype(np.int64) @ W.T.astype(np.int64))
+    for bad in (2, -3, 7):
+        Wb = W.copy()
+        Wb[3, 5] = bad
+        with pytest.raises(Exception):
+            orc.encode(Wb, 64, 64, I2, ROW)
