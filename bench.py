@@ -540,6 +540,27 @@ def measure_extras(us, torch, wl, dev, stream):
         fl = 2 * 4096 * 4096 * N
         pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_col_tiles_4096_s60"] = pfc
+    # W2A4 4096^2 at 50 %: int2 weights decoded into the same dense tiles
+    d2 = wl.w2a4(4096, 4096, 16, 0.5, seed=0)
+    E2 = us.us_encode(torch.from_numpy(d2["Wq"]).to(dev), 64, 64, us.US_I2, us.US_ORDER_ROW)
+    E2.flags = us.US_BITMAP_STATIC
+    n2 = max(4, math.ceil(2.2 * l2 / E2.nbytes()))
+    cps2 = [E2] + [us.Encoded(E2.M, E2.K, E2.TM, E2.TK, E2.elem, E2.order, E2.bitmap.clone(), E2.tile_off.clone(),
+                              E2.values.clone(), E2.values_bytes, E2.flags) for _ in range(n2 - 1)]
+    sw2 = torch.from_numpy(d2["s_w"].view(np.int16)).to(dev)
+    w2 = {"copies": n2, "value_bytes": E2.values_bytes}
+    for N in (1, 8, 16):
+        X2 = torch.from_numpy(wl.pack_int4(d2["Xq"][:N])).to(dev)
+        sx2 = torch.from_numpy(d2["s_x"][:N].view(np.int16)).to(dev)
+        Ya2 = torch.empty(N, 4096, dtype=torch.int32, device=dev)
+        Yh2 = torch.empty(N, 4096, dtype=torch.int16, device=dev)
+        ws2 = us.workspace(us.US_OP_SPMM_W4A4, E2, N)
+        ms = time_graph(torch, stream, lambda: [us.us_spmm_w4a4(E, X2, sw2, sx2, N, Ya2, Yh2, ws2, 0, stream)
+                                                for E in cps2], 20)
+        t = ms * 1e3 / n2
+        b2 = call_bytes(E2.values_bytes, 4096, 4096, N, 64, 64)
+        w2[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": b2, "GB/s": round(b2 / (t * 1e-6) / 1e9, 1)}
+    out["w2a4_4096_s50"] = w2
     # IE-BME with areas: W4A4 4096^2 at 50 %, 16 x 64 local tiles, 2 x 2 areas, with
     # and without the offline row reordering; encoded bytes and the SpMM time
     d = wl.w4a4(4096, 4096, 16, 0.5, seed=0)

@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libus.so")
 
 US_OK, US_ERR_INVALID_ARG, US_ERR_UNSUPPORTED, US_ERR_TOO_LARGE = 0, 1, 2, 3
 US_ERR_WORKSPACE, US_ERR_CUDA, US_ERR_TIMEOUT, US_ERR_CORRUPT = 4, 5, 6, 7
-US_F16, US_I4 = 0, 1
+US_F16, US_I4, US_I2 = 0, 1, 2
 US_ORDER_ROW, US_ORDER_COL = 0, 1
 US_OP_ENCODE, US_OP_SPMM_W4A4, US_OP_SPMM_F16, US_OP_SPMSPV_F16 = 0, 1, 2, 3
 US_BITMAP_STATIC = 1
@@ -170,7 +170,7 @@ def us_encode(W: torch.Tensor, TM: int, TK: int, elem: int, order: int, stream=N
                                       _dptr(tile_off), _dptr(values), values.numel(), _dptr(ws), ws.numel(),
                                       _stream(stream)))
     used_elems = int(tile_off[-1].item()) & 0xFFFFFFFF
-    used = used_elems * (2 if elem == US_F16 else 1) // (1 if elem == US_F16 else 2)
+    used = used_elems * {US_F16: 16, US_I4: 4, US_I2: 2}[elem] // 8
     if shrink:
         values = values[: max(used, 16)].clone()
     return Encoded(M, K, TM, TK, elem, order, bitmap, tile_off, values, used)
@@ -223,7 +223,7 @@ def us_encode_ie(W: torch.Tensor, TM: int, TK: int, RA: int, CA: int, elem: int,
                                             _dptr(perm), _dptr(bitmap), _dptr(tile_off), _dptr(values),
                                             values.numel(), _dptr(ws), ws.numel(), _stream(stream)))
     used_elems = int(tile_off[-1].item()) & 0xFFFFFFFF
-    used = used_elems * (2 if elem == US_F16 else 1) // (1 if elem == US_F16 else 2)
+    used = used_elems * {US_F16: 16, US_I4: 4, US_I2: 2}[elem] // 8
     values = values[: max(used, 16)].clone()
     return EncodedIE(Encoded(M, K, TM, TK, elem, US_ORDER_ROW, bitmap, tile_off, values, used), RA, CA, perm)
 

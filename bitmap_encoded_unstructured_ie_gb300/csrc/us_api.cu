@@ -46,7 +46,7 @@ bool tile_ok(int TM, int TK) {
 us_status check_shape(int M, int K, int TM, int TK, int elem) {
     if (M <= 0 || K <= 0 || !tile_ok(TM, TK)) return US_ERR_INVALID_ARG;
     if (M % TM || K % TK) return US_ERR_INVALID_ARG;
-    if (elem != US_F16 && elem != US_I4) return US_ERR_INVALID_ARG;
+    if (elem != US_F16 && elem != US_I4 && elem != US_I2) return US_ERR_INVALID_ARG;
     if ((uint64_t)M * (uint64_t)K >= (1ull << 32)) return US_ERR_TOO_LARGE;
     return US_OK;
 }
@@ -90,6 +90,7 @@ void fill_common(UsKParams& p, const us_bitmap* W, int N) {
     p.sk_grid = p.sk_per = p.sk_ring = p.sk_xcols = p.sk_nb = p.sk_slots = p.sk_pre = 0;
     p.flags = W->flags;
     p.order = W->order;
+    p.elem = W->elem;
     p.ie_ra = p.ie_ca = 1;
     p.perm = nullptr;
     p.status = status_ptr();
@@ -126,7 +127,7 @@ Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
         return pl;
     }
     const int nTM = W->M / W->TM, nTK = W->K / W->TK;
-    pl.fast = (op == US_OP_SPMM_W4A4) && us::w4a4_fast_supported(W->TM, W->TK, N) &&
+    pl.fast = (op == US_OP_SPMM_W4A4) && W->elem == US_I4 && us::w4a4_fast_supported(W->TM, W->TK, N) &&
               split_k <= us::w4a4_fast_max_split();
     pl.tok_block = pl.fast ? us::w4a4_fast_tok_block(N) : us::spmm_generic_tok_block(N);
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
@@ -192,7 +193,7 @@ us_status us_encode_sizes(int M, int K, int TM, int TK, us_elem elem, size_t* bi
     const uint64_t nT = (uint64_t)(M / TM) * (K / TK);
     if (bitmap_bytes) *bitmap_bytes = (size_t)M * K / 8;
     if (tile_off_bytes) *tile_off_bytes = (size_t)(nT + 1) * 4;
-    if (values_cap_bytes) *values_cap_bytes = (size_t)M * K * (elem == US_F16 ? 2 : 1) / (elem == US_F16 ? 1 : 2);
+    if (values_cap_bytes) *values_cap_bytes = (size_t)M * K * (elem == US_F16 ? 16 : (elem == US_I4 ? 4 : 2)) / 8;
     if (ws_bytes) *ws_bytes = ((size_t)nT * 4 + 255) & ~(size_t)255;
     return US_OK;
 }
@@ -250,7 +251,8 @@ us_status us_pick_split_k(us_op op, const us_bitmap* W, int N, int* split_k) {
 
 us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_w, const uint16_t* s_x, int N,
                        int32_t* Yacc, uint16_t* Y, void* ws, size_t ws_bytes, int split_k, void* stream) {
-    us_status s = check_bitmap(W, US_I4, US_ORDER_ROW);
+    // W4A4, or W2A4 with int2 weights
+    us_status s = check_bitmap(W, W && W->elem == US_I2 ? US_I2 : US_I4, US_ORDER_ROW);
     if (s != US_OK) return s;
     if (N < 1 || N > 2048 || W->K % 32) return US_ERR_INVALID_ARG;
     if (!Xq || !Yacc || !aligned16(Xq) || !aligned16(Yacc)) return US_ERR_INVALID_ARG;
@@ -270,7 +272,7 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
         p.ws = ws;
         return us::launch_w4a4_sk(p, st);
     }
-    return pl.fast ? us::launch_w4a4_fast(p, st) : us::launch_spmm_generic(p, US_I4, st);
+    return pl.fast ? us::launch_w4a4_fast(p, st) : us::launch_spmm_generic(p, W->elem, st);
 }
 
 us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y, void* ws, size_t ws_bytes,
@@ -512,8 +514,8 @@ us_status us_validate(const us_bitmap* W) {
     const int nTM = W->M / W->TM, nTK = W->K / W->TK;
     const int64_t nT = (int64_t)nTM * nTK;
     const int64_t wpt = (int64_t)W->TM * W->TK / 64;
-    const int bits = W->elem == US_F16 ? 16 : 4;
-    const uint32_t E = W->elem == US_F16 ? 8u : 32u;
+    const int bits = W->elem == US_F16 ? 16 : (W->elem == US_I4 ? 4 : 2);
+    const uint32_t E = 128u / (uint32_t)bits;
     const uint8_t* vals = static_cast<const uint8_t*>(W->values);
     if (W->tile_off[0] != 0) return US_ERR_CORRUPT;
     for (int64_t t = 0; t < nT; ++t) {
@@ -525,7 +527,9 @@ us_status us_validate(const us_bitmap* W) {
         if (P > o1 - o0 || (o1 - o0) - P >= E) return US_ERR_CORRUPT;
         for (uint64_t e = o0 + P; e < o1; ++e) {   // padding must be zero
             const uint8_t by = vals[e * bits / 8];
-            const uint8_t v = bits == 16 ? by : (uint8_t)((e & 1) ? (by >> 4) : (by & 15));
+            const uint8_t v = bits == 16 ? by
+                            : bits == 4 ? (uint8_t)((e & 1) ? (by >> 4) : (by & 15))
+                                        : (uint8_t)((by >> (2 * (e & 3))) & 3);
             if (v || (bits == 16 && vals[e * 2 + 1])) return US_ERR_CORRUPT;
         }
     }

@@ -271,6 +271,7 @@ struct UsKParams {
     // IE-BME with areas (generic kernel only): RA row x CA column partitions of
     // each tile, one union mask, Q = RA*CA value streams; perm: per tile, the
     // original row of each row of the reordered tile (nullptr = identity)
+    int elem;           // US_F16, US_I4 or US_I2 values
     int ie_ra, ie_ca;
     const uint8_t* perm;
     void* ws;           // split-K partials (after the counters)

@@ -51,10 +51,11 @@ enc_count_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nT
         const int64_t i0 = corner + pos_offset(order, TM, TK, p0, ldw);
         const int64_t i1 = corner + pos_offset(order, TM, TK, p1, ldw);
         const bool nz0 = is_nonzero<ELEM>(W, i0), nz1 = is_nonzero<ELEM>(W, i1);
-        if (ELEM == US_I4) {
+        if (ELEM != US_F16) {
+            const int lo = ELEM == US_I4 ? -8 : -2, hi = ELEM == US_I4 ? 7 : 1;
             const int8_t a = reinterpret_cast<const int8_t*>(W)[i0];
             const int8_t b = reinterpret_cast<const int8_t*>(W)[i1];
-            if (a < -8 || a > 7 || b < -8 || b > 7) us::set_status(status, US_ERR_INVALID_ARG);
+            if (a < lo || a > hi || b < lo || b > hi) us::set_status(status, US_ERR_INVALID_ARG);
         }
         const uint32_t lo = __ballot_sync(0xffffffffu, nz0);
         const uint32_t hi = __ballot_sync(0xffffffffu, nz1);
@@ -132,7 +133,7 @@ enc_pack_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK
     __shared__ uint32_t warp_tot[kEncThreads / 32];
 
     const uint64_t o0 = tile_off[t], o1 = tile_off[t + 1];
-    const int bits = (ELEM == US_F16) ? 16 : 4;
+    const int bits = (ELEM == US_F16) ? 16 : (ELEM == US_I4 ? 4 : 2);
     if (o1 < o0 || o1 * bits > values_cap * 8) {
         if (threadIdx.x == 0) us::set_status(status, US_ERR_WORKSPACE);
         return;
@@ -176,7 +177,7 @@ enc_pack_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK
             if (ELEM == US_F16)
                 reinterpret_cast<uint16_t*>(cbuf)[rank] = reinterpret_cast<const uint16_t*>(W)[idx];
             else
-                cbuf[rank] = (uint8_t)reinterpret_cast<const int8_t*>(W)[idx] & 0x0Fu;
+                cbuf[rank] = (uint8_t)reinterpret_cast<const int8_t*>(W)[idx] & (ELEM == US_I4 ? 0x0Fu : 0x03u);
         }
     }
     __syncthreads();
@@ -199,10 +200,14 @@ enc_pack_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK
                         const uint16_t h = reinterpret_cast<const uint16_t*>(cbuf)[e];
                         by = (byte & 1) ? (h >> 8) : (h & 0xFF);
                     }
-                } else {
+                } else if (ELEM == US_I4) {
                     const uint64_t e0 = byte * 2, e1 = e0 + 1;
                     if (e0 < P) by |= cbuf[e0];
                     if (e1 < P) by |= (uint32_t)cbuf[e1] << 4;
+                } else {                               // int2: four per byte, earlier lower
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (byte * 4 + u < P) by |= (uint32_t)cbuf[byte * 4 + u] << (2 * u);
                 }
                 word |= (by & 0xFFu) << (8 * bsub);
             }
@@ -408,12 +413,15 @@ us_status launch_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK
     if (elem == US_F16) {
         enc_count_kernel<US_F16><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, TK, nTK, order, bitmap, counts,
                                                                       status);
-    } else {
+    } else if (elem == US_I4) {
         enc_count_kernel<US_I4><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, TK, nTK, order, bitmap, counts,
+                                                                     status);
+    } else {
+        enc_count_kernel<US_I2><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, TK, nTK, order, bitmap, counts,
                                                                      status);
     }
     if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
-    enc_scan_kernel<<<1, 1024, 0, st>>>(counts, nT, elem == US_F16 ? 8 : 32, tile_off, status);
+    enc_scan_kernel<<<1, 1024, 0, st>>>(counts, nT, elem == US_F16 ? 8 : (elem == US_I4 ? 32 : 64), tile_off, status);
     if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
     if (elem == US_F16) {
         if (cudaFuncSetAttribute(enc_pack_kernel<US_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
@@ -421,11 +429,17 @@ us_status launch_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK
             return US_ERR_CUDA;
         enc_pack_kernel<US_F16><<<(unsigned)nT, kEncThreads, smem, st>>>(
             W, ldw, TM, TK, nTK, order, bitmap, tile_off, (uint8_t*)values, values_cap, status);
-    } else {
+    } else if (elem == US_I4) {
         if (cudaFuncSetAttribute(enc_pack_kernel<US_I4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return US_ERR_CUDA;
         enc_pack_kernel<US_I4><<<(unsigned)nT, kEncThreads, smem, st>>>(
+            W, ldw, TM, TK, nTK, order, bitmap, tile_off, (uint8_t*)values, values_cap, status);
+    } else {
+        if (cudaFuncSetAttribute(enc_pack_kernel<US_I2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return US_ERR_CUDA;
+        enc_pack_kernel<US_I2><<<(unsigned)nT, kEncThreads, smem, st>>>(
             W, ldw, TM, TK, nTK, order, bitmap, tile_off, (uint8_t*)values, values_cap, status);
     }
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;

@@ -55,8 +55,8 @@ template <int ELEM, int TM>
 __global__ void __launch_bounds__(kThreads)
 spmm_generic_kernel(const UsKParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int BITS = (ELEM == US_F16) ? 16 : 4;
-    constexpr int E16 = (ELEM == US_F16) ? 8 : 32;
+    constexpr int BITS = (ELEM == US_F16) ? 16 : (ELEM == US_I4 ? 4 : 2);   // int2: W2A4
+    constexpr int E16 = 128 / BITS;
     constexpr int G = kThreads / TM;                  // token groups
     constexpr int R = kTB / G;                        // tokens per thread
     using acc_t = typename std::conditional<ELEM == US_F16, float, int>::type;
@@ -225,8 +225,13 @@ spmm_generic_kernel(const UsKParams p) {
             } else {
                 int8_t v = 0;
                 if (set) {
-                    const uint8_t by = run[rank >> 1];
-                    v = (int8_t)us::sext4((rank & 1) ? (by >> 4) : by);
+                    if (ELEM == US_I4) {
+                        const uint8_t by = run[rank >> 1];
+                        v = (int8_t)us::sext4((rank & 1) ? (by >> 4) : by);
+                    } else {                          // int2, four per byte, earlier in the lower bits
+                        const uint32_t c = (run[rank >> 2] >> (2 * (rank & 3))) & 3u;
+                        v = (int8_t)((int)c - ((int)(c & 2u) << 1));
+                    }
                 }
                 reinterpret_cast<int8_t*>(dense)[j * TM + i] = v;
             }
@@ -301,7 +306,7 @@ spmm_generic_kernel(const UsKParams p) {
 
 size_t generic_smem(int TM, int TK, int elem, int nk) {
     const size_t npos = (size_t)TM * TK;
-    const size_t bits = elem == US_F16 ? 16 : 4;
+    const size_t bits = elem == US_F16 ? 16 : (elem == US_I4 ? 4 : 2);
     auto a16 = [](size_t x) { return (x + 15) & ~(size_t)15; };
     size_t off = 32;
     off = a16(off + (size_t)(nk + 1) * 4);
@@ -346,6 +351,12 @@ us_status launch_spmm_generic(const UsKParams& p, int elem, cudaStream_t st) {
             case 64: return launch_t<US_F16, 64>(p, st);
             case 128: return launch_t<US_F16, 128>(p, st);
             case 256: return launch_t<US_F16, 256>(p, st);
+        }
+    } else if (elem == US_I2) {
+        switch (p.TM) {
+            case 64: return launch_t<US_I2, 64>(p, st);
+            case 128: return launch_t<US_I2, 128>(p, st);
+            case 256: return launch_t<US_I2, 256>(p, st);
         }
     } else {
         switch (p.TM) {

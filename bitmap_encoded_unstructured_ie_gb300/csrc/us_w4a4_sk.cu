@@ -68,7 +68,20 @@ __host__ __device__ inline int sk_cta_of(int64_t t, int G, int nT) { return (int
 __host__ __device__ inline int sk_start(int c, int G, int nT) { return (int)((int64_t)c * nT / G); }
 
 
-template <int N, int NT>
+// Eight int2 values (low 16 bits, the earlier value in the lower bits) as
+// eight sign-extended int4 nibbles: spread the 2-bit fields 8, 4 and 2 bits
+// apart, then copy each sign bit into the two bits above it.
+__device__ __forceinline__ uint32_t int2x8_to_int4x8(uint32_t x) {
+    x &= 0xFFFFu;
+    x = (x | (x << 8)) & 0x00FF00FFu;
+    x = (x | (x << 4)) & 0x0F0F0F0Fu;
+    x = (x | (x << 2)) & 0x33333333u;
+    const uint32_t sgn = x & 0x22222222u;
+    return x | (sgn << 1) | (sgn << 2);
+}
+
+// WB: weight bits (4: W4A4, 2: W2A4; the dense tiles hold int4 either way)
+template <int N, int NT, int WB>
 __global__ void __launch_bounds__(threads_for(N, NT), 2)   // two per SM: this launch and the next
 w4a4_sk_kernel(const UsKParams p) {
     constexpr int kNW = nw_for(N, NT);
@@ -97,6 +110,8 @@ w4a4_sk_kernel(const UsKParams p) {
     const int nb = (t1 - 1) / p.nTK - band0 + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool early = (p.flags & US_BITMAP_STATIC) != 0;   // weights may be fetched before the wait
+    constexpr uint32_t kQ = 128u / WB;                      // elements per 16 bytes (run padding)
+    constexpr int kLogEPW = WB == 4 ? 3 : 4;                // elements per 32-bit word: 8 or 16
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kR; ++i) {
@@ -119,9 +134,9 @@ w4a4_sk_kernel(const UsKParams p) {
         if (early && lane == 0) us::bulk_prefetch_l2(p.bitmap + (int64_t)t0 * (kBm / 8), (uint32_t)per * kBm);
         for (int i = lane; i <= per; i += 32) offs[i] = p.tile_off[t0 + i];
         __syncwarp();
-        if (early && lane == 0 && offs[per] > offs[0] && (offs[0] & 31u) == 0 && (offs[per] & 31u) == 0 &&
-            (uint64_t)offs[per] * 4u <= p.values_bytes * 8ull)
-            us::bulk_prefetch_l2(p.values + offs[0] / 2u, (offs[per] - offs[0]) / 2u);
+        if (early && lane == 0 && offs[per] > offs[0] && (offs[0] & (kQ - 1u)) == 0 && (offs[per] & (kQ - 1u)) == 0 &&
+            (uint64_t)offs[per] * WB <= p.values_bytes * 8ull)
+            us::bulk_prefetch_l2(p.values + offs[0] * WB / 8u, (offs[per] - offs[0]) * WB / 8u);
         const int nch = (per + kC - 1) / kC;
         uint32_t pos = 0;                                     // end of the newest chunk in the ring
         bool waited = !early;
@@ -130,13 +145,13 @@ w4a4_sk_kernel(const UsKParams p) {
             bool ok = true;
             if (lane < ct) {
                 const uint32_t a = offs[q0 + lane], e = offs[q0 + lane + 1];
-                ok = e >= a && (e - a) <= (uint32_t)(kTM * kTK) && (a & 31u) == 0 && (e & 31u) == 0 &&
-                     (uint64_t)e * 4u <= p.values_bytes * 8ull;
+                ok = e >= a && (e - a) <= (uint32_t)(kTM * kTK) && (a & (kQ - 1u)) == 0 && (e & (kQ - 1u)) == 0 &&
+                     (uint64_t)e * WB <= p.values_bytes * 8ull;
             }
             const bool all_ok = __all_sync(0xffffffffu, ok);
             int fail = 0;
             if (lane == 0) {
-                const uint32_t vb = all_ok ? (offs[q0 + ct] - offs[q0]) / 2u : 0u;
+                const uint32_t vb = all_ok ? (offs[q0 + ct] - offs[q0]) * WB / 8u : 0u;
                 const uint32_t sz = (uint32_t)ct * kBm + vb;
                 // room for sz bytes: the ring holds the chunks [tail, ch) in order,
                 // from the start of chunk `tail` to `pos`, wrapping at D
@@ -174,7 +189,7 @@ w4a4_sk_kernel(const UsKParams p) {
                     us::mbar_arrive_expect_tx(&S.full[slot], sz);
                     us::bulk_g2s(ring + place, p.bitmap + (int64_t)(t0 + q0) * (kBm / 8), (uint32_t)ct * kBm,
                                  &S.full[slot]);
-                    if (vb) us::bulk_g2s(ring + place + ct * kBm, p.values + offs[q0] / 2u, vb, &S.full[slot]);
+                    if (vb) us::bulk_g2s(ring + place + ct * kBm, p.values + offs[q0] * WB / 8u, vb, &S.full[slot]);
                     // a short last chunk has fewer tiles: arrive for the missing ones
                     for (int i = ct; i < kC; ++i) us::mbar_arrive(&S.empty[slot]);
                     pos = place + sz;
@@ -271,7 +286,8 @@ w4a4_sk_kernel(const UsKParams p) {
             const uint32_t totA = tot & 0xFFFFu;
             const bool good = S.bad[slot] == 0 && totA + (tot >> 16) <= offs[q + 1] - offs[q];
             if (!good && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-            const uint32_t* vw = reinterpret_cast<const uint32_t*>(base + ct * kBm + (offs[q] - offs[ch * kC]) / 2u);
+            const uint32_t* vw =
+                reinterpret_cast<const uint32_t*>(base + ct * kBm + (offs[q] - offs[ch * kC]) * WB / 8u);
             const uint32_t vbase = (uint32_t)__cvta_generic_to_shared(vw);
             // rows lane (h = 0) and lane + 32 (h = 1) step by step side by side;
             // each keeps a three-word window over its run: a step consumes at
@@ -283,8 +299,8 @@ w4a4_sk_kernel(const UsKParams p) {
                 const uint64_t w = good ? (h ? wB : wA) : 0ull;        // a bad tile decodes as zeros
                 lo[h] = (uint32_t)w;
                 hi[h] = (uint32_t)(w >> 32);
-                ob[h] = h ? totA + (ex >> 16) : (ex & 0xFFFFu);         // nibble index of the row's first value
-                wi[h] = ob[h] >> 3;
+                ob[h] = h ? totA + (ex >> 16) : (ex & 0xFFFFu);         // element index of the row's first value
+                wi[h] = ob[h] >> kLogEPW;
                 cur[h] = vw[wi[h]];
                 nxt[h] = vw[wi[h] + 1];
                 nn[h] = vw[wi[h] + 2];
@@ -296,14 +312,16 @@ w4a4_sk_kernel(const UsKParams p) {
                 for (int h = 0; h < 2; ++h) {
                     const uint32_t bb = __byte_perm(bt < 4 ? lo[h] : hi[h], 0u, 0x4440u | (uint32_t)(bt & 3));
                     if (bt > 0) {
-                        const uint32_t nwi = ob[h] >> 3;
+                        const uint32_t nwi = ob[h] >> kLogEPW;
                         const uint32_t adv = nwi != wi[h];
                         cur[h] = adv ? nxt[h] : cur[h];
                         nxt[h] = adv ? nn[h] : nxt[h];
                         us::lds_u32_if(nn[h], adv, vbase + 4u * (nwi + 2u));
                         wi[h] = nwi;
                     }
-                    const uint32_t win = __funnelshift_r(cur[h], nxt[h], ob[h] << 2);
+                    // ranks ob .. ob + 7 as eight nibbles (int2: spread to sign-extended int4)
+                    const uint32_t win = WB == 4 ? __funnelshift_r(cur[h], nxt[h], ob[h] << 2)
+                                                 : int2x8_to_int4x8(__funnelshift_r(cur[h], nxt[h], ob[h] << 1));
                     const uint2 ent = lut[bb * kLutRep + lut_lane];
                     const uint32_t odd = win & ent.y;                       // 16 w, ranks 1,3,5,(7)
                     const uint32_t even = (win << 4) & 0xF0F0F0F0u;         // 16 w, ranks 0,2,4,6
@@ -672,7 +690,7 @@ bool sk_plan(int nTM, int nTK, int N, bool pre, SkPlan& pl) {
 
 template <int N, int NT>
 us_status launch_sk_n(UsKParams p, const SkPlan& pl, cudaStream_t st) {
-    auto kern = w4a4_sk_kernel<N, NT>;
+    auto kern = p.elem == US_I2 ? w4a4_sk_kernel<N, NT, 2> : w4a4_sk_kernel<N, NT, 4>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem) != cudaSuccess)
         return US_ERR_CUDA;
     p.sk_grid = pl.G; p.sk_per = pl.per; p.sk_ring = pl.ring; p.sk_xcols = pl.xcols; p.sk_nb = pl.nb;

@@ -18,6 +18,8 @@ their shapes and sparsity statistics:
 * int4 quantisation (W4A4): per row (weights) or per token (activations),
   ``s = fp16(max|v| / 7)`` and ``q = clip(rint(v / s), -8, 7)``; a kept weight
   that rounds to 0 is a zero of the quantised matrix;
+* int2 quantisation (W2A4, the plain reading of a setting the pages only name):
+  per row ``s = fp16(max|w| / 2)`` and ``q = clip(rint(w / s), -2, 1)``;
 * spMspV activations: ``x ~ N(0, 1)`` with its ``round(p * K)`` smallest entries
   set to 0 (a ReLU-style threshold at the empirical p-quantile).
 """
@@ -95,6 +97,29 @@ def w4a4(M: int, K: int, N: int, sparsity: float, seed: int, rows: str = "fixed"
     keep = beta_row_keep(seed + 2, M) if rows == "beta" else np.full(M, 1.0 - sparsity)
     W = np.where(magnitude_mask(W, keep), W, np.float32(0))
     Wq, s_w = quantize_int4_rows(W)
+    X = _normal(seed + 1, (N, K), 1.0)
+    Xq, s_x = quantize_int4_rows(X)
+    return {"Wq": Wq, "s_w": s_w, "Xq": Xq, "Xq_packed": pack_int4(Xq), "s_x": s_x}
+
+
+def quantize_int2_rows(V: np.ndarray):
+    """Per-row int2 codes in [-2, 1] with an fp16 scale amax / 2 per row (the
+    positive end saturates at +1; zeros of V stay zero)."""
+    V = np.asarray(V, dtype=np.float32)
+    amax = np.abs(V).max(axis=1)
+    s = (amax / np.float32(2.0)).astype(np.float16)
+    s = np.where(s == 0, np.float16(1.0), s).astype(np.float16)
+    q = np.clip(np.rint(V / s.astype(np.float32)[:, None]), -2, 1).astype(np.int8)
+    return q, s
+
+
+def w2a4(M: int, K: int, N: int, sparsity: float, seed: int):
+    """W2A4 workload (UnionSparse Fig. 11 names the setting): the W4A4 recipe
+    with magnitude-pruned weights quantised per row to int2 codes in [-2, 1];
+    activations per-token int4.  Same keys as ``w4a4``."""
+    W = _normal(seed, (M, K), 0.02)
+    W = np.where(magnitude_mask(W, np.full(M, 1.0 - sparsity)), W, np.float32(0))
+    Wq, s_w = quantize_int2_rows(W)
     X = _normal(seed + 1, (N, K), 1.0)
     Xq, s_x = quantize_int4_rows(X)
     return {"Wq": Wq, "s_w": s_w, "Xq": Xq, "Xq_packed": pack_int4(Xq), "s_x": s_x}

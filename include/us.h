@@ -72,7 +72,12 @@ typedef enum {
     US_ERR_CORRUPT = 7        /* inconsistent format detected (host or device) */
 } us_status;
 
-typedef enum { US_F16 = 0, US_I4 = 1 } us_elem;
+/* Element types of the value stream: fp16; int4 (two per byte, even element in
+ * the low nibble, two's complement in [-8, 7]); int2 for W2A4 (four per byte,
+ * the earlier element in the lower bits, two's complement in [-2, 1]: the
+ * pages name W2A4 in UnionSparse Fig. 11 without its layout, so this is the
+ * plain reading).  Runs are padded to 16 bytes: 8 / 32 / 64 elements. */
+typedef enum { US_F16 = 0, US_I4 = 1, US_I2 = 2 } us_elem;
 typedef enum { US_ORDER_ROW = 0, US_ORDER_COL = 1 } us_order;
 typedef enum {
     US_OP_ENCODE = 0,

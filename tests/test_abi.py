@@ -61,13 +61,16 @@ def _oracle_encoded(seed=0, elem=1, order=0, M=256, K=256, TM=64, TK=64):
     if elem == 1:
         W = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
         W[rng.random((M, K)) < 0.5] = 0
+    elif elem == 2:
+        W = rng.integers(-2, 2, size=(M, K)).astype(np.int8)
+        W[rng.random((M, K)) < 0.5] = 0
     else:
         W = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
         W[rng.random((M, K)) < 0.5] = 0
     return o.encode(W, TM, TK, elem, order)
 
 
-@pytest.mark.parametrize("elem,order", [(0, 0), (0, 1), (1, 0), (1, 1)])
+@pytest.mark.parametrize("elem,order", [(0, 0), (0, 1), (1, 0), (1, 1), (2, 0), (2, 1)])
 def test_validate_accepts_oracle_encoding(lib, elem, order):
     from bitmap_encoded_unstructured_ie_gb300 import binding as b
     bm, off, vals = _oracle_encoded(1, elem, order)
@@ -141,3 +144,15 @@ def test_bad_arguments_rejected_without_launch(lib):
     assert L.us_spmspv_f16_ci(ctypes.byref(fcol), CI, X, 2, ctypes.c_float(-1.0), Y, None, 0, None) == 1
     assert L.us_spmspv_f16_ci(ctypes.byref(fcol), None, X, 2, ctypes.c_float(0.0), Y, None, 0, None) == 1
     assert L.us_spmspv_f16_ci(ctypes.byref(fcol), CI, P(0x20002), 2, ctypes.c_float(0.0), Y, None, 0, None) == 1
+
+
+def test_validate_int2_padding(lib):
+    """int2 runs are padded to 64 elements; a nonzero crumb in the padding is corrupt."""
+    from bitmap_encoded_unstructured_ie_gb300 import binding as b
+    bm, off, vals = _oracle_encoded(3, 2, 0)
+    assert b.us_validate_host(bm, off, vals, 256, 256, 64, 64, 2, 0) == b.US_OK
+    P = bin(int(bm[0])).count("1")
+    assert int(off[1]) % 64 == 0 and int(off[1]) > P
+    bad = vals.copy()
+    bad[(int(off[1]) - 1) // 4] |= 0x40                  # the last padding element of tile 0
+    assert b.us_validate_host(bm, off, bad, 256, 256, 64, 64, 2, 0) == b.US_ERR_CORRUPT
