@@ -540,6 +540,32 @@ def measure_extras(us, torch, wl, dev, stream):
         fl = 2 * 4096 * 4096 * N
         pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_col_tiles_4096_s60"] = pfc
+    # the FFN shapes: W4A4 11008 x 4096 and 4096 x 11008, 50 % sparsity with a
+    # per-row Beta(2,2) keep rate, N = 1 / 4 / 16 / 32, static weights
+    ffn = {}
+    for (Mf, Kf) in ((11008, 4096), (4096, 11008)):
+        df = wl.w4a4(Mf, Kf, 32, 0.5, seed=0, rows="beta")
+        Ef = us.us_encode(torch.from_numpy(df["Wq"]).to(dev), 64, 64, us.US_I4, us.US_ORDER_ROW)
+        Ef.flags = us.US_BITMAP_STATIC
+        nf = max(4, math.ceil(2.2 * l2 / Ef.nbytes()))
+        cpf = [Ef] + [us.Encoded(Ef.M, Ef.K, Ef.TM, Ef.TK, Ef.elem, Ef.order, Ef.bitmap.clone(), Ef.tile_off.clone(),
+                                 Ef.values.clone(), Ef.values_bytes, Ef.flags) for _ in range(nf - 1)]
+        swf = torch.from_numpy(df["s_w"].view(np.int16)).to(dev)
+        row = {"copies": nf}
+        for N in (1, 4, 16, 32):
+            Xf_ = torch.from_numpy(wl.pack_int4(df["Xq"][:N])).to(dev)
+            sxf = torch.from_numpy(df["s_x"][:N].view(np.int16)).to(dev)
+            Yaf = torch.empty(N, Mf, dtype=torch.int32, device=dev)
+            Yhf = torch.empty(N, Mf, dtype=torch.int16, device=dev)
+            wsf_ = us.workspace(us.US_OP_SPMM_W4A4, Ef, N)
+            ms = time_graph(torch, stream, lambda: [us.us_spmm_w4a4(E, Xf_, swf, sxf, N, Yaf, Yhf, wsf_, 0, stream)
+                                                    for E in cpf], 10)
+            t = ms * 1e3 / nf
+            bf = call_bytes(Ef.values_bytes, Mf, Kf, N, 64, 64)
+            row[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": bf, "GB/s": round(bf / (t * 1e-6) / 1e9, 1),
+                            "eff_TOPS": round(2 * Mf * Kf * N / (t * 1e-6) / 1e12, 2)}
+        ffn[f"{Mf}x{Kf}"] = row
+    out["w4a4_ffn_beta_s50"] = ffn
     # W2A4 4096^2 at 50 %: int2 weights decoded into the same dense tiles
     d2 = wl.w2a4(4096, 4096, 16, 0.5, seed=0)
     E2 = us.us_encode(torch.from_numpy(d2["Wq"]).to(dev), 64, 64, us.US_I2, us.US_ORDER_ROW)

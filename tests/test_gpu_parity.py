@@ -112,7 +112,7 @@ def test_encode_reports_out_of_range_codes(us):
 
 
 # -------------------------------------------------------------------- W4A4 --
-def run_w4a4(us, E, Xq_packed, s_w, s_x, N, split_k=0, want_y=True):
+def run_w4a4(us, E, Xq_packed, s_w, s_x, N, split_k=0, want_y=True, static=False):
     dev = "cuda"
     X = torch.from_numpy(Xq_packed).to(dev)
     sw = torch.from_numpy(s_w.view(np.int16)).to(dev)
@@ -120,7 +120,9 @@ def run_w4a4(us, E, Xq_packed, s_w, s_x, N, split_k=0, want_y=True):
     Yacc = torch.empty(N, E.M, dtype=torch.int32, device=dev)
     Y = torch.empty(N, E.M, dtype=torch.int16, device=dev) if want_y else None
     ws = us.workspace(us.US_OP_SPMM_W4A4, E, N, split_k)
+    E.flags = us.US_BITMAP_STATIC if static else 0
     us.us_spmm_w4a4(E, X, sw, sx, N, Yacc, Y, ws, split_k)
+    E.flags = 0
     torch.cuda.synchronize()
     assert us.us_get_last_device_status() == us.US_OK
     y = Y.cpu().numpy().view(np.float16) if want_y else None
@@ -431,23 +433,27 @@ def test_spmspv_repeat(us, orc, M, K, TM, TK):
 
 
 # --------------------------------------------------------- full-size shapes --
+@pytest.mark.parametrize("static", [False, True])
 @pytest.mark.parametrize("s", [0.3, 0.5, 0.7])
-def test_w4a4_4096_full(us, orc, s):
+def test_w4a4_4096_full(us, orc, s, static):
     d = wl.w4a4(4096, 4096, 16, s, seed=0)
     E = encode_gpu(us, d["Wq"], 64, 64, I4, ROW)
     for N in (1, 8, 16):
-        acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N)
+        acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N, static=static)
         oacc, oy = orc.spmm_w4a4(d["Wq"], d["Xq"][:N], d["s_w"], d["s_x"][:N], nthreads=orc.max_threads())
         assert np.array_equal(acc, oacc)
         assert np.array_equal(y.view(np.uint16), oy.view(np.uint16))
 
 
+@pytest.mark.parametrize("static", [False, True])
 @pytest.mark.parametrize("M,K", [(11008, 4096), (4096, 11008)])
-def test_w4a4_ffn_full(us, orc, M, K):
+def test_w4a4_ffn_full(us, orc, M, K, static):
+    """The FFN shapes: with static weights a CTA's 73 tiles exceed its dense
+    slots, so some are decoded before the dependency wait and the rest after."""
     d = wl.w4a4(M, K, 32, 0.5, seed=0, rows="beta")
     E = encode_gpu(us, d["Wq"], 64, 64, I4, ROW)
     for N in (1, 4, 16, 32):
-        acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N)
+        acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N, static=static)
         rng = np.random.default_rng(N)
         n_idx = rng.integers(0, N, 3000)
         m_idx = rng.integers(0, M, 3000)
