@@ -137,8 +137,8 @@ class CpuSample:
 
 
 def run_reference(args):
-    rank = int(os.environ.get("RANK", "0"))
-    if rank != 0:
+    from bitmap_encoded_unstructured_ie_gb300 import replicas
+    if replicas.rank_env()[1] != 0:
         return 0
     from oracle import oracle as orc
     orc.build()
@@ -187,13 +187,9 @@ def main():
     from bitmap_encoded_unstructured_ie_gb300 import binding as us
     from bitmap_encoded_unstructured_ie_gb300 import workloads as wl
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
+    from bitmap_encoded_unstructured_ie_gb300 import replicas
+    world, rank, local = replicas.rank_env()
+    dist = replicas.init(world, "nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     us_build.build()
@@ -247,8 +243,7 @@ def main():
     ev = {N: ([], []) for N in NS}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if dist:
-        dist.barrier()
+    replicas.barrier(dist)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
@@ -267,13 +262,8 @@ def main():
         t_end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
-    if dist:
-        dist.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    replicas.barrier(dist)
+    total_ms = replicas.max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
     assert us.us_get_last_device_status(stream) == us.US_OK
 
     per_n = {}
@@ -295,7 +285,7 @@ def main():
     for v in per_n.values():
         v["share"] = round(v["us_per_launch"] / tot, 3)
     step_ms = total_ms / args.steps
-    value = step_bytes * world / (step_ms * 1e-3) / 1e9
+    value = replicas.aggregate_rate(step_bytes, world, step_ms * 1e-3) / 1e9
     # dominant kernel: largest time share
     dom_n = max(per_n, key=lambda k: per_n[k]["us_per_launch"])
     dom = per_n[dom_n]
@@ -305,6 +295,10 @@ def main():
                 "kernel": dom["kernel"], "at_N": int(dom_n), "peak_source": peak_src}
 
     e2e = measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L)
+    # whole job: every replica's bytes over the slowest replica's time
+    e2e_ms = replicas.max_over_ranks(dist, e2e["ms_per_step"], dev)
+    e2e["value"] = round(replicas.aggregate_rate(e2e.pop("_bytes_per_step"), world, e2e_ms * 1e-3) / 1e9, 1)
+    e2e["ms_per_step"] = round(e2e_ms, 4)
 
     extras = {}
     if not args.no_extras and rank == 0:
@@ -341,8 +335,7 @@ def main():
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
+    replicas.finish(dist)
     return 0
 
 
@@ -437,7 +430,7 @@ def measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L):
     ms = a.elapsed_time(b) / steps
     bytes_step = sum(call_bytes(copies[0].values_bytes, M_, K_, N, TM_, TK_) for N in NS) * L
     return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4),
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 4), "_bytes_per_step": bytes_step,
             "how": "CUDA graph of the C-ABI calls with pinned-host H2D of X and D2H of every fp16 output "
                    "(one copy per N per step)"}
 
