@@ -15,11 +15,12 @@
 //    value runs for each 64-column K step into a raw ring, and a 2-D TMA tile
 //    load (128-byte swizzle, zero fill past N) of the matching 256 x 64
 //    activation block into the B stage;
-//  * warps 2-9 (decoders): two threads per weight row; each rebuilds 32
+//  * warps 2-17 (decoders): four threads per weight row; each rebuilds 16
 //    positions per K step - rank = row base (warp scan of the band's row
 //    popcounts) + running popcount, value = run[rank] or 0 - and stores them as
 //    16-byte chunks at the swizzled positions of the A stage, then fences the
-//    generic->async proxy and arrives on the stage's "A full" barrier;
+//    generic->async proxy and arrives on the stage's "A full" barrier (COL
+//    tiles: 4 columns x 4 rows per thread, see the decoder);
 //  * warp 1 (MMA): allocates 256 TMEM columns; one thread issues four
 //    tcgen05.mma kind::f16 (M=128, N=256, K=16) per K step with the fp32
 //    accumulator in TMEM and commits to the stage's "empty" barrier;
@@ -39,7 +40,7 @@ constexpr int kBN = 256;                 // tokens per CTA
 constexpr int kBK = 64;                  // K per step (one bitmap tile column)
 constexpr int kStages = 3;               // A/B stages
 constexpr int kRawStages = 3;            // raw W staging
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 16;
 constexpr int kThreads = 32 * (2 + kDecWarps);
 constexpr int kABytes = kBM * kBK * 2;           // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
@@ -172,9 +173,9 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     } else {
         // ------------------------------------------------------------ decoders
         if constexpr (ORDER == US_ORDER_ROW) {
-            const int d = warp - 2;                            // 0..7: rows 16d .. 16d+15
-            const int row = 16 * d + (lane >> 1);              // 0..127 within the block
-            const int hb = lane & 1;                           // which 32 positions of the row
+            const int d = warp - 2;                            // 0..15: rows 8d .. 8d+7
+            const int row = 8 * d + (lane >> 2);               // 0..127 within the block
+            const int qq = lane & 3;                           // which 16 positions of the row
             const int band_h = row >> 6, i_in_band = row & 63;
             for (int q = 0; q < nk; ++q) {
                 const int rs = q % kRawStages, s = q % kStages;
@@ -201,8 +202,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                 const bool ok = P <= S.raw_len[rs][band_h];
                 if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
                 const uint64_t word = bm[i_in_band];
-                const uint32_t bits = hb ? (uint32_t)(word >> 32) : (uint32_t)word;
-                uint32_t rank = rowbase + (hb ? (uint32_t)__popc((uint32_t)word) : 0u);
+                const uint32_t bits = ok ? (uint32_t)(word >> (16 * qq)) & 0xFFFFu : 0u;
+                uint32_t rank = rowbase + (uint32_t)__popcll(word & ((1ull << (16 * qq)) - 1ull));
                 const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
                 // wait for the A stage to be free (the MMA of step q - kStages finished)
                 if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
@@ -211,19 +212,19 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                 }
                 uint8_t* arow = a_st + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
     #pragma unroll
-                for (int c = 0; c < 4; ++c) {                  // 8 positions per 16-byte chunk
+                for (int c = 0; c < 2; ++c) {                  // 8 positions per 16-byte chunk
                     uint32_t h2[4];
     #pragma unroll
                     for (int j = 0; j < 8; j += 2) {
-                        const uint32_t b0 = ok ? (bits >> (8 * c + j)) & 1u : 0u;
-                        const uint32_t b1 = ok ? (bits >> (8 * c + j + 1)) & 1u : 0u;
+                        const uint32_t b0 = (bits >> (8 * c + j)) & 1u;
+                        const uint32_t b1 = (bits >> (8 * c + j + 1)) & 1u;
                         const uint32_t v0 = b0 ? run[rank] : 0u;
                         rank += b0;
                         const uint32_t v1 = b1 ? run[rank] : 0u;
                         rank += b1;
                         h2[j >> 1] = v0 | (v1 << 16);
                     }
-                    const int chunk = 4 * hb + c;
+                    const int chunk = 2 * qq + c;
                     *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
                 }
                 us::fence_proxy_async_smem();                  // generic writes -> visible to the tensor core
@@ -237,16 +238,16 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
             // COL tiles (Tiled-CBC of "Unified Static-Dynamic Pruning for
             // Efficient LLM Inference", section 4.1: one bitmap word per column,
             // the values column after column).  A thread rebuilds 4 adjacent
-            // columns x 8 rows: per column, rank = column base (warp scan of the
+            // columns x 4 rows: per column, rank = column base (warp scan of the
             // band's column popcounts) + popcount of the rows above + running
             // count; per row it stores the 4 values as one 8-byte piece of the
             // K-major swizzled A stage - the layout alignment of that page's
             // section 4.3 done by the decoder's own stores.  Sixteen lanes (one
-            // 8-row group, all 16 column quads) fill 128 bytes of a row per step.
-            const int d = warp - 2;                        // 0..7
-            const int band_h = d >> 2;
+            // 4-row group, all 16 column quads) fill 128 bytes of a row per step.
+            const int d = warp - 2;                        // 0..15
+            const int band_h = d >> 3;
             const int quad = lane & 15;                    // columns 4 quad .. 4 quad + 3
-            const int rg = ((d & 3) << 1) | (lane >> 4);   // rows 8 rg .. 8 rg + 7 of the band
+            const int rg = ((d & 7) << 1) | (lane >> 4);   // rows 4 rg .. 4 rg + 3 of the band
             for (int q = 0; q < nk; ++q) {
                 const int rs = q % kRawStages, s = q % kStages;
                 if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
@@ -269,9 +270,9 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                 const bool ok = P <= S.raw_len[rs][band_h];
                 if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
                 // the four columns' words, bases (lane j % 32 holds column j's) and
-                // first ranks at row 8 rg
+                // first ranks at row 4 rg
                 uint32_t bits[4], rank[4];
-                const uint64_t below = rg ? (~0ull >> (64 - 8 * rg)) : 0ull;
+                const uint64_t below = rg ? (~0ull >> (64 - 4 * rg)) : 0ull;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int j = 4 * quad + c;
@@ -279,18 +280,19 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     const uint32_t base = j < 32 ? (e & 0xFFFFu) : (tot & 0xFFFFu) + (e >> 16);
                     const uint64_t word = ok ? bm[j] : 0ull;
                     rank[c] = base + (uint32_t)__popcll(word & below);
-                    bits[c] = (uint32_t)(word >> (8 * rg)) & 0xFFu;
+                    bits[c] = (uint32_t)(word >> (4 * rg)) & 0xFu;
                 }
                 const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
                 if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
                     failed = true;
                     break;
                 }
-                // row m = 64 band_h + 8 rg + i: 128 bytes at m * 128, chunk
-                // (4 quad >> 3) ^ (i), half (quad & 1) of it
-                uint8_t* arow = a_st + s * kABytes + (64 * band_h + 8 * rg) * 128 + (quad & 1) * 8;
+                // row m = 64 band_h + 4 rg + i: 128 bytes at m * 128, chunk
+                // (4 quad >> 3) ^ (m & 7), half (quad & 1) of it
+                uint8_t* arow = a_st + s * kABytes + (64 * band_h + 4 * rg) * 128 + (quad & 1) * 8;
+                const int m7 = 4 * (rg & 1);                   // (m & 7) - i
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < 4; ++i) {
                     uint32_t v[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -298,7 +300,7 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                         v[c] = b ? run[rank[c]] : 0u;
                         rank[c] += b;
                     }
-                    *reinterpret_cast<uint2*>(arow + i * 128 + (((quad >> 1) ^ i) << 4)) =
+                    *reinterpret_cast<uint2*>(arow + i * 128 + (((quad >> 1) ^ (m7 + i)) << 4)) =
                         make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
                 }
                 us::fence_proxy_async_smem();              // generic writes -> visible to the tensor core
