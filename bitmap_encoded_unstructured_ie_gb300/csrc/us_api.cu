@@ -120,7 +120,7 @@ Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
     }
     if (op == US_OP_SPMM_F16 && us::tc_f16_supported(W->TM, W->TK, W->M, N)) {
         pl.tc = true;
-        pl.tok_block = us::tc_tok_block();
+        pl.tok_block = us::tc_tok_block(N);
         pl.split = split_k > 0 ? split_k : us::tc_split(W->M, N, W->K / W->TK);
         if (pl.split > W->K / W->TK) pl.split = W->K / W->TK;
         pl.ws = us::tc_ws(W->M, N, pl.split);

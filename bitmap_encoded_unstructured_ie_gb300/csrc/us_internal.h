@@ -40,7 +40,7 @@ us_status launch_w4a4_sk(UsKParams p, cudaStream_t st);
 
 // tensor-core fp16 SpMM for many tokens (us_tc.cu)
 bool tc_f16_supported(int TM, int TK, int M, int N);
-int tc_tok_block();
+int tc_tok_block(int N);
 int tc_split(int M, int N, int nTK);
 size_t tc_ws(int M, int N, int split);
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);

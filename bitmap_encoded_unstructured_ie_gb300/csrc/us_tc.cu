@@ -10,23 +10,29 @@
 // decode writes the tensor cores' own K-major 128-byte-swizzled layout directly,
 // so no separate alignment pass is needed.
 //
-// One CTA computes a 128-row x 256-token output tile over its K slice:
-//  * warp 0 (producer): 1-D bulk copies of both 64-row bands' bitmap words and
-//    value runs for each 64-column K step into a raw ring, and a 2-D TMA tile
-//    load (128-byte swizzle, zero fill past N) of the matching 256 x 64
-//    activation block into the B stage;
-//  * warps 2-17 (decoders): four threads per weight row; each rebuilds 16
+// One CTA computes a 128-row x (256 NH)-token output tile over its K slice
+// (NH = 1 or 2 halves of 256 tokens; with two, every decoded A tile feeds twice
+// as many tokens):
+//  * warp 0 (W producer): 1-D bulk copies of both 64-row bands' bitmap words
+//    and value runs for each 64-column K step into a raw ring; the warp fetches
+//    the tile offsets of 32 K steps at a time;
+//  * warp 2 (X producer): 2-D TMA tile loads (128-byte swizzle, zero fill past
+//    N) of the matching 256 x 64 activation blocks into the B stage, one per
+//    token half that holds tokens;
+//  * warps 3-18 (decoders): four threads per weight row; each rebuilds 16
 //    positions per K step - rank = row base (warp scan of the band's row
 //    popcounts) + running popcount, value = run[rank] or 0 - and stores them as
 //    16-byte chunks at the swizzled positions of the A stage, then fences the
 //    generic->async proxy and arrives on the stage's "A full" barrier (COL
 //    tiles: 4 columns x 4 rows per thread, see the decoder);
-//  * warp 1 (MMA): allocates 256 TMEM columns; one thread issues four
-//    tcgen05.mma kind::f16 (M=128, N=256, K=16) per K step with the fp32
-//    accumulator in TMEM and commits to the stage's "empty" barrier;
-//  * warps 2-5 (epilogue): tcgen05.ld the accumulator (one TMEM lane per
-//    output row) and write fp16 outputs, or, under split-K, fp32 partials that
-//    the last CTA of the tile sums in fixed slice order.
+//  * warp 1 (MMA): allocates 256 NH TMEM columns; one thread issues four
+//    tcgen05.mma kind::f16 (M=128, N=256, K=16) per K step and token half, the
+//    halves into adjacent 256-column fp32 accumulators, and commits to the
+//    stage's "empty" barrier;
+//  * warps 3 .. 3+4NH-1 (epilogue): tcgen05.ld the accumulators (one TMEM lane
+//    per output row, one warp per lane quarter and token half) and write fp16
+//    outputs, or, under split-K, fp32 partials that the last CTA of the tile
+//    sums in fixed slice order.
 #include <cudaTypedefs.h>
 
 #include "us_common.cuh"
@@ -36,21 +42,31 @@
 namespace {
 
 constexpr int kBM = 128;                 // output rows per CTA (two 64-row bands)
-constexpr int kBN = 256;                 // tokens per CTA
+constexpr int kBH = 256;                 // tokens per MMA (one token half)
 constexpr int kBK = 64;                  // K per step (one bitmap tile column)
-constexpr int kStages = 3;               // A/B stages
+constexpr int kMaxStages = 3;            // A/B stages, at most
 constexpr int kRawStages = 3;            // raw W staging
 constexpr int kDecWarps = 16;
-constexpr int kThreads = 32 * (2 + kDecWarps);
+constexpr int kThreads = 32 * (3 + kDecWarps);
 constexpr int kABytes = kBM * kBK * 2;           // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;           // 32 KB
+constexpr int kHBytes = kBH * kBK * 2;           // 32 KB per token half
 constexpr int kRawBm = 2 * 512;                  // two bands' bitmaps (64x64 tiles)
 constexpr int kRawVal = 2 * 64 * 64 * 2;         // two bands' fp16 runs, worst case
 constexpr int kRawBytes = kRawBm + kRawVal;      // 17 KB
 
+// tile shape for NH token halves: 512 tokens leave room for two A/B stages
+template <int NH>
+struct TcShape {
+    static constexpr int kBN = kBH * NH;
+    static constexpr int kStages = NH == 1 ? 3 : 2;
+    static constexpr int kBBytes = kHBytes * NH;
+    static constexpr size_t kSmem = 1024 + kStages * (kABytes + kBBytes) + kRawStages * kRawBytes + 256;
+    static_assert(kSmem <= 232448, "shared memory per CTA");
+};
+
 struct TcSmem {
     uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-    uint64_t a_full[kStages], b_full[kStages], ab_empty[kStages];
+    uint64_t a_full[kMaxStages], b_full[kMaxStages], ab_empty[kMaxStages];
     uint64_t done;
     uint32_t tmem_base;
     uint32_t raw_len[kRawStages][2];     // run length (elements) of each band's tile
@@ -68,18 +84,62 @@ US_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_
 
 struct TcParams {
     UsKParams p;
-    int n_tiles;          // ceil(N / kBN)
+    int n_tiles;          // ceil(N / (256 NH))
 };
 
-template <int ORDER>
+// Sums the split-K partials of one output tile in slice order and writes fp16.
+// An item is four consecutive rows of one token (float4); with SP slices per
+// pass a thread keeps 8 / SP items, eight 16-byte loads, in flight at once.
+// part points at the tile's first row and token in slice 0, token-major with
+// row stride M; slice_stride separates the slices.
+template <int SP>
+US_DEV void tc_reduce(const UsKParams& p, float* part, int64_t slice_stride, int mt, int n0, int nitems) {
+    constexpr int PER = 8 / SP;
+    for (int i0 = threadIdx.x; i0 < nitems; i0 += kThreads * PER) {
+        float4 acc[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s0 = 0; s0 < p.split; s0 += SP) {
+            float4 w[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = u / SP, sl = s0 + u % SP, idx = i0 + j * kThreads;
+                if (sl < p.split && idx < nitems)
+                    w[u] = __ldcg(reinterpret_cast<const float4*>(
+                        part + sl * slice_stride + (int64_t)(idx >> 5) * p.M + (idx & 31) * 4));
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int j = u / SP, sl = s0 + u % SP, idx = i0 + j * kThreads;
+                if (sl < p.split && idx < nitems) {
+                    acc[j].x += w[u].x; acc[j].y += w[u].y; acc[j].z += w[u].z; acc[j].w += w[u].w;
+                    __stcg(reinterpret_cast<float4*>(part + sl * slice_stride + (int64_t)(idx >> 5) * p.M + (idx & 31) * 4),
+                           make_float4(0.f, 0.f, 0.f, 0.f));
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int idx = i0 + j * kThreads;
+            if (idx >= nitems) break;
+            const int n = n0 + (idx >> 5), m = mt * kBM + (idx & 31) * 4;
+            const uint32_t lo = (uint32_t)us::float_to_half_bits(acc[j].x) | ((uint32_t)us::float_to_half_bits(acc[j].y) << 16);
+            const uint32_t hi = (uint32_t)us::float_to_half_bits(acc[j].z) | ((uint32_t)us::float_to_half_bits(acc[j].w) << 16);
+            *reinterpret_cast<uint2*>(p.Y + (int64_t)n * p.M + m) = make_uint2(lo, hi);
+        }
+    }
+}
+
+template <int ORDER, int NH>
 __global__ void __launch_bounds__(kThreads, 1)
 spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) {
+    constexpr int kBN = TcShape<NH>::kBN, kStages = TcShape<NH>::kStages, kBBytes = TcShape<NH>::kBBytes;
     const UsKParams& p = tp.p;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* a_st = smem;                                   // kStages x 16 KB
-    uint8_t* b_st = a_st + kStages * kABytes;               // kStages x 32 KB
+    uint8_t* b_st = a_st + kStages * kABytes;               // kStages x 32 NH KB
     uint8_t* raw = b_st + kStages * kBBytes;                // kRawStages x 17 KB
     TcSmem& S = *reinterpret_cast<TcSmem*>(raw + kRawStages * kRawBytes);
 
@@ -91,7 +151,9 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     const int kt1 = (int)((int64_t)(slice + 1) * p.nTK / p.split);
     const int nk = kt1 - kt0;
     const int band0 = mt * 2;                               // two 64-row bands
-    const uint32_t idesc = us::umma_idesc_f16(kBM, kBN);
+    // token halves holding at least one token (the last tile may have one)
+    const int halves = NH == 1 ? 1 : (nt * kBN + kBH < p.N ? 2 : 1);
+    const uint32_t idesc = us::umma_idesc_f16(kBM, kBH);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawStages; ++s) {
@@ -114,40 +176,67 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     bool failed = false;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
-            for (int q = 0; q < nk && !failed; ++q) {
-                const int rs = q % kRawStages, s = q % kStages;
-                if (q >= kRawStages && !us::mbar_wait(&S.raw_empty[rs], ((q / kRawStages) - 1) & 1, p.status)) {
-                    failed = true;
-                    break;
-                }
-                uint32_t vb[2], o0[2];
+        // ------------------------------------------------------- W producer
+        // the warp loads the tile offsets of 32 K steps at once (lane l: step
+        // q + l), so no global load sits on the per-step path; lane 0 issues
+        uint32_t oa[2] = {0u, 0u}, ob[2] = {0u, 0u};
+        for (int q = 0; q < nk; ++q) {
+            const int rs = q % kRawStages;
+            if ((q & 31) == 0 && q + lane < nk) {
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q;
-                    const uint32_t a = p.tile_off[t], b = p.tile_off[t + 1];
-                    const bool ok = b >= a && (b - a) <= 4096u && (a & 7u) == 0 && (b & 7u) == 0 &&
-                                    (uint64_t)b * 2u <= p.values_bytes;
-                    if (!ok) us::set_status(p.status, US_ERR_CORRUPT);
-                    o0[h] = a;
-                    vb[h] = ok ? (b - a) * 2u : 0u;
-                    S.raw_len[rs][h] = ok ? (b - a) : 0u;
+                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q + lane;
+                    oa[h] = p.tile_off[t];
+                    ob[h] = p.tile_off[t + 1];
+                }
+            }
+            bool ok = true;
+            if (q >= kRawStages && lane == 0) ok = us::mbar_wait(&S.raw_empty[rs], ((q / kRawStages) - 1) & 1, p.status);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                failed = true;
+                break;
+            }
+            uint32_t a[2], b[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                a[h] = __shfl_sync(0xffffffffu, oa[h], q & 31);
+                b[h] = __shfl_sync(0xffffffffu, ob[h], q & 31);
+            }
+            if (lane == 0) {
+                uint32_t vb[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const bool good = b[h] >= a[h] && (b[h] - a[h]) <= 4096u && (a[h] & 7u) == 0 && (b[h] & 7u) == 0 &&
+                                      (uint64_t)b[h] * 2u <= p.values_bytes;
+                    if (!good) us::set_status(p.status, US_ERR_CORRUPT);
+                    vb[h] = good ? (b[h] - a[h]) * 2u : 0u;
+                    S.raw_len[rs][h] = good ? (b[h] - a[h]) : 0u;
                 }
                 uint8_t* r = raw + rs * kRawBytes;
                 us::mbar_arrive_expect_tx(&S.raw_full[rs], kRawBm + vb[0] + vb[1]);
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q;
                     us::bulk_g2s(r + h * 512, p.bitmap + t * 64, 512, &S.raw_full[rs]);
-                    if (vb[h]) us::bulk_g2s(r + kRawBm + h * 8192, p.values + (uint64_t)o0[h] * 2u, vb[h], &S.raw_full[rs]);
+                    if (vb[h]) us::bulk_g2s(r + kRawBm + h * 8192, p.values + (uint64_t)a[h] * 2u, vb[h], &S.raw_full[rs]);
                 }
-                // activation tile for this K step
+            }
+            __syncwarp();
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------- X producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+            for (int q = 0; q < nk; ++q) {
+                const int s = q % kStages;
                 if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
                     failed = true;
                     break;
                 }
-                us::mbar_arrive_expect_tx(&S.b_full[s], kBBytes);
-                tma_load_2d(b_st + s * kBBytes, &xmap, (kt0 + q) * kBK, nt * kBN, &S.b_full[s]);
+                us::mbar_arrive_expect_tx(&S.b_full[s], (uint32_t)(kHBytes * halves));
+                for (int h = 0; h < halves; ++h)
+                    tma_load_2d(b_st + s * kBBytes + h * kHBytes, &xmap, (kt0 + q) * kBK, nt * kBN + h * kBH,
+                                &S.b_full[s]);
             }
         }
     } else if (warp == 1) {
@@ -163,9 +252,13 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                 us::tc_fence_after();
                 const uint64_t ad = us::umma_smem_desc_sw128(a_st + s * kABytes);
                 const uint64_t bd = us::umma_smem_desc_sw128(b_st + s * kBBytes);
+                // K = 16 per MMA: +32 bytes = +2 in the descriptor's address field;
+                // token half h: +32 KB of B, +256 TMEM columns
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)   // K = 16 per MMA: +32 bytes = +2 in the address field
-                    us::umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (q > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    for (int h = 0; h < halves; ++h)
+                        us::umma_f16(tmem + (uint32_t)(h * kBH), ad + 2 * kk, bd + (uint64_t)(h * (kHBytes >> 4)) + 2 * kk,
+                                     idesc, (q > 0 || kk > 0) ? 1u : 0u);
                 us::umma_commit(&S.ab_empty[s]);
             }
             us::umma_commit(&S.done);
@@ -173,7 +266,7 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     } else {
         // ------------------------------------------------------------ decoders
         if constexpr (ORDER == US_ORDER_ROW) {
-            const int d = warp - 2;                            // 0..15: rows 8d .. 8d+7
+            const int d = warp - 3;                            // 0..15: rows 8d .. 8d+7
             const int row = 8 * d + (lane >> 2);               // 0..127 within the block
             const int qq = lane & 3;                           // which 16 positions of the row
             const int band_h = row >> 6, i_in_band = row & 63;
@@ -189,7 +282,7 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                 const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
                 const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
                 uint32_t incl = packed;
-    #pragma unroll
+#pragma unroll
                 for (int dd = 1; dd < 32; dd <<= 1) {
                     const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
                     if (lane >= dd) incl += o;
@@ -244,7 +337,7 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
             // K-major swizzled A stage - the layout alignment of that page's
             // section 4.3 done by the decoder's own stores.  Sixteen lanes (one
             // 4-row group, all 16 column quads) fill 128 bytes of a row per step.
-            const int d = warp - 2;                        // 0..15
+            const int d = warp - 3;                        // 0..15
             const int band_h = d >> 3;
             const int quad = lane & 15;                    // columns 4 quad .. 4 quad + 3
             const int rg = ((d & 7) << 1) | (lane >> 4);   // rows 4 rg .. 4 rg + 3 of the band
@@ -323,25 +416,28 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         for (int q = nk > kStages ? nk - kStages : 0; q < nk; ++q)
             us::mbar_wait(&S.b_full[q % kStages], (q / kStages) & 1, nullptr);
     }
-    if (warp >= 2 && warp < 6) {
+    if (warp >= 3 && warp < 3 + 4 * halves) {
         // the final commit also covers MMAs issued before a failure: wait for it (bounded)
         const bool ready = us::mbar_wait(&S.done, 0, any_failed ? nullptr : p.status) && !any_failed;
         us::tc_fence_after();
         const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
+        const int half = (warp - 3) >> 2;                   // token half: TMEM columns 256 half ..
         const int m = mt * kBM + quarter * 32 + lane;
         const int nbase = nt * kBN;
         float* part = reinterpret_cast<float*>(p.ws);
         const int nTB = tp.n_tiles;
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = half * kBH; c0 < (half + 1) * kBH && nbase + c0 < p.N; c0 += 32) {
             float v[32];
             us::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
             if (!ready) continue;
             if (p.split > 1) {
                 // partials token-major, [slice][token tile][n][m]: a warp's 32 lanes
-                // (rows) store 128 contiguous bytes per column
+                // (rows) store 128 contiguous bytes per column; columns past N are
+                // never written, so they stay zero
                 const int64_t base = (((int64_t)slice * nTB + nt) * kBN + c0) * p.M + m;
 #pragma unroll
-                for (int i = 0; i < 32; ++i) __stcg(part + base + (int64_t)i * p.M, v[i]);
+                for (int i = 0; i < 32; ++i)
+                    if (nbase + c0 + i < p.N) __stcg(part + base + (int64_t)i * p.M, v[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
@@ -362,42 +458,21 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         __syncthreads();
         if (!S.flag) return;
         __threadfence();
-        // the last CTA of this output tile sums the slices in fixed order: four
-        // consecutive rows per thread (float4), every slice's load in flight at
-        // once, outputs written row-contiguous; the partials are cleared behind
-        // (a workspace may be shared with kernels that need it all zero)
-        float* part = reinterpret_cast<float*>(p.ws);
-        // every column is cleared (the slices wrote all kBN of them, padding -0.0
-        // included); outputs only for real tokens
-        for (int idx = threadIdx.x; idx < kBN * (kBM / 4); idx += kThreads) {
-            const int nc = idx / (kBM / 4), mr = (idx - nc * (kBM / 4)) * 4;
-            const int m = mt * kBM + mr, n = nt * kBN + nc;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int s0 = 0; s0 < p.split; s0 += 8) {
-                float4 w[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (s0 + u < p.split)
-                        w[u] = __ldcg(reinterpret_cast<float4*>(
-                            part + (((int64_t)(s0 + u) * tp.n_tiles + nt) * kBN + nc) * p.M + m));
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    if (s0 + u < p.split) {
-                        acc.x += w[u].x; acc.y += w[u].y; acc.z += w[u].z; acc.w += w[u].w;
-                        __stcg(reinterpret_cast<float4*>(part + (((int64_t)(s0 + u) * tp.n_tiles + nt) * kBN + nc) * p.M + m),
-                               make_float4(0.f, 0.f, 0.f, 0.f));
-                    }
-            }
-            if (n >= p.N) continue;
-            const uint32_t lo = (uint32_t)us::float_to_half_bits(acc.x) | ((uint32_t)us::float_to_half_bits(acc.y) << 16);
-            const uint32_t hi = (uint32_t)us::float_to_half_bits(acc.z) | ((uint32_t)us::float_to_half_bits(acc.w) << 16);
-            *reinterpret_cast<uint2*>(p.Y + (int64_t)n * p.M + m) = make_uint2(lo, hi);
-        }
+        // the last CTA of this output tile sums the slices in fixed order and
+        // clears the partials behind (a workspace may be shared with kernels that
+        // need it all zero); the slices wrote the columns of real tokens only
+        const int ntok = min(kBN, p.N - nt * kBN);
+        float* part = reinterpret_cast<float*>(p.ws) + ((int64_t)nt * kBN) * p.M + mt * kBM;
+        const int64_t slice_stride = (int64_t)tp.n_tiles * kBN * p.M;
+        if (p.split == 2)
+            tc_reduce<2>(p, part, slice_stride, mt, nt * kBN, ntok * (kBM / 4));
+        else if (p.split <= 4)
+            tc_reduce<4>(p, part, slice_stride, mt, nt * kBN, ntok * (kBM / 4));
+        else
+            tc_reduce<8>(p, part, slice_stride, mt, nt * kBN, ntok * (kBM / 4));
         if (threadIdx.x == 0) p.counters[mt * tp.n_tiles + nt] = 0u;
     }
 }
-
-constexpr size_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kRawStages * kRawBytes + 256;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -420,19 +495,23 @@ bool tc_f16_supported(int TM, int TK, int M, int N) {
     return TM == 64 && TK == 64 && M % kBM == 0 && N >= 64;
 }
 
-int tc_tok_block() { return kBN; }
+// 512 tokens per CTA once there are more than 256: each decoded A tile then
+// feeds twice as many tokens
+int tc_tok_block(int N) { return N > kBH ? 2 * kBH : kBH; }
 
 int tc_split(int M, int N, int nTK) {
-    const int ctas = (M / kBM) * ((N + kBN - 1) / kBN);
+    const int bn = tc_tok_block(N);
+    const int ctas = (M / kBM) * ((N + bn - 1) / bn);
     int s = 1;
     while (ctas * s * 2 <= num_sms() && nTK / (s * 2) >= 8 && s < 8) s *= 2;
     return s;
 }
 
 size_t tc_ws(int M, int N, int split) {
-    const int n_tiles = (N + kBN - 1) / kBN;
+    const int bn = tc_tok_block(N);
+    const int n_tiles = (N + bn - 1) / bn;
     const size_t counters = ((size_t)(M / kBM) * n_tiles * 4 + 255) & ~(size_t)255;
-    return split <= 1 ? counters : counters + (size_t)split * n_tiles * M * kBN * 4;
+    return split <= 1 ? counters : counters + (size_t)split * n_tiles * M * bn * 4;
 }
 
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
@@ -441,20 +520,24 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)p.K, (cuuint64_t)p.N};
     const cuuint64_t gstride[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBN};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBH};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(p.X), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return US_ERR_CUDA;
+    if (p.tok_block != kBH && p.tok_block != 2 * kBH) return US_ERR_INVALID_ARG;
+    const bool two = p.tok_block == 2 * kBH;
     TcParams tp;
     tp.p = p;
-    tp.n_tiles = (p.N + kBN - 1) / kBN;
-    auto kern = p.order == US_ORDER_COL ? spmm_f16_tc_kernel<US_ORDER_COL> : spmm_f16_tc_kernel<US_ORDER_ROW>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
+    tp.n_tiles = (p.N + p.tok_block - 1) / p.tok_block;
+    auto kern = two ? (p.order == US_ORDER_COL ? spmm_f16_tc_kernel<US_ORDER_COL, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 2>)
+                    : (p.order == US_ORDER_COL ? spmm_f16_tc_kernel<US_ORDER_COL, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 1>);
+    const size_t smem = two ? TcShape<2>::kSmem : TcShape<1>::kSmem;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
     dim3 grid((unsigned)(p.M / kBM), (unsigned)(tp.n_tiles * p.split));
-    kern<<<grid, kThreads, kSmemBytes, st>>>(tp, map);
+    kern<<<grid, kThreads, smem, st>>>(tp, map);
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }
 

@@ -352,6 +352,10 @@ F16_CASES = [
     (256, 1024, 64, 64, 300, 0.5, 2),
     (384, 768, 64, 64, 257, 0.6, 3),
     (128, 512, 64, 64, 512, 1.0, 0),
+    # 512-token tiles: a second tile holding one token half, and one whose
+    # second half holds 9 tokens, under split-K
+    (256, 512, 64, 64, 600, 0.5, 0),
+    (128, 1024, 64, 64, 777, 0.5, 3),
     # CUDA-core paths
     (256, 512, 64, 64, 1, 0.5, 0),
     (256, 512, 64, 64, 5, 0.5, 3),

@@ -61,6 +61,7 @@ CASES = [
     (256, 1024, 64, 64, 64, 0.4, 0),      # tensor cores, one token tile
     (384, 512, 64, 64, 300, 0.6, 0),      # tensor cores, a ragged second token tile
     (256, 2048, 64, 64, 128, 0.5, 4),     # tensor cores, split-K
+    (256, 512, 64, 64, 700, 0.5, 2),      # tensor cores, 512-token tiles, split-K, ragged
     (128, 768, 64, 64, 1, 0.5, 0),        # CUDA cores, one token
     (256, 512, 64, 64, 33, 0.3, 2),       # CUDA cores, split-K, ragged token block
     (256, 512, 128, 32, 40, 0.5, 0),      # other tile shapes: CUDA cores
