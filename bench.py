@@ -234,10 +234,12 @@ def main():
         with torch.cuda.graph(g, stream=stream):
             launch_all(N)
         graphs[N] = g
-    for _ in range(args.warmup):
-        for N in NS:
-            graphs[N].replay()
+    with torch.cuda.stream(stream):        # replays run on the current stream
+        for _ in range(args.warmup):
+            for N in NS:
+                graphs[N].replay()
     stream.synchronize()
+    assert us.us_get_last_device_status(stream) == us.US_OK
 
     # ---- timed region
     ev = {N: ([], []) for N in NS}
@@ -416,8 +418,9 @@ def measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         step()
-    for _ in range(3):
-        g.replay()
+    with torch.cuda.stream(stream):        # replays run on the current stream
+        for _ in range(3):
+            g.replay()
     stream.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -427,6 +430,7 @@ def measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L):
             g.replay()
         b.record(stream)
     stream.synchronize()
+    assert us.us_get_last_device_status(stream) == us.US_OK
     ms = a.elapsed_time(b) / steps
     bytes_step = sum(call_bytes(copies[0].values_bytes, M_, K_, N, TM_, TK_) for N in NS) * L
     return {"value": round(bytes_step / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -435,14 +439,17 @@ def measure_e2e(us, torch, wl, d, copies, sw, dev, stream, args, L):
                    "(one copy per N per step)"}
 
 
-def time_graph(torch, stream, fn, reps=5):
+def time_graph(torch, stream, us, fn, reps=5):
+    """Mean device time (ms) of one replay of a CUDA graph of fn(), captured and
+    replayed on `stream`; the library's device status must stay clean."""
     with torch.cuda.stream(stream):
         fn()
     stream.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         fn()
-    g.replay()
+    with torch.cuda.stream(stream):        # replays run on the current stream
+        g.replay()
     stream.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
@@ -452,6 +459,7 @@ def time_graph(torch, stream, fn, reps=5):
             g.replay()
         b.record(stream)
     stream.synchronize()
+    assert us.us_get_last_device_status(stream) == us.US_OK
     return a.elapsed_time(b) / reps
 
 
@@ -478,7 +486,7 @@ def measure_extras(us, torch, wl, dev, stream):
         act_vals = int(Wnz[:, active].sum()) * 2
         nT = (14336 // 64) * (4096 // 64)
         alg = 14336 * 4096 // 8 + 4 * (nT + 1) + act_vals + 4096 * 2 + 14336 * 2
-        ms = time_graph(torch, stream, lambda: [us.us_spmspv_f16(E, xt, 0.0, ys, wsb, stream) for E in cps])
+        ms = time_graph(torch, stream, us, lambda: [us.us_spmspv_f16(E, xt, 0.0, ys, wsb, stream) for E in cps])
         t = ms * 1e3 / n_cp
         sp[f"zeros_{int(zf * 100)}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
                                         "GB/s": round(alg / (t * 1e-6) / 1e9, 1)}
@@ -496,7 +504,7 @@ def measure_extras(us, torch, wl, dev, stream):
         active = (np.abs(X.astype(np.float32)) > 0).any(axis=0)
         alg = (4 * nTM_s * 4096 + 4 * (nTM_s * 64 + 1) + nTM_s * int(active.sum()) * 8 +
                int(Wnz[:, active].sum()) * 2 + N * 4096 * 2 + N * 14336 * 2)
-        ms = time_graph(torch, stream,
+        ms = time_graph(torch, stream, us,
                         lambda: [us.us_spmspv_f16_ci(E, c, Xt, N, 0.0, Yt, None, stream) for E, c in zip(cps, cis)])
         t = ms * 1e3 / n_cp
         sci[f"zeros_{int(zf * 100)}_N{N}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
@@ -508,7 +516,7 @@ def measure_extras(us, torch, wl, dev, stream):
     Wd = torch.from_numpy(d["Wq"]).to(dev)
     Ee = us.us_encode(Wd, 64, 64, us.US_I4, us.US_ORDER_ROW, None, False)
     wse = torch.zeros(us.encode_sizes(4096, 4096, 64, 64, us.US_I4)[3], dtype=torch.uint8, device=dev)
-    ms = time_graph(torch, stream, lambda: us.us_encode_into(Wd, Ee, wse, stream), 5)
+    ms = time_graph(torch, stream, us, lambda: us.us_encode_into(Wd, Ee, wse, stream), 5)
     out["encode_w4a4_4096"] = {"ms_per_encode": round(ms, 4),
                                "dense_GB/s": round(4096 * 4096 / (ms * 1e-3) / 1e9, 1)}
     # fp16 prefill 4096^2, 60 % sparsity, N = 256 / 1024 / 2048
@@ -519,7 +527,7 @@ def measure_extras(us, torch, wl, dev, stream):
     for N in (256, 1024, 2048):
         Yf = torch.empty(N, 4096, dtype=torch.int16, device=dev)
         wsf = us.workspace(us.US_OP_SPMM_F16, Ef, N)
-        ms = time_graph(torch, stream, lambda: us.us_spmm_f16(Ef, Xf[:N], N, Yf, wsf, 0, stream), 3)
+        ms = time_graph(torch, stream, us, lambda: us.us_spmm_f16(Ef, Xf[:N], N, Yf, wsf, 0, stream), 3)
         fl = 2 * 4096 * 4096 * N
         pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_4096_s60"] = pf
@@ -529,7 +537,7 @@ def measure_extras(us, torch, wl, dev, stream):
     for N in (256, 1024, 2048):
         Yf = torch.empty(N, 4096, dtype=torch.int16, device=dev)
         wsf = us.workspace(us.US_OP_SPMM_F16, Efc, N)
-        ms = time_graph(torch, stream, lambda: us.us_spmm_f16(Efc, Xf[:N], N, Yf, wsf, 0, stream), 3)
+        ms = time_graph(torch, stream, us, lambda: us.us_spmm_f16(Efc, Xf[:N], N, Yf, wsf, 0, stream), 3)
         fl = 2 * 4096 * 4096 * N
         pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_col_tiles_4096_s60"] = pfc
@@ -551,7 +559,7 @@ def measure_extras(us, torch, wl, dev, stream):
             Yaf = torch.empty(N, Mf, dtype=torch.int32, device=dev)
             Yhf = torch.empty(N, Mf, dtype=torch.int16, device=dev)
             wsf_ = us.workspace(us.US_OP_SPMM_W4A4, Ef, N)
-            ms = time_graph(torch, stream, lambda: [us.us_spmm_w4a4(E, Xf_, swf, sxf, N, Yaf, Yhf, wsf_, 0, stream)
+            ms = time_graph(torch, stream, us, lambda: [us.us_spmm_w4a4(E, Xf_, swf, sxf, N, Yaf, Yhf, wsf_, 0, stream)
                                                     for E in cpf], 10)
             t = ms * 1e3 / nf
             bf = call_bytes(Ef.values_bytes, Mf, Kf, N, 64, 64)
@@ -574,7 +582,7 @@ def measure_extras(us, torch, wl, dev, stream):
         Ya2 = torch.empty(N, 4096, dtype=torch.int32, device=dev)
         Yh2 = torch.empty(N, 4096, dtype=torch.int16, device=dev)
         ws2 = us.workspace(us.US_OP_SPMM_W4A4, E2, N)
-        ms = time_graph(torch, stream, lambda: [us.us_spmm_w4a4(E, X2, sw2, sx2, N, Ya2, Yh2, ws2, 0, stream)
+        ms = time_graph(torch, stream, us, lambda: [us.us_spmm_w4a4(E, X2, sw2, sx2, N, Ya2, Yh2, ws2, 0, stream)
                                                 for E in cps2], 20)
         t = ms * 1e3 / n2
         b2 = call_bytes(E2.values_bytes, 4096, 4096, N, 64, 64)
@@ -602,7 +610,7 @@ def measure_extras(us, torch, wl, dev, stream):
             X = torch.from_numpy(wl.pack_int4(d["Xq"][:N])).to(dev)
             Ya = torch.empty(N, 4096, dtype=torch.int32, device=dev)
             wsi = us.workspace_ie(Ei, N)
-            ms = time_graph(torch, stream, lambda: us.us_spmm_w4a4_ie(Ei, X, None, None, N, Ya, None, wsi, 0, stream), 20)
+            ms = time_graph(torch, stream, us, lambda: us.us_spmm_w4a4_ie(Ei, X, None, None, N, Ya, None, wsi, 0, stream), 20)
             row[f"N{N}_us"] = round(ms * 1e3, 2)
         ie[name] = row
     ie["reorder_host_s"] = round(reorder_s, 2)
@@ -613,7 +621,7 @@ def measure_extras(us, torch, wl, dev, stream):
         Xh = torch.from_numpy(np.random.default_rng(4).standard_normal((N, 4096)).astype(np.float16).view(np.int16)).to(dev)
         Xq = torch.empty(N, 2048, dtype=torch.uint8, device=dev)
         sq = torch.empty(N, dtype=torch.int16, device=dev)
-        ms = time_graph(torch, stream, lambda: us.us_quantize_x(Xh, N, 4096, Xq, sq, stream), 20)
+        ms = time_graph(torch, stream, us, lambda: us.us_quantize_x(Xh, N, 4096, Xq, sq, stream), 20)
         byt = N * 4096 * 2 + N * 2048 + N * 2
         qz[str(N)] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1)}
     out["quantize_x_k4096"] = qz

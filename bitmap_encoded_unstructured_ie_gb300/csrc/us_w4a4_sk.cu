@@ -258,7 +258,9 @@ w4a4_sk_kernel(const UsKParams p) {
         us::named_bar_sync(1, kNW * 32);
 
         const uint32_t lut_lane = (uint32_t)(lane % kLutRep);
-        const int P = early ? p.sk_pre : 0;                   // tiles decoded before the wait
+        // tiles decoded before the wait: the plan's count, capped at this CTA's
+        // own range (ranges differ by one tile where G does not divide nT)
+        const int P = early ? min(p.sk_pre, per) : 0;
         // Decode tile q of the range into the dense packed-int4 tile dst: lane l
         // takes rows l and l + 32; row bases come from one warp scan of packed
         // popcounts (the word-level part of UnionSparse's idx_base, section
