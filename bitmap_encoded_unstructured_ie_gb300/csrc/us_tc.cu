@@ -14,21 +14,23 @@
 // (NH = 1 or 2 halves of 256 tokens; with two, every decoded A tile feeds twice
 // as many tokens):
 //  * warp 0 (W producer): 1-D bulk copies of both 64-row bands' bitmap words
-//    and value runs for each 64-column K step into a raw ring; the warp fetches
-//    the tile offsets of 32 K steps at a time;
+//    and value runs for each 64-column K step, packed by their real length into
+//    a byte ring (up to eight K steps in flight), the next step's tile
+//    offsets loaded one step ahead;
 //  * warp 2 (X producer): 2-D TMA tile loads (128-byte swizzle, zero fill past
 //    N) of the matching 256 x 64 activation blocks into the B stage, one per
 //    token half that holds tokens;
-//  * warps 3-18 (decoders): four threads per weight row; each rebuilds 16
-//    positions per K step - rank = row base (warp scan of the band's row
-//    popcounts) + running popcount, value = run[rank] or 0 - and stores them as
-//    16-byte chunks at the swizzled positions of the A stage, then fences the
-//    generic->async proxy and arrives on the stage's "A full" barrier (COL
-//    tiles: 4 columns x 4 rows per thread, see the decoder);
+//  * warps 3-18 (decoders), two groups of eight on alternate K steps, so that
+//    two steps are decoded at once into three A stages: four threads per weight
+//    row, each rebuilding 16 positions of two rows per K step - rank = row base
+//    (warp scan of the band's row popcounts) + running popcount, value =
+//    run[rank] or 0 - stored as 16-byte chunks at the swizzled positions of the
+//    A stage, then a generic->async proxy fence and an arrive on the stage's
+//    "A full" barrier (COL tiles: 4 columns x 4 rows per thread, twice);
 //  * warp 1 (MMA): allocates 256 NH TMEM columns; one thread issues four
 //    tcgen05.mma kind::f16 (M=128, N=256, K=16) per K step and token half, the
-//    halves into adjacent 256-column fp32 accumulators, and commits to the
-//    stage's "empty" barrier;
+//    halves into adjacent 256-column fp32 accumulators, and commits to the A
+//    and B stages' "empty" barriers;
 //  * warps 3 .. 3+4NH-1 (epilogue): tcgen05.ld the accumulators (one TMEM lane
 //    per output row, one warp per lane quarter and token half) and write fp16
 //    outputs, or, under split-K, fp32 partials that the last CTA of the tile
@@ -44,34 +46,46 @@ namespace {
 constexpr int kBM = 128;                 // output rows per CTA (two 64-row bands)
 constexpr int kBH = 256;                 // tokens per MMA (one token half)
 constexpr int kBK = 64;                  // K per step (one bitmap tile column)
-constexpr int kMaxStages = 3;            // A/B stages, at most
-constexpr int kRawStages = 3;            // raw W staging
-constexpr int kDecWarps = 16;
+constexpr int kAStages = 3;              // decoded A stages
+constexpr int kMaxBStages = 3;           // activation stages, at most
+constexpr int kRawSlots = 8;             // K steps whose raw weights may be in flight
+constexpr int kGroups = 2;               // decoder groups, on alternate K steps
+constexpr int kGroupWarps = 8;           // warps per decoder group
+constexpr int kDecWarps = kGroups * kGroupWarps;
 constexpr int kThreads = 32 * (3 + kDecWarps);
 constexpr int kABytes = kBM * kBK * 2;           // 16 KB
 constexpr int kHBytes = kBH * kBK * 2;           // 32 KB per token half
 constexpr int kRawBm = 2 * 512;                  // two bands' bitmaps (64x64 tiles)
-constexpr int kRawVal = 2 * 64 * 64 * 2;         // two bands' fp16 runs, worst case
-constexpr int kRawBytes = kRawBm + kRawVal;      // 17 KB
+constexpr int kRawMax = kRawBm + 2 * 64 * 64 * 2;   // one K step's raw weights, worst case (17 KB)
+constexpr int kHeader = 512;
+constexpr size_t kSmemCap = 232448;              // dynamic shared memory per CTA
 
-// tile shape for NH token halves: 512 tokens leave room for two A/B stages
+// tile shape for NH token halves; the raw ring takes what the stages leave
 template <int NH>
 struct TcShape {
     static constexpr int kBN = kBH * NH;
-    static constexpr int kStages = NH == 1 ? 3 : 2;
+    static constexpr int kBStages = NH == 1 ? 3 : 2;
     static constexpr int kBBytes = kHBytes * NH;
-    static constexpr size_t kSmem = 1024 + kStages * (kABytes + kBBytes) + kRawStages * kRawBytes + 256;
-    static_assert(kSmem <= 232448, "shared memory per CTA");
+    static constexpr size_t kFixed = 1024 + (size_t)kAStages * kABytes + (size_t)kBStages * kBBytes + kHeader;
+    static constexpr size_t kRingAll = kSmemCap - kFixed;
+    static constexpr int kRing = (int)((kRingAll > 65536 ? 65536 : kRingAll) & ~size_t(15));
+    static constexpr size_t kSmem = kFixed + (size_t)kRing;
+    static_assert(kRing >= 2 * kRawMax, "the raw ring holds two worst-case K steps");
+    static_assert(kSmem <= kSmemCap, "shared memory per CTA");
 };
 
 struct TcSmem {
-    uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-    uint64_t a_full[kMaxStages], b_full[kMaxStages], ab_empty[kMaxStages];
+    uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];
+    uint64_t a_full[kAStages], a_empty[kAStages];
+    uint64_t b_full[kMaxBStages], b_empty[kMaxBStages];
     uint64_t done;
     uint32_t tmem_base;
-    uint32_t raw_len[kRawStages][2];     // run length (elements) of each band's tile
+    uint32_t raw_pos[kRawSlots];         // ring offset of the K step in slot s
+    uint32_t raw_len[kRawSlots][2];      // run length (elements) of each band's tile
+    uint32_t issued_w, issued_x;         // K steps whose copies were issued
     uint32_t flag;
 };
+static_assert(sizeof(TcSmem) <= kHeader, "header");
 
 // 2-D TMA tile load (x = K element, y = token) completing on `bar`
 US_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
@@ -79,6 +93,16 @@ US_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
         "[%4];" ::"r"(us::smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(us::smem_addr(bar))
+        : "memory");
+}
+
+// As tma_load_2d, the tile written at the same offset in every CTA of the
+// cluster named in `mask`, each completing on its own barrier at `bar`'s offset
+US_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(us::smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(us::smem_addr(bar)), "h"(mask)
         : "memory");
 }
 
@@ -130,18 +154,23 @@ US_DEV void tc_reduce(const UsKParams& p, float* part, int64_t slice_stride, int
     }
 }
 
-template <int ORDER, int NH>
+// CL: CTAs per cluster along M (1 or 2).  A pair of row blocks shares every
+// activation tile: each CTA loads half of it and multicasts it to both, and
+// each CTA's MMA releases the B stage in both, so a CTA reads half the
+// activation bytes from L2.
+template <int ORDER, int NH, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) {
-    constexpr int kBN = TcShape<NH>::kBN, kStages = TcShape<NH>::kStages, kBBytes = TcShape<NH>::kBBytes;
+    using Sh = TcShape<NH>;
+    constexpr int kBN = Sh::kBN, kBStages = Sh::kBStages, kBBytes = Sh::kBBytes, kRing = Sh::kRing;
     const UsKParams& p = tp.p;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled operand tiles
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* a_st = smem;                                   // kStages x 16 KB
-    uint8_t* b_st = a_st + kStages * kABytes;               // kStages x 32 NH KB
-    uint8_t* raw = b_st + kStages * kBBytes;                // kRawStages x 17 KB
-    TcSmem& S = *reinterpret_cast<TcSmem*>(raw + kRawStages * kRawBytes);
+    uint8_t* a_st = smem;                                   // kAStages x 16 KB
+    uint8_t* b_st = a_st + kAStages * kABytes;              // kBStages x 32 NH KB
+    uint8_t* ring = b_st + kBStages * kBBytes;              // raw weights of the K steps in flight
+    TcSmem& S = *reinterpret_cast<TcSmem*>(ring + kRing);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x;                              // 128-row block
@@ -156,20 +185,26 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     const uint32_t idesc = us::umma_idesc_f16(kBM, kBH);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRawStages; ++s) {
+        for (int s = 0; s < kRawSlots; ++s) {
             us::mbar_init(&S.raw_full[s], 1);
-            us::mbar_init(&S.raw_empty[s], kDecWarps);
+            us::mbar_init(&S.raw_empty[s], kGroupWarps);
         }
-        for (int s = 0; s < kStages; ++s) {
-            us::mbar_init(&S.a_full[s], kDecWarps);
+        for (int s = 0; s < kAStages; ++s) {
+            us::mbar_init(&S.a_full[s], kGroupWarps);
+            us::mbar_init(&S.a_empty[s], 1);
+        }
+        for (int s = 0; s < kBStages; ++s) {
             us::mbar_init(&S.b_full[s], 1);
-            us::mbar_init(&S.ab_empty[s], 1);
+            us::mbar_init(&S.b_empty[s], CL);                 // one release per CTA of the cluster
         }
         us::mbar_init(&S.done, 1);
+        S.issued_w = S.issued_x = 0;
         us::fence_mbar_init();
     }
     if (warp == 1) us::tmem_alloc(&S.tmem_base, kBN);
-    __syncthreads();
+    // the peer CTA multicasts into this CTA's stages and barriers: both must be
+    // initialised before either starts
+    if constexpr (CL > 1) us::cluster_sync(); else __syncthreads();
     us::tc_fence_after();
     const uint32_t tmem = S.tmem_base;
     us::pdl_wait();
@@ -177,81 +212,130 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
 
     if (warp == 0) {
         // ------------------------------------------------------- W producer
-        // the warp loads the tile offsets of 32 K steps at once (lane l: step
-        // q + l), so no global load sits on the per-step path; lane 0 issues
-        uint32_t oa[2] = {0u, 0u}, ob[2] = {0u, 0u};
-        for (int q = 0; q < nk; ++q) {
-            const int rs = q % kRawStages;
-            if ((q & 31) == 0 && q + lane < nk) {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q + lane;
-                    oa[h] = p.tile_off[t];
-                    ob[h] = p.tile_off[t + 1];
-                }
-            }
-            bool ok = true;
-            if (q >= kRawStages && lane == 0) ok = us::mbar_wait(&S.raw_empty[rs], ((q / kRawStages) - 1) & 1, p.status);
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
-                failed = true;
-                break;
-            }
-            uint32_t a[2], b[2];
+        // Each K step's two bitmaps and two value runs are packed by their real
+        // length into a byte ring (16-byte aligned), so dense tiles still fit
+        // and sparse ones leave room for more steps in flight.  One thread
+        // places and issues; the next step's tile offsets are loaded one step
+        // ahead.  The ring holds the steps [tail, q) in order, from the start of
+        // step `tail` to `head`, wrapping at kRing.
+        if (lane == 0) {
+            uint32_t na[2], nb[2];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                a[h] = __shfl_sync(0xffffffffu, oa[h], q & 31);
-                b[h] = __shfl_sync(0xffffffffu, ob[h], q & 31);
+                const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0;
+                na[h] = nk > 0 ? p.tile_off[t] : 0u;
+                nb[h] = nk > 0 ? p.tile_off[t + 1] : 0u;
             }
-            if (lane == 0) {
+            uint32_t head = 0;
+            int tail = 0;
+            for (int q = 0; q < nk; ++q) {
+                const int slot = q % kRawSlots;
+                const uint32_t a[2] = {na[0], na[1]}, b[2] = {nb[0], nb[1]};
+                if (q + 1 < nk) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q + 1;
+                        na[h] = p.tile_off[t];
+                        nb[h] = p.tile_off[t + 1];
+                    }
+                }
                 uint32_t vb[2];
+                bool good[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const bool good = b[h] >= a[h] && (b[h] - a[h]) <= 4096u && (a[h] & 7u) == 0 && (b[h] & 7u) == 0 &&
-                                      (uint64_t)b[h] * 2u <= p.values_bytes;
-                    if (!good) us::set_status(p.status, US_ERR_CORRUPT);
-                    vb[h] = good ? (b[h] - a[h]) * 2u : 0u;
-                    S.raw_len[rs][h] = good ? (b[h] - a[h]) : 0u;
+                    good[h] = b[h] >= a[h] && (b[h] - a[h]) <= 4096u && (a[h] & 7u) == 0 && (b[h] & 7u) == 0 &&
+                              (uint64_t)b[h] * 2u <= p.values_bytes;
+                    vb[h] = good[h] ? (b[h] - a[h]) * 2u : 0u;
                 }
-                uint8_t* r = raw + rs * kRawBytes;
-                us::mbar_arrive_expect_tx(&S.raw_full[rs], kRawBm + vb[0] + vb[1]);
+                const uint32_t sz = kRawBm + vb[0] + vb[1];
+                uint32_t place = 0;
+                bool fail = false;
+                for (;;) {
+                    const int inflight = q - tail;
+                    if (inflight == 0) { place = 0; break; }
+                    if (inflight < kRawSlots) {
+                        const uint32_t s0 = S.raw_pos[tail % kRawSlots];
+                        if (head > s0) {
+                            if (head + sz <= (uint32_t)kRing) { place = head; break; }
+                            if (sz <= s0) { place = 0; break; }
+                        } else if (head + sz <= s0) {
+                            place = head;
+                            break;
+                        }
+                    }
+                    if (!us::mbar_wait(&S.raw_empty[tail % kRawSlots], (uint32_t)(tail / kRawSlots) & 1u, p.status)) {
+                        fail = true;
+                        break;
+                    }
+                    ++tail;
+                }
+                if (fail) {
+                    failed = true;
+                    break;
+                }
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (!good[h]) us::set_status(p.status, US_ERR_CORRUPT);
+                    S.raw_len[slot][h] = vb[h] / 2u;
+                }
+                S.raw_pos[slot] = place;
+                uint8_t* r = ring + place;
+                us::mbar_arrive_expect_tx(&S.raw_full[slot], sz);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q;
-                    us::bulk_g2s(r + h * 512, p.bitmap + t * 64, 512, &S.raw_full[rs]);
-                    if (vb[h]) us::bulk_g2s(r + kRawBm + h * 8192, p.values + (uint64_t)a[h] * 2u, vb[h], &S.raw_full[rs]);
+                    us::bulk_g2s(r + h * 512, p.bitmap + t * 64, 512, &S.raw_full[slot]);
+                    if (vb[h])
+                        us::bulk_g2s(r + kRawBm + (h ? vb[0] : 0u), p.values + (uint64_t)a[h] * 2u, vb[h],
+                                     &S.raw_full[slot]);
                 }
+                head = place + sz;
+                S.issued_w = (uint32_t)(q + 1);
             }
-            __syncwarp();
         }
     } else if (warp == 2) {
         // ------------------------------------------------------- X producer
+        const int crank = CL > 1 ? (int)us::cluster_ctarank() : 0;
+        (void)crank;
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
             for (int q = 0; q < nk; ++q) {
-                const int s = q % kStages;
-                if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
+                const int s = q % kBStages;
+                if (q >= kBStages && !us::mbar_wait(&S.b_empty[s], ((q / kBStages) - 1) & 1, p.status)) {
                     failed = true;
                     break;
                 }
                 us::mbar_arrive_expect_tx(&S.b_full[s], (uint32_t)(kHBytes * halves));
-                for (int h = 0; h < halves; ++h)
-                    tma_load_2d(b_st + s * kBBytes + h * kHBytes, &xmap, (kt0 + q) * kBK, nt * kBN + h * kBH,
-                                &S.b_full[s]);
+                if constexpr (CL == 1) {
+                    for (int h = 0; h < halves; ++h)
+                        tma_load_2d(b_st + s * kBBytes + h * kHBytes, &xmap, (kt0 + q) * kBK, nt * kBN + h * kBH,
+                                    &S.b_full[s]);
+                } else if constexpr (NH == 2) {
+                    // CTA r loads token half r (if it holds tokens) into both CTAs
+                    if (crank < halves)
+                        tma_load_2d_mc(b_st + s * kBBytes + crank * kHBytes, &xmap, (kt0 + q) * kBK,
+                                       nt * kBN + crank * kBH, &S.b_full[s], (uint16_t)0x3);
+                } else {
+                    // CTA r loads tokens 128 r .. 128 r + 127 of the 256 (box of 128 rows)
+                    tma_load_2d_mc(b_st + s * kBBytes + crank * (kHBytes / 2), &xmap, (kt0 + q) * kBK,
+                                   nt * kBN + crank * (kBH / 2), &S.b_full[s], (uint16_t)0x3);
+                }
+                S.issued_x = (uint32_t)(q + 1);
             }
         }
     } else if (warp == 1) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
             for (int q = 0; q < nk; ++q) {
-                const int s = q % kStages;
-                if (!us::mbar_wait(&S.a_full[s], (q / kStages) & 1, p.status) ||
-                    !us::mbar_wait(&S.b_full[s], (q / kStages) & 1, p.status)) {
+                const int sa = q % kAStages, sb = q % kBStages;
+                if (!us::mbar_wait(&S.a_full[sa], (q / kAStages) & 1, p.status) ||
+                    !us::mbar_wait(&S.b_full[sb], (q / kBStages) & 1, p.status)) {
                     failed = true;
                     break;
                 }
                 us::tc_fence_after();
-                const uint64_t ad = us::umma_smem_desc_sw128(a_st + s * kABytes);
-                const uint64_t bd = us::umma_smem_desc_sw128(b_st + s * kBBytes);
+                const uint64_t ad = us::umma_smem_desc_sw128(a_st + sa * kABytes);
+                const uint64_t bd = us::umma_smem_desc_sw128(b_st + sb * kBBytes);
                 // K = 16 per MMA: +32 bytes = +2 in the descriptor's address field;
                 // token half h: +32 KB of B, +256 TMEM columns
 #pragma unroll
@@ -259,149 +343,145 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     for (int h = 0; h < halves; ++h)
                         us::umma_f16(tmem + (uint32_t)(h * kBH), ad + 2 * kk, bd + (uint64_t)(h * (kHBytes >> 4)) + 2 * kk,
                                      idesc, (q > 0 || kk > 0) ? 1u : 0u);
-                us::umma_commit(&S.ab_empty[s]);
+                us::umma_commit(&S.a_empty[sa]);
+                if constexpr (CL > 1)
+                    us::umma_commit_mc(&S.b_empty[sb], (uint16_t)0x3);   // both CTAs' loads may reuse it
+                else
+                    us::umma_commit(&S.b_empty[sb]);
             }
             us::umma_commit(&S.done);
         }
     } else {
         // ------------------------------------------------------------ decoders
-        if constexpr (ORDER == US_ORDER_ROW) {
-            const int d = warp - 3;                            // 0..15: rows 8d .. 8d+7
-            const int row = 8 * d + (lane >> 2);               // 0..127 within the block
-            const int qq = lane & 3;                           // which 16 positions of the row
-            const int band_h = row >> 6, i_in_band = row & 63;
-            for (int q = 0; q < nk; ++q) {
-                const int rs = q % kRawStages, s = q % kStages;
-                if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
-                    failed = true;
-                    break;
-                }
-                const uint8_t* r = raw + rs * kRawBytes;
-                const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
-                // row base: popcounts of the earlier rows of this band (warp scan)
-                const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
-                const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
-                uint32_t incl = packed;
-#pragma unroll
-                for (int dd = 1; dd < 32; dd <<= 1) {
-                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
-                    if (lane >= dd) incl += o;
-                }
-                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-                const uint32_t ex = incl - packed;
-                const uint32_t exr = __shfl_sync(0xffffffffu, ex, i_in_band & 31);
-                const uint32_t rowbase = (i_in_band < 32) ? (exr & 0xFFFFu) : (tot & 0xFFFFu) + (exr >> 16);
-                const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
-                const bool ok = P <= S.raw_len[rs][band_h];
-                if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-                const uint64_t word = bm[i_in_band];
-                const uint32_t bits = ok ? (uint32_t)(word >> (16 * qq)) & 0xFFFFu : 0u;
-                uint32_t rank = rowbase + (uint32_t)__popcll(word & ((1ull << (16 * qq)) - 1ull));
-                const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
-                // wait for the A stage to be free (the MMA of step q - kStages finished)
-                if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
-                    failed = true;
-                    break;
-                }
-                uint8_t* arow = a_st + s * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
-    #pragma unroll
-                for (int c = 0; c < 2; ++c) {                  // 8 positions per 16-byte chunk
-                    uint32_t h2[4];
-    #pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const uint32_t b0 = (bits >> (8 * c + j)) & 1u;
-                        const uint32_t b1 = (bits >> (8 * c + j + 1)) & 1u;
-                        const uint32_t v0 = b0 ? run[rank] : 0u;
-                        rank += b0;
-                        const uint32_t v1 = b1 ? run[rank] : 0u;
-                        rank += b1;
-                        h2[j >> 1] = v0 | (v1 << 16);
-                    }
-                    const int chunk = 2 * qq + c;
-                    *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-                }
-                us::fence_proxy_async_smem();                  // generic writes -> visible to the tensor core
-                __syncwarp();
-                if (lane == 0) {
-                    us::mbar_arrive(&S.a_full[s]);
-                    us::mbar_arrive(&S.raw_empty[rs]);
-                }
+        // two groups of eight warps take alternate K steps, so two steps are
+        // decoded at once while the tensor core works on an earlier one; a warp
+        // covers 16 rows of the 128-row A tile
+        const int d = warp - 3;
+        const int grp = d / kGroupWarps, dd = d % kGroupWarps;
+        const int band_h = dd >> 2;                        // 16 dd .. 16 dd + 15 lie in one band
+        for (int q = grp; q < nk; q += kGroups) {
+            const int slot = q % kRawSlots, sa = q % kAStages;
+            if (!us::mbar_wait(&S.raw_full[slot], (q / kRawSlots) & 1, p.status)) {
+                failed = true;
+                break;
             }
-        } else {
-            // COL tiles (Tiled-CBC of "Unified Static-Dynamic Pruning for
-            // Efficient LLM Inference", section 4.1: one bitmap word per column,
-            // the values column after column).  A thread rebuilds 4 adjacent
-            // columns x 4 rows: per column, rank = column base (warp scan of the
-            // band's column popcounts) + popcount of the rows above + running
-            // count; per row it stores the 4 values as one 8-byte piece of the
-            // K-major swizzled A stage - the layout alignment of that page's
-            // section 4.3 done by the decoder's own stores.  Sixteen lanes (one
-            // 4-row group, all 16 column quads) fill 128 bytes of a row per step.
-            const int d = warp - 3;                        // 0..15
-            const int band_h = d >> 3;
-            const int quad = lane & 15;                    // columns 4 quad .. 4 quad + 3
-            const int rg = ((d & 7) << 1) | (lane >> 4);   // rows 4 rg .. 4 rg + 3 of the band
-            for (int q = 0; q < nk; ++q) {
-                const int rs = q % kRawStages, s = q % kStages;
-                if (!us::mbar_wait(&S.raw_full[rs], (q / kRawStages) & 1, p.status)) {
+            const uint8_t* r = ring + S.raw_pos[slot];
+            const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
+            // bases: popcounts of the earlier rows (ROW) or columns (COL) of the
+            // band, one warp scan of packed pairs
+            const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
+            const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
+            uint32_t incl = packed;
+#pragma unroll
+            for (int sh = 1; sh < 32; sh <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xffffffffu, incl, sh);
+                if (lane >= sh) incl += o;
+            }
+            const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+            const uint32_t ex = incl - packed;
+            const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
+            const bool ok = P <= S.raw_len[slot][band_h];
+            if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
+            const uint16_t* run =
+                reinterpret_cast<const uint16_t*>(r + kRawBm + (band_h ? S.raw_len[slot][0] * 2u : 0u));
+            if constexpr (ORDER == US_ORDER_ROW) {
+                // four threads per row (16 positions each), rows i and i + 8:
+                // rank = row base + running popcount, value = run[rank] or 0,
+                // stored as 16-byte chunks at their swizzled place
+                const int qq = lane & 3;
+                uint32_t bits[2], rank[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int ib = ((16 * dd) & 63) + (lane >> 2) + 8 * u;      // row within the band
+                    const uint32_t exr = __shfl_sync(0xffffffffu, ex, ib & 31);
+                    const uint32_t rowbase = (ib < 32) ? (exr & 0xFFFFu) : (tot & 0xFFFFu) + (exr >> 16);
+                    const uint64_t word = bm[ib];
+                    bits[u] = ok ? (uint32_t)(word >> (16 * qq)) & 0xFFFFu : 0u;
+                    rank[u] = rowbase + (uint32_t)__popcll(word & ((1ull << (16 * qq)) - 1ull));
+                }
+                // wait for the A stage to be free (the MMA of step q - kAStages finished)
+                if (q >= kAStages && !us::mbar_wait(&S.a_empty[sa], ((q / kAStages) - 1) & 1, p.status)) {
                     failed = true;
                     break;
                 }
-                const uint8_t* r = raw + rs * kRawBytes;
-                const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
-                const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
-                const uint32_t packed = (uint32_t)__popcll(w0) | ((uint32_t)__popcll(w1) << 16);
-                uint32_t incl = packed;
 #pragma unroll
-                for (int dd = 1; dd < 32; dd <<= 1) {
-                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, dd);
-                    if (lane >= dd) incl += o;
+                for (int u = 0; u < 2; ++u) {
+                    const int row = 16 * dd + (lane >> 2) + 8 * u;    // row & 7 == lane >> 2
+                    uint8_t* arow = a_st + sa * kABytes + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {                 // 8 positions per 16-byte chunk
+                        uint32_t h2[4];
+#pragma unroll
+                        for (int j = 0; j < 8; j += 2) {
+                            const uint32_t b0 = (bits[u] >> (8 * c + j)) & 1u;
+                            const uint32_t b1 = (bits[u] >> (8 * c + j + 1)) & 1u;
+                            const uint32_t v0 = b0 ? run[rank[u]] : 0u;
+                            rank[u] += b0;
+                            const uint32_t v1 = b1 ? run[rank[u]] : 0u;
+                            rank[u] += b1;
+                            h2[j >> 1] = v0 | (v1 << 16);
+                        }
+                        const int chunk = 2 * qq + c;
+                        *reinterpret_cast<uint4*>(arow + ((chunk ^ (row & 7)) << 4)) =
+                            make_uint4(h2[0], h2[1], h2[2], h2[3]);
+                    }
                 }
-                const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-                const uint32_t ex = incl - packed;
-                const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
-                const bool ok = P <= S.raw_len[rs][band_h];
-                if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-                // the four columns' words, bases (lane j % 32 holds column j's) and
-                // first ranks at row 4 rg
-                uint32_t bits[4], rank[4];
-                const uint64_t below = rg ? (~0ull >> (64 - 4 * rg)) : 0ull;
+            } else {
+                // COL tiles (Tiled-CBC of "Unified Static-Dynamic Pruning for
+                // Efficient LLM Inference", section 4.1: one bitmap word per
+                // column, the values column after column).  A thread rebuilds 4
+                // adjacent columns x 4 rows, twice (row groups rg and rg + 2): per
+                // column, rank = column base + popcount of the rows above +
+                // running count; per row it stores the 4 values as one 8-byte
+                // piece of the K-major swizzled A stage - the layout alignment of
+                // that page's section 4.3 done by the decoder's own stores.
+                const int quad = lane & 15;                    // columns 4 quad .. 4 quad + 3
+                uint32_t base[4];
+                uint64_t wc[4];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int j = 4 * quad + c;
                     const uint32_t e = __shfl_sync(0xffffffffu, ex, j & 31);
-                    const uint32_t base = j < 32 ? (e & 0xFFFFu) : (tot & 0xFFFFu) + (e >> 16);
-                    const uint64_t word = ok ? bm[j] : 0ull;
-                    rank[c] = base + (uint32_t)__popcll(word & below);
-                    bits[c] = (uint32_t)(word >> (4 * rg)) & 0xFu;
+                    base[c] = j < 32 ? (e & 0xFFFFu) : (tot & 0xFFFFu) + (e >> 16);
+                    wc[c] = ok ? bm[j] : 0ull;
                 }
-                const uint16_t* run = reinterpret_cast<const uint16_t*>(r + kRawBm + band_h * 8192);
-                if (q >= kStages && !us::mbar_wait(&S.ab_empty[s], ((q / kStages) - 1) & 1, p.status)) {
+                if (q >= kAStages && !us::mbar_wait(&S.a_empty[sa], ((q / kAStages) - 1) & 1, p.status)) {
                     failed = true;
                     break;
                 }
-                // row m = 64 band_h + 4 rg + i: 128 bytes at m * 128, chunk
-                // (4 quad >> 3) ^ (m & 7), half (quad & 1) of it
-                uint8_t* arow = a_st + s * kABytes + (64 * band_h + 4 * rg) * 128 + (quad & 1) * 8;
-                const int m7 = 4 * (rg & 1);                   // (m & 7) - i
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t v[4];
+                for (int u = 0; u < 2; ++u) {
+                    const int rg = 4 * (dd & 3) + (lane >> 4) + 2 * u;    // rows 4 rg .. 4 rg + 3 of the band
+                    const uint64_t below = rg ? (~0ull >> (64 - 4 * rg)) : 0ull;
+                    uint32_t bits[4], rank[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        const uint32_t b = (bits[c] >> i) & 1u;
-                        v[c] = b ? run[rank[c]] : 0u;
-                        rank[c] += b;
+                        rank[c] = base[c] + (uint32_t)__popcll(wc[c] & below);
+                        bits[c] = (uint32_t)(wc[c] >> (4 * rg)) & 0xFu;
                     }
-                    *reinterpret_cast<uint2*>(arow + i * 128 + (((quad >> 1) ^ (m7 + i)) << 4)) =
-                        make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+                    // row m = 64 band_h + 4 rg + i: 128 bytes at m * 128, chunk
+                    // (4 quad >> 3) ^ (m & 7), half (quad & 1) of it
+                    uint8_t* arow = a_st + sa * kABytes + (64 * band_h + 4 * rg) * 128 + (quad & 1) * 8;
+                    const int m7 = 4 * (rg & 1);               // (m & 7) - i
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint32_t v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t bb = (bits[c] >> i) & 1u;
+                            v[c] = bb ? run[rank[c]] : 0u;
+                            rank[c] += bb;
+                        }
+                        *reinterpret_cast<uint2*>(arow + i * 128 + (((quad >> 1) ^ (m7 + i)) << 4)) =
+                            make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+                    }
                 }
-                us::fence_proxy_async_smem();              // generic writes -> visible to the tensor core
-                __syncwarp();
-                if (lane == 0) {
-                    us::mbar_arrive(&S.a_full[s]);
-                    us::mbar_arrive(&S.raw_empty[rs]);
-                }
+            }
+            us::fence_proxy_async_smem();                  // generic writes -> visible to the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                us::mbar_arrive(&S.a_full[sa]);
+                us::mbar_arrive(&S.raw_empty[slot]);
             }
         }
     }
@@ -410,11 +490,13 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     __syncthreads();
     const bool any_failed = __syncthreads_or(failed);
     if (any_failed && warp == 0 && lane == 0) {
-        // let this CTA's copies still in flight land (bounded) before it exits
-        for (int q = nk > kRawStages ? nk - kRawStages : 0; q < nk; ++q)
-            us::mbar_wait(&S.raw_full[q % kRawStages], (q / kRawStages) & 1, nullptr);
-        for (int q = nk > kStages ? nk - kStages : 0; q < nk; ++q)
-            us::mbar_wait(&S.b_full[q % kStages], (q / kStages) & 1, nullptr);
+        // let this CTA's copies still in flight land (bounded) before it exits:
+        // the last issued step of each slot / stage
+        const int iw = (int)S.issued_w, ix = (int)S.issued_x;
+        for (int q = iw > kRawSlots ? iw - kRawSlots : 0; q < iw; ++q)
+            us::mbar_wait(&S.raw_full[q % kRawSlots], (q / kRawSlots) & 1, nullptr);
+        for (int q = ix > kBStages ? ix - kBStages : 0; q < ix; ++q)
+            us::mbar_wait(&S.b_full[q % kBStages], (q / kBStages) & 1, nullptr);
     }
     if (warp >= 3 && warp < 3 + 4 * halves) {
         // the final commit also covers MMAs issued before a failure: wait for it (bounded)
@@ -449,6 +531,9 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     }
     us::tc_fence_before();
     __syncthreads();
+    // no CTA leaves while its MMAs' releases may still arrive at the peer's
+    // barriers, or the peer's copies at its own stages
+    if constexpr (CL > 1) us::cluster_sync();
     if (warp == 1) us::tmem_dealloc(tmem, kBN);
     if (p.split > 1 && !any_failed) {
         __threadfence();
@@ -517,27 +602,44 @@ size_t tc_ws(int M, int N, int split) {
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     auto enc = encode_fn();
     if (!enc) return US_ERR_CUDA;
+    if (p.tok_block != kBH && p.tok_block != 2 * kBH) return US_ERR_INVALID_ARG;
+    const bool two = p.tok_block == 2 * kBH;
+    // pairs of row blocks share their activation tiles when the count is even
+    const bool pair = (p.M / kBM) % 2 == 0;
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)p.K, (cuuint64_t)p.N};
     const cuuint64_t gstride[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBH};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)(pair && !two ? kBH / 2 : kBH)};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(p.X), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return US_ERR_CUDA;
-    if (p.tok_block != kBH && p.tok_block != 2 * kBH) return US_ERR_INVALID_ARG;
-    const bool two = p.tok_block == 2 * kBH;
     TcParams tp;
     tp.p = p;
     tp.n_tiles = (p.N + p.tok_block - 1) / p.tok_block;
-    auto kern = two ? (p.order == US_ORDER_COL ? spmm_f16_tc_kernel<US_ORDER_COL, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 2>)
-                    : (p.order == US_ORDER_COL ? spmm_f16_tc_kernel<US_ORDER_COL, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 1>);
+    const bool col = p.order == US_ORDER_COL;
+    void (*kern)(const TcParams, const CUtensorMap) =
+        two ? (pair ? (col ? spmm_f16_tc_kernel<US_ORDER_COL, 2, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 2, 2>)
+                    : (col ? spmm_f16_tc_kernel<US_ORDER_COL, 2, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 2, 1>))
+            : (pair ? (col ? spmm_f16_tc_kernel<US_ORDER_COL, 1, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 1, 2>)
+                    : (col ? spmm_f16_tc_kernel<US_ORDER_COL, 1, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 1, 1>));
     const size_t smem = two ? TcShape<2>::kSmem : TcShape<1>::kSmem;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
-    dim3 grid((unsigned)(p.M / kBM), (unsigned)(tp.n_tiles * p.split));
-    kern<<<grid, kThreads, smem, st>>>(tp, map);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.M / kBM), (unsigned)(tp.n_tiles * p.split));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pair ? 2 : 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tp, map) != cudaSuccess) return US_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }
 
