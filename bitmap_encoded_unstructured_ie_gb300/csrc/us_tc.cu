@@ -14,9 +14,9 @@
 // (NH = 1 or 2 halves of 256 tokens; with two, every decoded A tile feeds twice
 // as many tokens):
 //  * warp 0 (W producer): 1-D bulk copies of both 64-row bands' bitmap words
-//    and value runs for each 64-column K step, packed by their real length into
-//    a byte ring (up to eight K steps in flight), the next step's tile
-//    offsets loaded one step ahead;
+//    and value runs for chunks of two 64-column K steps (a band's consecutive
+//    tiles are contiguous), packed by their real length into a byte ring (up to
+//    eight chunks in flight), the next chunk's tile offsets loaded one ahead;
 //  * warp 2 (X producer): 2-D TMA tile loads (128-byte swizzle, zero fill past
 //    N) of the matching 256 x 64 activation blocks into the B stage, one per
 //    token half that holds tokens;
@@ -48,7 +48,8 @@ constexpr int kBH = 256;                 // tokens per MMA (one token half)
 constexpr int kBK = 64;                  // K per step (one bitmap tile column)
 constexpr int kAStages = 3;              // decoded A stages
 constexpr int kMaxBStages = 3;           // activation stages, at most
-constexpr int kRawSlots = 8;             // K steps whose raw weights may be in flight
+constexpr int kC = 2;                    // K steps per raw chunk (one placement, one barrier)
+constexpr int kRawSlots = 8;             // raw chunks that may be in flight
 constexpr int kGroups = 2;               // decoder groups, on alternate K steps
 constexpr int kGroupWarps = 8;           // warps per decoder group
 constexpr int kDecWarps = kGroups * kGroupWarps;
@@ -56,8 +57,8 @@ constexpr int kThreads = 32 * (3 + kDecWarps);
 constexpr int kABytes = kBM * kBK * 2;           // 16 KB
 constexpr int kHBytes = kBH * kBK * 2;           // 32 KB per token half
 constexpr int kRawBm = 2 * 512;                  // two bands' bitmaps (64x64 tiles)
-constexpr int kRawMax = kRawBm + 2 * 64 * 64 * 2;   // one K step's raw weights, worst case (17 KB)
-constexpr int kHeader = 512;
+constexpr int kRawMax = kC * (kRawBm + 2 * 64 * 64 * 2);   // one chunk's raw weights, worst case (34 KB)
+constexpr int kHeader = 1024;
 constexpr size_t kSmemCap = 232448;              // dynamic shared memory per CTA
 
 // tile shape for NH token halves; the raw ring takes what the stages leave
@@ -70,7 +71,7 @@ struct TcShape {
     static constexpr size_t kRingAll = kSmemCap - kFixed;
     static constexpr int kRing = (int)((kRingAll > 65536 ? 65536 : kRingAll) & ~size_t(15));
     static constexpr size_t kSmem = kFixed + (size_t)kRing;
-    static_assert(kRing >= 2 * kRawMax, "the raw ring holds two worst-case K steps");
+    static_assert(kRing >= kRawMax, "the raw ring holds a worst-case chunk");
     static_assert(kSmem <= kSmemCap, "shared memory per CTA");
 };
 
@@ -80,8 +81,10 @@ struct TcSmem {
     uint64_t b_full[kMaxBStages], b_empty[kMaxBStages];
     uint64_t done;
     uint32_t tmem_base;
-    uint32_t raw_pos[kRawSlots];         // ring offset of the K step in slot s
-    uint32_t raw_len[kRawSlots][2];      // run length (elements) of each band's tile
+    uint32_t raw_pos[kRawSlots];         // ring offset of the chunk in slot s
+    uint32_t raw_vb0[kRawSlots];         // bytes of band 0's value runs in the chunk
+    uint32_t raw_off[kRawSlots][2][kC];  // a tile's run start within its band's runs (elements)
+    uint32_t raw_len[kRawSlots][2][kC];  // a tile's run length (elements)
     uint32_t issued_w, issued_x;         // K steps whose copies were issued
     uint32_t flag;
 };
@@ -187,7 +190,7 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kRawSlots; ++s) {
             us::mbar_init(&S.raw_full[s], 1);
-            us::mbar_init(&S.raw_empty[s], kGroupWarps);
+            us::mbar_init(&S.raw_empty[s], kC * kGroupWarps);   // every step of the chunk
         }
         for (int s = 0; s < kAStages; ++s) {
             us::mbar_init(&S.a_full[s], kGroupWarps);
@@ -212,46 +215,51 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
 
     if (warp == 0) {
         // ------------------------------------------------------- W producer
-        // Each K step's two bitmaps and two value runs are packed by their real
-        // length into a byte ring (16-byte aligned), so dense tiles still fit
-        // and sparse ones leave room for more steps in flight.  One thread
-        // places and issues; the next step's tile offsets are loaded one step
-        // ahead.  The ring holds the steps [tail, q) in order, from the start of
-        // step `tail` to `head`, wrapping at kRing.
+        // Chunks of kC consecutive K steps: a band's tiles are consecutive in
+        // the bitmap and in the value array, so a chunk is four bulk copies
+        // (each band's bitmaps, each band's value runs), packed by real length
+        // into a byte ring (16-byte aligned).  One thread places and issues;
+        // the next chunk's tile offsets are loaded one chunk ahead.  The ring
+        // holds the chunks [tail, c) in order, from the start of chunk `tail`
+        // to `head`, wrapping at kRing.
         if (lane == 0) {
-            uint32_t na[2], nb[2];
+            const int nch = (nk + kC - 1) / kC;
+            uint32_t no[2][kC + 1];
+            auto load_offs = [&](int c) {
+                const int q0 = c * kC, cnt = min(kC, nk - q0);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0;
-                na[h] = nk > 0 ? p.tile_off[t] : 0u;
-                nb[h] = nk > 0 ? p.tile_off[t + 1] : 0u;
-            }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j <= kC; ++j)
+                        no[h][j] = p.tile_off[(int64_t)(band0 + h) * p.nTK + kt0 + q0 + min(j, cnt)];
+            };
+            if (nch > 0) load_offs(0);
             uint32_t head = 0;
             int tail = 0;
-            for (int q = 0; q < nk; ++q) {
-                const int slot = q % kRawSlots;
-                const uint32_t a[2] = {na[0], na[1]}, b[2] = {nb[0], nb[1]};
-                if (q + 1 < nk) {
+            for (int c = 0; c < nch; ++c) {
+                const int slot = c % kRawSlots, q0 = c * kC, cnt = min(kC, nk - q0);
+                uint32_t o[2][kC + 1];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q + 1;
-                        na[h] = p.tile_off[t];
-                        nb[h] = p.tile_off[t + 1];
-                    }
-                }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int j = 0; j <= kC; ++j) o[h][j] = no[h][j];
+                if (c + 1 < nch) load_offs(c + 1);
                 uint32_t vb[2];
                 bool good[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    good[h] = b[h] >= a[h] && (b[h] - a[h]) <= 4096u && (a[h] & 7u) == 0 && (b[h] & 7u) == 0 &&
-                              (uint64_t)b[h] * 2u <= p.values_bytes;
-                    vb[h] = good[h] ? (b[h] - a[h]) * 2u : 0u;
+                    good[h] = (o[h][0] & 7u) == 0 && (uint64_t)o[h][kC] * 2u <= p.values_bytes;
+#pragma unroll
+                    for (int j = 0; j < kC; ++j)
+                        good[h] = good[h] && o[h][j + 1] >= o[h][j] && (o[h][j + 1] - o[h][j]) <= 4096u &&
+                                  (o[h][j + 1] & 7u) == 0;
+                    vb[h] = good[h] ? (o[h][kC] - o[h][0]) * 2u : 0u;
                 }
-                const uint32_t sz = kRawBm + vb[0] + vb[1];
+                const uint32_t sz = (uint32_t)cnt * kRawBm + vb[0] + vb[1];
                 uint32_t place = 0;
                 bool fail = false;
                 for (;;) {
-                    const int inflight = q - tail;
+                    const int inflight = c - tail;
                     if (inflight == 0) { place = 0; break; }
                     if (inflight < kRawSlots) {
                         const uint32_t s0 = S.raw_pos[tail % kRawSlots];
@@ -276,21 +284,28 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (!good[h]) us::set_status(p.status, US_ERR_CORRUPT);
-                    S.raw_len[slot][h] = vb[h] / 2u;
+#pragma unroll
+                    for (int j = 0; j < kC; ++j) {
+                        S.raw_off[slot][h][j] = good[h] ? o[h][j] - o[h][0] : 0u;
+                        S.raw_len[slot][h][j] = good[h] ? o[h][j + 1] - o[h][j] : 0u;
+                    }
                 }
+                S.raw_vb0[slot] = vb[0];
                 S.raw_pos[slot] = place;
                 uint8_t* r = ring + place;
                 us::mbar_arrive_expect_tx(&S.raw_full[slot], sz);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q;
-                    us::bulk_g2s(r + h * 512, p.bitmap + t * 64, 512, &S.raw_full[slot]);
+                    const int64_t t = (int64_t)(band0 + h) * p.nTK + kt0 + q0;
+                    us::bulk_g2s(r + h * cnt * 512, p.bitmap + t * 64, (uint32_t)cnt * 512u, &S.raw_full[slot]);
                     if (vb[h])
-                        us::bulk_g2s(r + kRawBm + (h ? vb[0] : 0u), p.values + (uint64_t)a[h] * 2u, vb[h],
+                        us::bulk_g2s(r + 2 * cnt * 512 + (h ? vb[0] : 0u), p.values + (uint64_t)o[h][0] * 2u, vb[h],
                                      &S.raw_full[slot]);
                 }
+                // a short last chunk: arrive for the steps it does not have
+                if (cnt < kC) us::mbar_arrive_n(&S.raw_empty[slot], (uint32_t)((kC - cnt) * kGroupWarps));
                 head = place + sz;
-                S.issued_w = (uint32_t)(q + 1);
+                S.issued_w = (uint32_t)(c + 1);
             }
         }
     } else if (warp == 2) {
@@ -360,13 +375,14 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         const int grp = d / kGroupWarps, dd = d % kGroupWarps;
         const int band_h = dd >> 2;                        // 16 dd .. 16 dd + 15 lie in one band
         for (int q = grp; q < nk; q += kGroups) {
-            const int slot = q % kRawSlots, sa = q % kAStages;
-            if (!us::mbar_wait(&S.raw_full[slot], (q / kRawSlots) & 1, p.status)) {
+            const int ch = q / kC, jj = q % kC, slot = ch % kRawSlots, sa = q % kAStages;
+            const int cnt = min(kC, nk - ch * kC);
+            if (!us::mbar_wait(&S.raw_full[slot], (ch / kRawSlots) & 1, p.status)) {
                 failed = true;
                 break;
             }
             const uint8_t* r = ring + S.raw_pos[slot];
-            const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + band_h * 512);
+            const uint64_t* bm = reinterpret_cast<const uint64_t*>(r + (band_h * cnt + jj) * 512);
             // bases: popcounts of the earlier rows (ROW) or columns (COL) of the
             // band, one warp scan of packed pairs
             const uint64_t w0 = bm[lane], w1 = bm[lane + 32];
@@ -380,10 +396,10 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
             const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
             const uint32_t ex = incl - packed;
             const uint32_t P = (tot & 0xFFFFu) + (tot >> 16);
-            const bool ok = P <= S.raw_len[slot][band_h];
+            const bool ok = P <= S.raw_len[slot][band_h][jj];
             if (!ok && lane == 0) us::set_status(p.status, US_ERR_CORRUPT);
-            const uint16_t* run =
-                reinterpret_cast<const uint16_t*>(r + kRawBm + (band_h ? S.raw_len[slot][0] * 2u : 0u));
+            const uint16_t* run = reinterpret_cast<const uint16_t*>(
+                r + 2 * cnt * 512 + (band_h ? S.raw_vb0[slot] : 0u) + S.raw_off[slot][band_h][jj] * 2u);
             if constexpr (ORDER == US_ORDER_ROW) {
                 // four threads per row (16 positions each), rows i and i + 8:
                 // rank = row base + running popcount, value = run[rank] or 0,
@@ -493,8 +509,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         // let this CTA's copies still in flight land (bounded) before it exits:
         // the last issued step of each slot / stage
         const int iw = (int)S.issued_w, ix = (int)S.issued_x;
-        for (int q = iw > kRawSlots ? iw - kRawSlots : 0; q < iw; ++q)
-            us::mbar_wait(&S.raw_full[q % kRawSlots], (q / kRawSlots) & 1, nullptr);
+        for (int c = iw > kRawSlots ? iw - kRawSlots : 0; c < iw; ++c)
+            us::mbar_wait(&S.raw_full[c % kRawSlots], (c / kRawSlots) & 1, nullptr);
         for (int q = ix > kBStages ? ix - kBStages : 0; q < ix; ++q)
             us::mbar_wait(&S.b_full[q % kBStages], (q / kBStages) & 1, nullptr);
     }
