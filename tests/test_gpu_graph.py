@@ -32,7 +32,8 @@ def orc():
     return o
 
 
-@pytest.mark.parametrize("M,K,N", [(1024, 2048, 1), (1024, 2048, 8), (1024, 2048, 16), (704, 1536, 5)])
+@pytest.mark.parametrize("M,K,N", [(1024, 2048, 1), (1024, 2048, 8), (1024, 2048, 16), (704, 1536, 5),
+                                   (11008, 4096, 1), (11008, 4096, 3)])
 def test_w4a4_graph_of_static_launches(us, orc, M, K, N):
     dev = "cuda"
     # four distinct weight matrices, launched in turn, each writing its own output

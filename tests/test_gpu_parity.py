@@ -456,7 +456,7 @@ def test_w4a4_ffn_full(us, orc, M, K, static):
     slots, so some are decoded before the dependency wait and the rest after."""
     d = wl.w4a4(M, K, 32, 0.5, seed=0, rows="beta")
     E = encode_gpu(us, d["Wq"], 64, 64, I4, ROW)
-    for N in (1, 4, 16, 32):
+    for N in (1, 3, 4, 16, 32):
         acc, y = run_w4a4(us, E, wl.pack_int4(d["Xq"][:N]), d["s_w"], d["s_x"][:N], N, static=static)
         rng = np.random.default_rng(N)
         n_idx = rng.integers(0, N, 3000)
