@@ -29,8 +29,8 @@
 //    "A full" barrier (COL tiles: 4 columns x 4 rows per thread, twice);
 //  * warp 1 (MMA): allocates 256 NH TMEM columns; one thread issues four
 //    tcgen05.mma kind::f16 (M=128, N=256, K=16) per K step and token half, the
-//    halves into adjacent 256-column fp32 accumulators, and commits to the A
-//    and B stages' "empty" barriers;
+//    halves into adjacent 256-column fp32 accumulators, and commits once per
+//    K step to that step's "done" barrier, which frees its A and B stages;
 //  * warps 3 .. 3+4NH-1 (epilogue): tcgen05.ld the accumulators (one TMEM lane
 //    per output row, one warp per lane quarter and token half) and write fp16
 //    outputs, or, under split-K, fp32 partials that the last CTA of the tile
@@ -47,6 +47,7 @@ constexpr int kBM = 128;                 // output rows per CTA (two 64-row band
 constexpr int kBH = 256;                 // tokens per MMA (one token half)
 constexpr int kBK = 64;                  // K per step (one bitmap tile column)
 constexpr int kAStages = 3;              // decoded A stages
+constexpr int kSD = 6;                   // "MMAs of step q done" barriers (a multiple of the stage counts)
 constexpr int kMaxBStages = 3;           // activation stages, at most
 constexpr int kC = 2;                    // K steps per raw chunk (one placement, one barrier)
 constexpr int kRawSlots = 8;             // raw chunks that may be in flight
@@ -77,8 +78,8 @@ struct TcShape {
 
 struct TcSmem {
     uint64_t raw_full[kRawSlots], raw_empty[kRawSlots];
-    uint64_t a_full[kAStages], a_empty[kAStages];
-    uint64_t b_full[kMaxBStages], b_empty[kMaxBStages];
+    uint64_t a_full[kAStages], b_full[kMaxBStages];
+    uint64_t sdone[kSD];                 // step q's MMAs finished: its A and B stages are free
     uint64_t done;
     uint32_t tmem_base;
     uint32_t raw_pos[kRawSlots];         // ring offset of the chunk in slot s
@@ -192,14 +193,9 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
             us::mbar_init(&S.raw_full[s], 1);
             us::mbar_init(&S.raw_empty[s], kC * kGroupWarps);   // every step of the chunk
         }
-        for (int s = 0; s < kAStages; ++s) {
-            us::mbar_init(&S.a_full[s], kGroupWarps);
-            us::mbar_init(&S.a_empty[s], 1);
-        }
-        for (int s = 0; s < kBStages; ++s) {
-            us::mbar_init(&S.b_full[s], 1);
-            us::mbar_init(&S.b_empty[s], CL);                 // one release per CTA of the cluster
-        }
+        for (int s = 0; s < kAStages; ++s) us::mbar_init(&S.a_full[s], kGroupWarps);
+        for (int s = 0; s < kBStages; ++s) us::mbar_init(&S.b_full[s], 1);
+        for (int s = 0; s < kSD; ++s) us::mbar_init(&S.sdone[s], CL);   // one release per CTA of the cluster
         us::mbar_init(&S.done, 1);
         S.issued_w = S.issued_x = 0;
         us::fence_mbar_init();
@@ -316,7 +312,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
             for (int q = 0; q < nk; ++q) {
                 const int s = q % kBStages;
-                if (q >= kBStages && !us::mbar_wait(&S.b_empty[s], ((q / kBStages) - 1) & 1, p.status)) {
+                if (q >= kBStages &&
+                    !us::mbar_wait(&S.sdone[(q - kBStages) % kSD], ((q - kBStages) / kSD) & 1, p.status)) {
                     failed = true;
                     break;
                 }
@@ -358,11 +355,12 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     for (int h = 0; h < halves; ++h)
                         us::umma_f16(tmem + (uint32_t)(h * kBH), ad + 2 * kk, bd + (uint64_t)(h * (kHBytes >> 4)) + 2 * kk,
                                      idesc, (q > 0 || kk > 0) ? 1u : 0u);
-                us::umma_commit(&S.a_empty[sa]);
+                // one release for both stages (in both CTAs of a pair: the B stage
+                // is reloaded by both)
                 if constexpr (CL > 1)
-                    us::umma_commit_mc(&S.b_empty[sb], (uint16_t)0x3);   // both CTAs' loads may reuse it
+                    us::umma_commit_mc(&S.sdone[q % kSD], (uint16_t)0x3);
                 else
-                    us::umma_commit(&S.b_empty[sb]);
+                    us::umma_commit(&S.sdone[q % kSD]);
             }
             us::umma_commit(&S.done);
         }
@@ -416,7 +414,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     rank[u] = rowbase + (uint32_t)__popcll(word & ((1ull << (16 * qq)) - 1ull));
                 }
                 // wait for the A stage to be free (the MMA of step q - kAStages finished)
-                if (q >= kAStages && !us::mbar_wait(&S.a_empty[sa], ((q / kAStages) - 1) & 1, p.status)) {
+                if (q >= kAStages &&
+                    !us::mbar_wait(&S.sdone[(q - kAStages) % kSD], ((q - kAStages) / kSD) & 1, p.status)) {
                     failed = true;
                     break;
                 }
@@ -461,7 +460,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     base[c] = j < 32 ? (e & 0xFFFFu) : (tot & 0xFFFFu) + (e >> 16);
                     wc[c] = ok ? bm[j] : 0ull;
                 }
-                if (q >= kAStages && !us::mbar_wait(&S.a_empty[sa], ((q / kAStages) - 1) & 1, p.status)) {
+                if (q >= kAStages &&
+                    !us::mbar_wait(&S.sdone[(q - kAStages) % kSD], ((q - kAStages) / kSD) & 1, p.status)) {
                     failed = true;
                     break;
                 }
