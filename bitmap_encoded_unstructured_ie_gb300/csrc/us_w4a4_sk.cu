@@ -44,7 +44,7 @@ constexpr int kR = 16;                      // chunks in flight at most (mbarrie
 // Consumer warps: as many as two CTAs per SM can hold with every accumulator
 // in registers.
 __host__ __device__ constexpr int nw_for(int N, int NT) {
-    return NT ? (NT == 1 ? 12 : (NT == 2 ? 10 : 6)) : (N == 1 ? 16 : (N <= 3 ? 12 : 8));
+    return NT ? (NT == 1 ? 14 : (NT == 2 ? 10 : 6)) : (N == 1 ? 16 : (N <= 3 ? 14 : 12));
 }
 // consumer warps, then the weight producer warp, then the activation warp
 __host__ __device__ constexpr int threads_for(int N, int NT) { return (nw_for(N, NT) + 2) * 32; }
