@@ -32,15 +32,19 @@ def orc():
     return o
 
 
-@pytest.mark.parametrize("M,K,N", [(1024, 2048, 1), (1024, 2048, 8), (1024, 2048, 16), (704, 1536, 5),
-                                   (11008, 4096, 1), (11008, 4096, 3)])
-def test_w4a4_graph_of_static_launches(us, orc, M, K, N):
+@pytest.mark.parametrize("M,K,N,bits", [(1024, 2048, 1, 4), (1024, 2048, 8, 4), (1024, 2048, 16, 4), (704, 1536, 5, 4),
+                                        (11008, 4096, 1, 4), (11008, 4096, 3, 4), (1024, 2048, 3, 2),
+                                        (1024, 2048, 16, 2)])
+def test_w4a4_graph_of_static_launches(us, orc, M, K, N, bits):
     dev = "cuda"
-    # four distinct weight matrices, launched in turn, each writing its own output
-    mats = [wl.w4a4(M, K, N, 0.5, seed=10 + i) for i in range(4)]
+    # four distinct weight matrices (int4, or int2 for W2A4), launched in turn,
+    # each writing its own output
+    gen = wl.w4a4 if bits == 4 else wl.w2a4
+    mats = [gen(M, K, N, 0.5, seed=10 + i) for i in range(4)]
     Es = []
     for d in mats:
-        E = us.us_encode(torch.from_numpy(d["Wq"]).to(dev), 64, 64, us.US_I4, us.US_ORDER_ROW)
+        E = us.us_encode(torch.from_numpy(d["Wq"]).to(dev), 64, 64, us.US_I4 if bits == 4 else us.US_I2,
+                         us.US_ORDER_ROW)
         E.flags = us.US_BITMAP_STATIC
         Es.append(E)
     X = torch.from_numpy(mats[0]["Xq_packed"]).to(dev)
