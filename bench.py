@@ -531,6 +531,23 @@ def measure_extras(us, torch, wl, dev, stream):
         fl = 2 * 4096 * 4096 * N
         pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
     out["prefill_f16_4096_s60"] = pf
+    # fp16 decode 4096^2, 50 % sparsity, N = 1 / 8 / 16 / 32 (mma.sync decode
+    # kernel); rotating weight copies so every launch reads from HBM
+    fd = wl.f16_spmm(4096, 4096, 32, 0.5, seed=1)
+    Eg = us.us_encode(torch.from_numpy(fd["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_ROW)
+    ng = max(2, math.ceil(2.2 * l2 / Eg.nbytes()))
+    cpg = [Eg] + [us.Encoded(Eg.M, Eg.K, Eg.TM, Eg.TK, Eg.elem, Eg.order, Eg.bitmap.clone(), Eg.tile_off.clone(),
+                             Eg.values.clone(), Eg.values_bytes) for _ in range(ng - 1)]
+    Xg = torch.from_numpy(fd["X"].view(np.int16)).to(dev)
+    dec = {"copies": ng}
+    for N in (1, 8, 16, 32):
+        Yg = torch.empty(N, 4096, dtype=torch.int16, device=dev)
+        wsg = us.workspace(us.US_OP_SPMM_F16, Eg, N)
+        ms = time_graph(torch, stream, us, lambda: [us.us_spmm_f16(E, Xg[:N], N, Yg, wsg, 0, stream) for E in cpg])
+        t = ms * 1e3 / ng
+        byt = Eg.nbytes() + 2 * N * 4096 * 2
+        dec[str(N)] = {"us_per_call": round(t, 3), "bytes": byt, "GB/s": round(byt / (t * 1e-6) / 1e9, 1)}
+    out["decode_f16_4096_s50"] = dec
     # the same on COL tiles: the format spMspV reads serves prefill too
     Efc = us.us_encode(torch.from_numpy(f["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_COL)
     pfc = {}

@@ -101,6 +101,7 @@ struct Plan {
     bool sk;        // W4A4 CUDA-core kernel over a balanced partition of the tiles
     bool fast;      // W4A4 register-decode kernel
     bool tc;        // fp16 tensor-core kernel
+    bool dec;       // fp16 decode kernel (1-63 tokens, mma.sync)
     int split;
     int tok_block;
     size_t ws;
@@ -127,6 +128,14 @@ Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
         return pl;
     }
     const int nTM = W->M / W->TM, nTK = W->K / W->TK;
+    if (op == US_OP_SPMM_F16 && us::f16_dec_supported(W->TM, W->TK, W->order, N) &&
+        (split_k == 0 || us::f16_dec_fits(nTK, split_k, N))) {
+        pl.dec = true;
+        pl.tok_block = us::f16_dec_tok_block(N);
+        pl.split = split_k > 0 ? split_k : us::f16_dec_split(nTM, nTK, N);
+        pl.ws = us::spmm_generic_ws(W->M, W->TM, N, pl.split, pl.tok_block);
+        return pl;
+    }
     pl.fast = (op == US_OP_SPMM_W4A4) && W->elem == US_I4 && us::w4a4_fast_supported(W->TM, W->TK, N) &&
               split_k <= us::w4a4_fast_max_split();
     pl.tok_block = pl.fast ? us::w4a4_fast_tok_block(N) : us::spmm_generic_tok_block(N);
@@ -297,6 +306,7 @@ us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
         return us::launch_tc_f16(p, static_cast<cudaStream_t>(stream));
     }
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
+    if (pl.dec) return us::launch_f16_dec(p, static_cast<cudaStream_t>(stream));
     return us::launch_spmm_generic(p, US_F16, static_cast<cudaStream_t>(stream));
 }
 
@@ -351,7 +361,8 @@ us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint
     if (cudaMemsetAsync(scratch, 0, cbytes, st) != cudaSuccess) return US_ERR_CUDA;
     p.counters = reinterpret_cast<unsigned*>(scratch);
     p.ws = scratch + cbytes;
-    return pl.tc ? us::launch_tc_f16(p, st) : us::launch_spmm_generic(p, US_F16, st);
+    if (pl.tc) return us::launch_tc_f16(p, st);
+    return pl.dec ? us::launch_f16_dec(p, st) : us::launch_spmm_generic(p, US_F16, st);
 }
 
 us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16_t* y, void* ws, size_t ws_bytes,

@@ -4,6 +4,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include "../../include/us.h"
 
@@ -44,6 +45,15 @@ int tc_tok_block(int N);
 int tc_split(int M, int N, int nTK);
 size_t tc_ws(int M, int N, int split);
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
+// the driver's cuTensorMapEncodeTiled (nullptr if the driver lacks it)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// fp16 SpMM for 1-63 tokens on 64 x 64 row-scan tiles (us_f16_dec.cu)
+bool f16_dec_supported(int TM, int TK, int order, int N);
+int f16_dec_tok_block(int N);
+bool f16_dec_fits(int nTK, int split, int N);
+int f16_dec_split(int nTM, int nTK, int N);
+us_status launch_f16_dec(const UsKParams& p, cudaStream_t st);
 
 
 // spMspV (us_spmspv.cu)

@@ -575,7 +575,12 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+namespace us {
+
+// the driver's tiled tensor-map encoder, looked up once
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         void* ptr = nullptr;
@@ -587,10 +592,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     }
     return fn;
 }
-
-}  // namespace
-
-namespace us {
 
 bool tc_f16_supported(int TM, int TK, int M, int N) {
     return TM == 64 && TK == 64 && M % kBM == 0 && N >= 64;
@@ -616,7 +617,7 @@ size_t tc_ws(int M, int N, int split) {
 }
 
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
-    auto enc = encode_fn();
+    auto enc = tensor_map_encoder();
     if (!enc) return US_ERR_CUDA;
     if (p.tok_block != kBH && p.tok_block != 2 * kBH) return US_ERR_INVALID_ARG;
     const bool two = p.tok_block == 2 * kBH;

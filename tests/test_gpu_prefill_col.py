@@ -1,13 +1,17 @@
 """One format for prefill and decode: us_spmm_f16 on COL-order tiles (the
 Tiled-CBC layout that spMspV reads), through the C ABI, against the oracle.
 
-Both scan orders decode to the same dense operand, and the kernels sum it in
-the same order, so a matrix encoded ROW and COL must give bit-identical
-outputs. Each must also be within the fp16 bar of the fp64 oracle: relative
+Where both scan orders run the same kernel (the tensor-core path: 64 x 64
+tiles, N >= 64; the generic CUDA-core path: other tile shapes) they decode to
+the same dense operand and sum it in the same order, so a matrix encoded ROW
+and COL must give bit-identical outputs. For 64 x 64 tiles and N < 64, ROW
+tiles take the mma.sync decode kernel and COL tiles the generic one, whose
+fp32 sums run in another order: there each is held to the oracle on its own.
+Every output must be within the fp16 bar of the fp64 oracle: relative
 L2 <= 1e-3, max-abs <= 2e-2.
 
 Cases cover the tensor-core path (64 x 64 tiles, N >= 64, with and without
-split-K, ragged token tiles) and the CUDA-core path (any tile, any N).
+split-K, ragged token tiles) and the CUDA-core paths (any tile, any N).
 """
 import numpy as np
 import pytest
@@ -62,8 +66,8 @@ CASES = [
     (384, 512, 64, 64, 300, 0.6, 0),      # tensor cores, a ragged second token tile
     (256, 2048, 64, 64, 128, 0.5, 4),     # tensor cores, split-K
     (256, 512, 64, 64, 700, 0.5, 2),      # tensor cores, 512-token tiles, split-K, ragged
-    (128, 768, 64, 64, 1, 0.5, 0),        # CUDA cores, one token
-    (256, 512, 64, 64, 33, 0.3, 2),       # CUDA cores, split-K, ragged token block
+    (128, 768, 64, 64, 1, 0.5, 0),        # CUDA cores (ROW: mma.sync decode kernel), one token
+    (256, 512, 64, 64, 33, 0.3, 2),       # the same, split-K, ragged token block
     (256, 512, 128, 32, 40, 0.5, 0),      # other tile shapes: CUDA cores
     (512, 256, 256, 16, 7, 0.5, 0),
     (128, 384, 64, 128, 65, 0.5, 0),      # TK = 128: CUDA cores even at N >= 64
@@ -78,11 +82,15 @@ def test_col_tiles_match_row_tiles_and_oracle(us, orc, case):
     X = rng.standard_normal((N, K)).astype(np.float16)
     y_col = run(us, W, X, TM, TK, COL, split)
     y_row = run(us, W, X, TM, TK, ROW, split)
-    assert np.array_equal(y_col.view(np.uint16), y_row.view(np.uint16)), "ROW and COL tiles disagree"
+    same_kernel = not (TM == 64 and TK == 64 and N < 64)
+    if same_kernel:
+        assert np.array_equal(y_col.view(np.uint16), y_row.view(np.uint16)), "ROW and COL tiles disagree"
     n_idx, m_idx = np.meshgrid(np.arange(N), np.arange(M), indexing="ij")
     sel = rng.choice(N * M, size=min(N * M, 4096), replace=False)
     _, exact = orc.spmm_f16_at(W, X, n_idx.reshape(-1)[sel], m_idx.reshape(-1)[sel])
-    check_f16(y_col.reshape(-1)[sel], exact, f"{case}")
+    check_f16(y_col.reshape(-1)[sel], exact, f"{case} COL")
+    if not same_kernel:
+        check_f16(y_row.reshape(-1)[sel], exact, f"{case} ROW")
 
 
 def test_col_prefill_edge_tiles(us, orc):
