@@ -136,18 +136,25 @@ us_status us_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK,
  * s_w: M fp16 bit patterns, s_x: N fp16.  Yacc: N x M int32, Y: N x M fp16.
  * 1 <= N <= 2048.  split_k: 0 = automatic, else K tiles are split into that
  * many slices (1..nTK).  Results do not depend on split_k.  With 64 x 64 tiles
- * and N <= 8 the automatic choice slices nothing: the tile sequence is spread
- * evenly over the SMs and a band shared by several CTAs is finished by the last
- * one to arrive (arrival counters in the workspace). */
+ * and 1 <= N <= 32 the automatic choice slices nothing: the tile sequence is
+ * spread evenly over the SMs, and a band shared by several CTAs is finished by
+ * the CTA holding its first tile from the others' posted {value, tag} words
+ * (the workspace, left zeroed after every call). */
 us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_w,
                        const uint16_t* s_x, int N, int32_t* Yacc, uint16_t* Y,
                        void* ws, size_t ws_bytes, int split_k, void* stream);
 
-/* fp16 SpMM:  Y[n][m] = fp16(sum_k W[m][k] * X[n][k]) with fp32 accumulation
- * (tensor cores for large N).  W: elem US_F16, order US_ORDER_ROW.
- * X: N x K fp16 token-major, Y: N x M fp16, 1 <= N <= 2048.  split_k as above;
- * the fp32 partial sums are reduced in fixed slice order, so repeated calls
- * give bitwise identical results. */
+/* fp16 SpMM (UnionSparse Fig. 2 with fp16 operands; SPDP section 4 for the
+ * prefill shapes):  Y[n][m] = fp16(sum_k W[m][k] * X[n][k]) with fp32
+ * accumulation.  W: elem US_F16, order US_ORDER_ROW or US_ORDER_COL (the
+ * spMspV layout serves this product too).  X: N x K fp16 token-major,
+ * Y: N x M fp16, 1 <= N <= 2048.  split_k as above.  With 64 x 64 tiles,
+ * N >= 64 and M % 128 == 0 the product runs on the tensor cores (tcgen05);
+ * 1-63 tokens on ROW tiles run on the mma.sync decode kernel; every other
+ * case on the generic CUDA-core kernel.  The fp32 partial sums are reduced in
+ * fixed slice order, so repeated calls with the same arguments give bitwise
+ * identical results; calls that take different kernels may differ in the
+ * last bits. */
 us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
                       void* ws, size_t ws_bytes, int split_k, void* stream);
 
