@@ -304,7 +304,12 @@ def main():
 
     extras = {}
     if not args.no_extras and rank == 0:
-        extras = measure_extras(us, torch, wl, dev, stream)
+        # secondary rows: a failure there is reported in the line, and does not
+        # take the headline measurement down with it
+        try:
+            extras = measure_extras(us, torch, wl, dev, stream)
+        except Exception as e:                       # noqa: BLE001
+            extras = {"error": f"{type(e).__name__}: {e}"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
