@@ -100,16 +100,6 @@ US_DEV void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_
         : "memory");
 }
 
-// As tma_load_2d, the tile written at the same offset in every CTA of the
-// cluster named in `mask`, each completing on its own barrier at `bar`'s offset
-US_DEV void tma_load_2d_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(us::smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(us::smem_addr(bar)), "h"(mask)
-        : "memory");
-}
-
 struct TcParams {
     UsKParams p;
     int n_tiles;          // ceil(N / (256 NH))
@@ -158,11 +148,9 @@ US_DEV void tc_reduce(const UsKParams& p, float* part, int64_t slice_stride, int
     }
 }
 
-// CL: CTAs per cluster along M (1 or 2).  A pair of row blocks shares every
-// activation tile: each CTA loads half of it and multicasts it to both, and
-// each CTA's MMA releases the B stage in both, so a CTA reads half the
-// activation bytes from L2.
-template <int ORDER, int NH, int CL>
+// Each CTA loads its own activation tiles; CTAs of neighbouring row blocks
+// read the same tiles, which the L2 serves after the first.
+template <int ORDER, int NH>
 __global__ void __launch_bounds__(kThreads, 1)
 spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) {
     using Sh = TcShape<NH>;
@@ -195,15 +183,13 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         }
         for (int s = 0; s < kAStages; ++s) us::mbar_init(&S.a_full[s], kGroupWarps);
         for (int s = 0; s < kBStages; ++s) us::mbar_init(&S.b_full[s], 1);
-        for (int s = 0; s < kSD; ++s) us::mbar_init(&S.sdone[s], CL);   // one release per CTA of the cluster
+        for (int s = 0; s < kSD; ++s) us::mbar_init(&S.sdone[s], 1);
         us::mbar_init(&S.done, 1);
         S.issued_w = S.issued_x = 0;
         us::fence_mbar_init();
     }
     if (warp == 1) us::tmem_alloc(&S.tmem_base, kBN);
-    // the peer CTA multicasts into this CTA's stages and barriers: both must be
-    // initialised before either starts
-    if constexpr (CL > 1) us::cluster_sync(); else __syncthreads();
+    __syncthreads();
     us::tc_fence_after();
     const uint32_t tmem = S.tmem_base;
     us::pdl_wait();
@@ -306,8 +292,6 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         }
     } else if (warp == 2) {
         // ------------------------------------------------------- X producer
-        const int crank = CL > 1 ? (int)us::cluster_ctarank() : 0;
-        (void)crank;
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
             for (int q = 0; q < nk; ++q) {
@@ -318,20 +302,9 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     break;
                 }
                 us::mbar_arrive_expect_tx(&S.b_full[s], (uint32_t)(kHBytes * halves));
-                if constexpr (CL == 1) {
-                    for (int h = 0; h < halves; ++h)
-                        tma_load_2d(b_st + s * kBBytes + h * kHBytes, &xmap, (kt0 + q) * kBK, nt * kBN + h * kBH,
-                                    &S.b_full[s]);
-                } else if constexpr (NH == 2) {
-                    // CTA r loads token half r (if it holds tokens) into both CTAs
-                    if (crank < halves)
-                        tma_load_2d_mc(b_st + s * kBBytes + crank * kHBytes, &xmap, (kt0 + q) * kBK,
-                                       nt * kBN + crank * kBH, &S.b_full[s], (uint16_t)0x3);
-                } else {
-                    // CTA r loads tokens 128 r .. 128 r + 127 of the 256 (box of 128 rows)
-                    tma_load_2d_mc(b_st + s * kBBytes + crank * (kHBytes / 2), &xmap, (kt0 + q) * kBK,
-                                   nt * kBN + crank * (kBH / 2), &S.b_full[s], (uint16_t)0x3);
-                }
+                for (int h = 0; h < halves; ++h)
+                    tma_load_2d(b_st + s * kBBytes + h * kHBytes, &xmap, (kt0 + q) * kBK, nt * kBN + h * kBH,
+                                &S.b_full[s]);
                 S.issued_x = (uint32_t)(q + 1);
             }
         }
@@ -355,12 +328,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                     for (int h = 0; h < halves; ++h)
                         us::umma_f16(tmem + (uint32_t)(h * kBH), ad + 2 * kk, bd + (uint64_t)(h * (kHBytes >> 4)) + 2 * kk,
                                      idesc, (q > 0 || kk > 0) ? 1u : 0u);
-                // one release for both stages (in both CTAs of a pair: the B stage
-                // is reloaded by both)
-                if constexpr (CL > 1)
-                    us::umma_commit_mc(&S.sdone[q % kSD], (uint16_t)0x3);
-                else
-                    us::umma_commit(&S.sdone[q % kSD]);
+                // one release for both stages
+                us::umma_commit(&S.sdone[q % kSD]);
             }
             us::umma_commit(&S.done);
         }
@@ -547,9 +516,6 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
     }
     us::tc_fence_before();
     __syncthreads();
-    // no CTA leaves while its MMAs' releases may still arrive at the peer's
-    // barriers, or the peer's copies at its own stages
-    if constexpr (CL > 1) us::cluster_sync();
     if (warp == 1) us::tmem_dealloc(tmem, kBN);
     if (p.split > 1 && !any_failed) {
         __threadfence();
@@ -621,12 +587,10 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     if (!enc) return US_ERR_CUDA;
     if (p.tok_block != kBH && p.tok_block != 2 * kBH) return US_ERR_INVALID_ARG;
     const bool two = p.tok_block == 2 * kBH;
-    // pairs of row blocks share their activation tiles when the count is even
-    const bool pair = (p.M / kBM) % 2 == 0;
     CUtensorMap map;
     const cuuint64_t gdim[2] = {(cuuint64_t)p.K, (cuuint64_t)p.N};
     const cuuint64_t gstride[1] = {(cuuint64_t)p.K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)(pair && !two ? kBH / 2 : kBH)};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)kBH};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(p.X), gdim, gstride, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -637,10 +601,8 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     tp.n_tiles = (p.N + p.tok_block - 1) / p.tok_block;
     const bool col = p.order == US_ORDER_COL;
     void (*kern)(const TcParams, const CUtensorMap) =
-        two ? (pair ? (col ? spmm_f16_tc_kernel<US_ORDER_COL, 2, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 2, 2>)
-                    : (col ? spmm_f16_tc_kernel<US_ORDER_COL, 2, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 2, 1>))
-            : (pair ? (col ? spmm_f16_tc_kernel<US_ORDER_COL, 1, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 1, 2>)
-                    : (col ? spmm_f16_tc_kernel<US_ORDER_COL, 1, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 1, 1>));
+        two ? (col ? spmm_f16_tc_kernel<US_ORDER_COL, 2> : spmm_f16_tc_kernel<US_ORDER_ROW, 2>)
+            : (col ? spmm_f16_tc_kernel<US_ORDER_COL, 1> : spmm_f16_tc_kernel<US_ORDER_ROW, 1>);
     const size_t smem = two ? TcShape<2>::kSmem : TcShape<1>::kSmem;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
@@ -649,13 +611,6 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = pair ? 2 : 1;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kern, tp, map) != cudaSuccess) return US_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }

@@ -33,15 +33,6 @@ US_DEV void umma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// As umma_commit, arriving on the barrier at the same offset in every CTA of
-// the cluster named in `mask`
-US_DEV void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                     us::smem_addr(bar)),
-                 "h"(mask)
-                 : "memory");
-}
-
 US_DEV void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(us::smem_addr(dst_smem)),
                  "r"(ncols)

@@ -356,8 +356,8 @@ F16_CASES = [
     # second half holds 9 tokens, under split-K
     (256, 512, 64, 64, 600, 0.5, 0),
     (128, 1024, 64, 64, 777, 0.5, 3),
-    # a pair of row blocks sharing activation tiles by multicast, split-K, and
-    # a last tile whose second token half holds no tokens
+    # two row blocks under split-K, and a last tile whose second token half
+    # holds no tokens
     (256, 1024, 64, 64, 600, 0.5, 2),
     # CUDA-core paths
     (256, 512, 64, 64, 1, 0.5, 0),
