@@ -160,9 +160,9 @@ us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
 
 /* fp16 SpMM with no workspace argument and no allocation.  (No counterpart on
  * the pages: this is a convenience of this library.)  For callers that cannot
- * allocate device memory where they multiply - code running inside CUDA graph
- * capture, where a cudaMalloc would break the capture; fixed-arena allocators;
- * embedders that own every allocation - the split-K scratch comes from a
+ * allocate device memory where they multiply - fixed-arena allocators that
+ * hand out no extra buffers, embedders that own every allocation, code paths
+ * that must not enter the CUDA allocator - the split-K scratch comes from a
  * device array inside the library, US_NOALLOC_SCRATCH_BYTES (8 MiB), which
  * every GPU that loads the library keeps until the process exits.
  * Same arguments and results as us_spmm_f16 without ws/ws_bytes.  With
@@ -304,6 +304,18 @@ us_status us_validate(const us_bitmap* W);
  * kernels set on device-side errors (US_ERR_TIMEOUT, US_ERR_CORRUPT,
  * US_ERR_INVALID_ARG, US_ERR_WORKSPACE; US_OK if none). */
 us_status us_get_last_device_status(void* stream);
+
+/* Self-test of the device-side timeout path.  (No counterpart on the pages:
+ * every wait of every kernel here is bounded, and this entry point shows that
+ * a wait that runs out ends the kernel with a status instead of a hang.)
+ * Launches one thread that waits, through the same bounded mbarrier wait the
+ * kernels use, on a barrier that nothing completes, with no copy or other
+ * asynchronous operation in flight.  After limit_ns the wait gives up and
+ * records US_ERR_TIMEOUT in the device status word; the kernel then returns
+ * and the context stays usable.  limit_ns: 1000 .. 1000000000 (else
+ * US_ERR_INVALID_ARG).  elapsed_ns: device, 8-byte aligned, nullable; receives
+ * the nanoseconds the wait took before giving up (0 if it completed). */
+us_status us_selftest_wait_timeout(uint64_t limit_ns, uint64_t* elapsed_ns, void* stream);
 
 /* Static description of a status code. */
 const char* us_status_string(us_status s);
