@@ -33,7 +33,7 @@ EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_s
             "us_colinfo", "us_spmspv_f16_ci", "us_quantize_x",
             "us_encode_ie_sizes", "us_encode_ie", "us_reorder_rows", "us_spmm_w4a4_ie", "us_workspace_bytes_ie",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
-            "us_status_string", "us_version")
+            "us_selftest_wait_timeout", "us_status_string", "us_version")
 
 
 class LibraryMissing(RuntimeError):
@@ -93,6 +93,7 @@ def load(path: str = LIB_PATH):
         lib.us_pick_split_k.argtypes = [i32, pbm, i32, ctypes.POINTER(ctypes.c_int)]
         lib.us_validate.argtypes = [pbm]
         lib.us_get_last_device_status.argtypes = [P]
+        lib.us_selftest_wait_timeout.argtypes = [ctypes.c_uint64, P, P]
         lib.us_status_string.argtypes = [i32]
         lib.us_status_string.restype = ctypes.c_char_p
         lib.us_version.argtypes = []
@@ -356,6 +357,13 @@ def us_validate_host(bitmap, tile_off, values, M, K, TM, TK, elem, order) -> int
     d = us_bitmap(M, K, TM, TK, elem, order, bm.ctypes.data, off.ctypes.data,
                   v.ctypes.data if v.size else None, v.size, 0, 0)
     return int(load().us_validate(ctypes.byref(d)))
+
+
+def us_selftest_wait_timeout(limit_ns: int, elapsed: torch.Tensor | None = None, stream=None):
+    """Run the bounded-wait self-test: one device wait that nothing completes,
+    given up after limit_ns (elapsed: optional int64 device tensor of one element)."""
+    _check("us_selftest_wait_timeout", load().us_selftest_wait_timeout(int(limit_ns), _dptr(elapsed),
+                                                                       _stream(stream)))
 
 
 def us_get_last_device_status(stream=None) -> int:

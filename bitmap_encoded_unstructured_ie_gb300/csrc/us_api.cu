@@ -177,6 +177,23 @@ int num_sms() {
 
 }  // namespace us
 
+namespace {
+
+// One thread waits on an mbarrier that nothing arrives on (no copy or other
+// asynchronous operation is in flight), through the same bounded wait every
+// kernel uses, with the caller's limit.
+__global__ void wait_selftest_kernel(unsigned* status, uint64_t limit_ns, uint64_t* elapsed_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    us::mbar_init(&bar, 1);
+    us::fence_mbar_init();
+    const uint64_t t0 = us::globaltimer_ns();
+    const bool done = us::mbar_wait_for(&bar, 0u, status, limit_ns);
+    if (elapsed_ns) *elapsed_ns = done ? 0ull : us::globaltimer_ns() - t0;
+}
+
+}  // namespace
+
 extern "C" {
 
 int us_version(void) { return 100; }
@@ -545,6 +562,15 @@ us_status us_validate(const us_bitmap* W) {
         }
     }
     return US_OK;
+}
+
+us_status us_selftest_wait_timeout(uint64_t limit_ns, uint64_t* elapsed_ns, void* stream) {
+    if (limit_ns < 1000ull || limit_ns > 1000000000ull) return US_ERR_INVALID_ARG;
+    if (elapsed_ns && (reinterpret_cast<uintptr_t>(elapsed_ns) & 7u)) return US_ERR_INVALID_ARG;
+    unsigned* status = status_ptr();
+    if (!status) return US_ERR_CUDA;
+    wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns, elapsed_ns);
+    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }
 
 us_status us_get_last_device_status(void* stream) {

@@ -89,16 +89,21 @@ US_DEV bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
     return ok != 0;
 }
 
-US_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+// As mbar_wait, with the limit given in nanoseconds.
+US_DEV bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned* status, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait_sleep(bar, parity, 100000u)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             set_status(status, US_ERR_TIMEOUT);
             return false;
         }
     }
     return true;
+}
+
+US_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
+    return mbar_wait_for(bar, parity, status, kWaitLimitNs);
 }
 
 // Bulk copy global -> shared (TMA, 1-D, no tensor map), completing `bytes`
