@@ -149,9 +149,17 @@ Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
     return pl;
 }
 
-Plan plan_spmspv(const us_bitmap* W) {
+// streamed: us_spmspv_f16 may take the streamed kernel (64 x 64 tiles); the
+// batched ColInfo kernel plans with streamed = false
+Plan plan_spmspv(const us_bitmap* W, bool streamed = true) {
     Plan pl{};
     pl.tok_block = 1;
+    const int ss = streamed ? us::spmspv_stream_split(W->TM, W->TK, W->M / W->TM, W->K / W->TK) : 0;
+    if (ss > 0) {
+        pl.dec = true;                    // the streamed kernel
+        pl.split = ss;
+        return pl;
+    }
     pl.split = auto_split(W->M / W->TM, W->K / W->TK, 1, 2 * us::num_sms(), us::spmspv_max_split());
     pl.ws = us::spmspv_ws(W->M, W->TM, pl.split);
     return pl;
@@ -395,6 +403,7 @@ us_status us_spmspv_f16(const us_bitmap* W, const uint16_t* x, float tau, uint16
     p.split = pl.split; p.tok_block = 1;
     p.counters = static_cast<unsigned*>(ws);
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, 1);
+    if (pl.dec) return us::launch_spmspv_stream(p, static_cast<cudaStream_t>(stream));
     return us::launch_spmspv(p, static_cast<cudaStream_t>(stream));
 }
 
@@ -517,7 +526,7 @@ us_status us_spmspv_f16_ci(const us_bitmap* W, const uint32_t* colinfo, const ui
     if (N < 1 || !colinfo || !X || !Y || !aligned16(colinfo) || !aligned16(X) || !aligned16(Y) || !(tau >= 0.f))
         return US_ERR_INVALID_ARG;
     if ((int64_t)N * W->K >= ((int64_t)1 << 31) || (int64_t)N * W->M >= ((int64_t)1 << 31)) return US_ERR_TOO_LARGE;
-    const Plan pl = plan_spmspv(W);
+    const Plan pl = plan_spmspv(W, false);
     if (pl.ws && (!ws || ws_bytes < pl.ws || !aligned16(ws))) return US_ERR_WORKSPACE;
     UsKParams p;
     fill_common(p, W, N);

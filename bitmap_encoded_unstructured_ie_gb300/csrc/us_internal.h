@@ -65,6 +65,10 @@ us_status launch_colinfo(const uint64_t* bitmap, int TM, int TK, int64_t nT, uin
 us_status launch_spmspv_ci(const UsKParams& p, const uint32_t* colinfo, cudaStream_t st);
 size_t spmspv_ws(int M, int TM, int split);
 int spmspv_max_split();
+// streamed spMspV on 64 x 64 tiles (us_spmspv_stream.cu): its K split, 0 when
+// the shape is not supported
+int spmspv_stream_split(int TM, int TK, int nTM, int nTK);
+us_status launch_spmspv_stream(UsKParams p, cudaStream_t st);
 
 // per-token int4 quantisation of fp16 activations (us_quant.cu)
 us_status launch_quantize_x(const uint16_t* X, int N, int K, uint8_t* Xq, uint16_t* s_x, cudaStream_t st);
