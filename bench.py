@@ -307,7 +307,8 @@ def main():
         # secondary rows: a failure there is reported in the line, and does not
         # take the headline measurement down with it
         try:
-            extras = measure_extras(us, torch, wl, dev, stream)
+            extras = measure_extras(us, torch, wl, dev, stream, hbm_peak, bf16_peak,
+                                    cpu=(world == 1 and not args.no_cpu))
         except Exception as e:                       # noqa: BLE001
             extras = {"error": f"{type(e).__name__}: {e}"}
 
@@ -468,11 +469,153 @@ def time_graph(torch, stream, us, fn, reps=5):
     return a.elapsed_time(b) / reps
 
 
-def measure_extras(us, torch, wl, dev, stream):
-    """Secondary rows, each timed on its own: spMspV, the encoder, fp16 prefill,
-    the FFN W4A4 shapes.  Copies rotate so every launch reads from HBM."""
+def oracle_ms(fn, min_s: float = 0.25, max_reps: int = 20) -> float:
+    """Mean wall time (ms) of one oracle call, repeated for at least min_s."""
+    reps, el = 0, 0.0
+    while reps == 0 or (el < min_s and reps < max_reps):
+        t0 = time.perf_counter()
+        fn()
+        el += time.perf_counter() - t0
+        reps += 1
+    return el / reps * 1e3
+
+
+class OracleRows:
+    """The CPU oracle's time for one call of a configuration, measured on the
+    first `bands` tile-row bands of the encoded matrix (decode + multiply of
+    that shard) and scaled to the whole matrix by the band count."""
+
+    def __init__(self):
+        from oracle import oracle as orc
+        from bitmap_encoded_unstructured_ie_gb300 import sharding
+        self.orc, self.sharding = orc, sharding
+        self.threads = orc.max_threads()
+
+    def w4a4(self, Wq, Xq, s_w, s_x, bands: int):
+        orc = self.orc
+        M, K = Wq.shape
+        enc = orc.encode(Wq, 64, 64, orc.I4, orc.ROW)
+        bands = min(bands, M // 64)
+        bm, off, vals, Ms = self.sharding.shard_arrays(*enc, M, K, 64, 64, orc.I4, 0, bands)
+
+        def call():
+            Wd = orc.decode(bm, off, vals, Ms, K, 64, 64, orc.I4, orc.ROW)
+            orc.spmm_w4a4(Wd, Xq, s_w[:Ms], s_x, nthreads=self.threads)
+        return self._row(oracle_ms(call) * (M // 64) / bands, bands, M // 64)
+
+    def f16(self, W, X, order: int, bands: int):
+        orc = self.orc
+        M, K = W.shape
+        enc = orc.encode(W, 64, 64, orc.F16, order)
+        bands = min(bands, M // 64)
+        bm, off, vals, Ms = self.sharding.shard_arrays(*enc, M, K, 64, 64, orc.F16, 0, bands)
+
+        def call():
+            Wd = orc.decode(bm, off, vals, Ms, K, 64, 64, orc.F16, order)
+            orc.spmm_f16(Wd, X, nthreads=self.threads)
+        return self._row(oracle_ms(call) * (M // 64) / bands, bands, M // 64)
+
+    def spmspv(self, W, x, bands: int):
+        orc = self.orc
+        M, K = W.shape
+        enc = orc.encode(W, 64, 64, orc.F16, orc.COL)
+        bands = min(bands, M // 64)
+        bm, off, vals, Ms = self.sharding.shard_arrays(*enc, M, K, 64, 64, orc.F16, 0, bands)
+
+        def call():
+            Wd = orc.decode(bm, off, vals, Ms, K, 64, 64, orc.F16, orc.COL)
+            orc.spmspv_f16(Wd, x, 0.0, nthreads=self.threads)
+        return self._row(oracle_ms(call) * (M // 64) / bands, bands, M // 64)
+
+    def _row(self, ms, bands, total):
+        return {"us_per_call": round(ms * 1e3, 1), "cores": self.threads, "kind": "oracle",
+                "sample": f"decode + multiply of {bands} of {total} tile-row bands, scaled"}
+
+
+def pct(gbs: float, peak: float) -> float:
+    return round(100.0 * gbs / peak, 2)
+
+
+def tensor_peaks(torch, dev):
+    """Dense int8 tensor throughput of this GPU (cuBLAS through torch._int_mm,
+    8192^3, best of 5), the denominator for an int8 tensor path."""
+    try:
+        a = torch.randint(-8, 8, (8192, 8192), dtype=torch.int8, device=dev)
+        b = torch.randint(-8, 8, (8192, 8192), dtype=torch.int8, device=dev)
+        torch._int_mm(a, b)
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(5):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._int_mm(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return {"int8_dense_TOPS": round(2 * 8192 ** 3 / (best * 1e-3) / 1e12, 1),
+                "how": "torch._int_mm (cuBLAS) int8 x int8 -> int32, 8192^3, best of 5, CUDA events"}
+    except Exception as e:                            # noqa: BLE001
+        return {"int8_dense_TOPS": None, "error": f"{type(e).__name__}: {e}"}
+
+
+def measure_extras(us, torch, wl, dev, stream, hbm_peak, bf16_peak, cpu=True):
+    """Secondary rows, each timed on its own: every configuration besides the
+    headline (fp16 256 x 512, W4A4 4096^2 at 30 and 70 % sparsity, the FFN
+    shapes, fp16 prefill and decode, spMspV), the encoder, W2A4, IE-BME areas,
+    the activation quantiser.  Copies rotate so every launch reads from HBM.
+    Each row gives its % of the measured HBM (or fp16 tensor) peak and, where
+    `cpu`, the oracle's time for the same call."""
     out = {}
     l2 = 126 * 2 ** 20
+    ocpu = OracleRows() if cpu else None
+    out["tensor_peaks"] = tensor_peaks(torch, dev)
+    # fp16 bitmap SpMM 256 x 512, 50 % uniform sparsity, N = 1 (latency row):
+    # enough rotating copies that the chain streams more than twice L2
+    c1 = wl.f16_spmm(256, 512, 1, 0.5, seed=0)
+    E1 = us.us_encode(torch.from_numpy(c1["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_ROW)
+    E1.flags = us.US_BITMAP_STATIC
+    n1 = max(4, math.ceil(2.2 * l2 / E1.nbytes()))
+    cp1 = [E1] + [us.Encoded(E1.M, E1.K, E1.TM, E1.TK, E1.elem, E1.order, E1.bitmap.clone(), E1.tile_off.clone(),
+                             E1.values.clone(), E1.values_bytes, E1.flags) for _ in range(n1 - 1)]
+    X1 = torch.from_numpy(c1["X"].view(np.int16)).to(dev)
+    Y1 = torch.empty(1, 256, dtype=torch.int16, device=dev)
+    ws1 = us.workspace(us.US_OP_SPMM_F16, E1, 1)
+    ms = time_graph(torch, stream, us, lambda: [us.us_spmm_f16(E, X1, 1, Y1, ws1, 0, stream) for E in cp1], 3)
+    t = ms * 1e3 / n1
+    b1 = E1.nbytes() + 512 * 2 + 256 * 2
+    out["f16_256x512_s50_n1"] = {"us_per_call": round(t, 3), "bytes": b1, "GB/s": round(b1 / (t * 1e-6) / 1e9, 1),
+                                 "pct_hbm_measured": pct(b1 / (t * 1e-6) / 1e9, hbm_peak), "copies": n1,
+                                 "cpu_oracle": ocpu.f16(c1["W"], c1["X"], 0, 4) if ocpu else None}
+    # W4A4 4096^2 at 30 % and 70 % sparsity (the headline is 50 %), N = 1 / 8 / 16
+    spars = {}
+    for sp_ in (0.3, 0.7):
+        ds = wl.w4a4(4096, 4096, 16, sp_, seed=0)
+        Es = us.us_encode(torch.from_numpy(ds["Wq"]).to(dev), 64, 64, us.US_I4, us.US_ORDER_ROW)
+        Es.flags = us.US_BITMAP_STATIC
+        ns_ = max(4, math.ceil(2.2 * l2 / Es.nbytes()))
+        cps_ = [Es] + [us.Encoded(Es.M, Es.K, Es.TM, Es.TK, Es.elem, Es.order, Es.bitmap.clone(), Es.tile_off.clone(),
+                                  Es.values.clone(), Es.values_bytes, Es.flags) for _ in range(ns_ - 1)]
+        sws = torch.from_numpy(ds["s_w"].view(np.int16)).to(dev)
+        row = {"copies": ns_, "value_bytes": Es.values_bytes}
+        for N in NS:
+            Xs = torch.from_numpy(wl.pack_int4(ds["Xq"][:N])).to(dev)
+            sxs = torch.from_numpy(ds["s_x"][:N].view(np.int16)).to(dev)
+            Yas = torch.empty(N, 4096, dtype=torch.int32, device=dev)
+            Yhs = torch.empty(N, 4096, dtype=torch.int16, device=dev)
+            wss = us.workspace(us.US_OP_SPMM_W4A4, Es, N)
+            ms = time_graph(torch, stream, us, lambda: [us.us_spmm_w4a4(E, Xs, sws, sxs, N, Yas, Yhs, wss, 0, stream)
+                                                    for E in cps_], 20)
+            t = ms * 1e3 / ns_
+            bs = call_bytes(Es.values_bytes, 4096, 4096, N, 64, 64)
+            gbs = bs / (t * 1e-6) / 1e9
+            row[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": bs, "GB/s": round(gbs, 1),
+                            "pct_hbm_measured": pct(gbs, hbm_peak),
+                            "eff_TOPS": round(2 * 4096 * 4096 * N / (t * 1e-6) / 1e12, 2),
+                            "cpu_oracle": ocpu.w4a4(ds["Wq"], ds["Xq"][:N], ds["s_w"], ds["s_x"][:N], 8)
+                            if ocpu else None}
+        spars[f"s{int(sp_ * 100)}"] = row
+    out["w4a4_4096_sparsity"] = spars
     # spMspV 14336 x 4096, 50 % static sparsity, activations with 50/70/90 % zeros
     s = wl.spmspv(14336, 4096, 0.5, 0.5, seed=0)
     Es = us.us_encode(torch.from_numpy(s["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_COL)
@@ -494,7 +637,9 @@ def measure_extras(us, torch, wl, dev, stream):
         ms = time_graph(torch, stream, us, lambda: [us.us_spmspv_f16(E, xt, 0.0, ys, wsb, stream) for E in cps])
         t = ms * 1e3 / n_cp
         sp[f"zeros_{int(zf * 100)}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
-                                        "GB/s": round(alg / (t * 1e-6) / 1e9, 1)}
+                                        "GB/s": round(alg / (t * 1e-6) / 1e9, 1),
+                                        "pct_hbm_measured": pct(alg / (t * 1e-6) / 1e9, hbm_peak),
+                                        "cpu_oracle": ocpu.spmspv(s["W"], x, 8) if ocpu else None}
     out["spmspv_f16_14336x4096"] = sp
     # the same with ColInfo (per tile column: offset and count), N = 1 and a batch of 8
     cis = [us.us_colinfo(E, None, stream) for E in cps]
@@ -514,7 +659,8 @@ def measure_extras(us, torch, wl, dev, stream):
         t = ms * 1e3 / n_cp
         sci[f"zeros_{int(zf * 100)}_N{N}"] = {"us_per_launch": round(t, 3), "alg_bytes": alg,
                                               "active_columns": round(float(active.mean()), 3),
-                                              "GB/s": round(alg / (t * 1e-6) / 1e9, 1)}
+                                              "GB/s": round(alg / (t * 1e-6) / 1e9, 1),
+                                              "pct_hbm_measured": pct(alg / (t * 1e-6) / 1e9, hbm_peak)}
     out["spmspv_colinfo_f16_14336x4096"] = sci
     # encoder, W4A4 4096^2 (dense int8 codes in): count + scan + pack
     d = wl.w4a4(4096, 4096, 1, 0.5, seed=0)
@@ -523,7 +669,8 @@ def measure_extras(us, torch, wl, dev, stream):
     wse = torch.zeros(us.encode_sizes(4096, 4096, 64, 64, us.US_I4)[3], dtype=torch.uint8, device=dev)
     ms = time_graph(torch, stream, us, lambda: us.us_encode_into(Wd, Ee, wse, stream), 5)
     out["encode_w4a4_4096"] = {"ms_per_encode": round(ms, 4),
-                               "dense_GB/s": round(4096 * 4096 / (ms * 1e-3) / 1e9, 1)}
+                               "dense_GB/s": round(4096 * 4096 / (ms * 1e-3) / 1e9, 1),
+                               "pct_hbm_measured": pct(4096 * 4096 / (ms * 1e-3) / 1e9, hbm_peak)}
     # fp16 prefill 4096^2, 60 % sparsity, N = 256 / 1024 / 2048
     f = wl.f16_spmm(4096, 4096, 2048, 0.6, seed=0)
     Ef = us.us_encode(torch.from_numpy(f["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_ROW)
@@ -534,7 +681,9 @@ def measure_extras(us, torch, wl, dev, stream):
         wsf = us.workspace(us.US_OP_SPMM_F16, Ef, N)
         ms = time_graph(torch, stream, us, lambda: us.us_spmm_f16(Ef, Xf[:N], N, Yf, wsf, 0, stream), 3)
         fl = 2 * 4096 * 4096 * N
-        pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
+        tf = fl / (ms * 1e-3) / 1e12
+        pf[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(tf, 2), "pct_f16_tensor_measured": pct(tf, bf16_peak),
+                      "cpu_oracle": ocpu.f16(f["W"], f["X"][:N], 0, 1) if ocpu else None}
     out["prefill_f16_4096_s60"] = pf
     # fp16 decode 4096^2, 50 % sparsity, N = 1 / 8 / 16 / 32 (mma.sync decode
     # kernel); rotating weight copies so every launch reads from HBM
@@ -551,7 +700,9 @@ def measure_extras(us, torch, wl, dev, stream):
         ms = time_graph(torch, stream, us, lambda: [us.us_spmm_f16(E, Xg[:N], N, Yg, wsg, 0, stream) for E in cpg])
         t = ms * 1e3 / ng
         byt = Eg.nbytes() + 2 * N * 4096 * 2
-        dec[str(N)] = {"us_per_call": round(t, 3), "bytes": byt, "GB/s": round(byt / (t * 1e-6) / 1e9, 1)}
+        dec[str(N)] = {"us_per_call": round(t, 3), "bytes": byt, "GB/s": round(byt / (t * 1e-6) / 1e9, 1),
+                       "pct_hbm_measured": pct(byt / (t * 1e-6) / 1e9, hbm_peak),
+                       "cpu_oracle": ocpu.f16(fd["W"], fd["X"][:N], 0, 8) if ocpu else None}
     out["decode_f16_4096_s50"] = dec
     # the same on COL tiles: the format spMspV reads serves prefill too
     Efc = us.us_encode(torch.from_numpy(f["W"].view(np.int16)).to(dev), 64, 64, us.US_F16, us.US_ORDER_COL)
@@ -561,7 +712,8 @@ def measure_extras(us, torch, wl, dev, stream):
         wsf = us.workspace(us.US_OP_SPMM_F16, Efc, N)
         ms = time_graph(torch, stream, us, lambda: us.us_spmm_f16(Efc, Xf[:N], N, Yf, wsf, 0, stream), 3)
         fl = 2 * 4096 * 4096 * N
-        pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(fl / (ms * 1e-3) / 1e12, 2)}
+        tf = fl / (ms * 1e-3) / 1e12
+        pfc[str(N)] = {"ms": round(ms, 4), "eff_TFLOPs": round(tf, 2), "pct_f16_tensor_measured": pct(tf, bf16_peak)}
     out["prefill_f16_col_tiles_4096_s60"] = pfc
     # the FFN shapes: W4A4 11008 x 4096 and 4096 x 11008, 50 % sparsity with a
     # per-row Beta(2,2) keep rate, N = 1 / 4 / 16 / 32, static weights
@@ -586,7 +738,10 @@ def measure_extras(us, torch, wl, dev, stream):
             t = ms * 1e3 / nf
             bf = call_bytes(Ef.values_bytes, Mf, Kf, N, 64, 64)
             row[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": bf, "GB/s": round(bf / (t * 1e-6) / 1e9, 1),
-                            "eff_TOPS": round(2 * Mf * Kf * N / (t * 1e-6) / 1e12, 2)}
+                            "pct_hbm_measured": pct(bf / (t * 1e-6) / 1e9, hbm_peak),
+                            "eff_TOPS": round(2 * Mf * Kf * N / (t * 1e-6) / 1e12, 2),
+                            "cpu_oracle": ocpu.w4a4(df["Wq"], df["Xq"][:N], df["s_w"], df["s_x"][:N], 4)
+                            if ocpu else None}
         ffn[f"{Mf}x{Kf}"] = row
     out["w4a4_ffn_beta_s50"] = ffn
     # W2A4 4096^2 at 50 %: int2 weights decoded into the same dense tiles
@@ -608,7 +763,8 @@ def measure_extras(us, torch, wl, dev, stream):
                                                 for E in cps2], 20)
         t = ms * 1e3 / n2
         b2 = call_bytes(E2.values_bytes, 4096, 4096, N, 64, 64)
-        w2[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": b2, "GB/s": round(b2 / (t * 1e-6) / 1e9, 1)}
+        w2[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": b2, "GB/s": round(b2 / (t * 1e-6) / 1e9, 1),
+                       "pct_hbm_measured": pct(b2 / (t * 1e-6) / 1e9, hbm_peak)}
     out["w2a4_4096_s50"] = w2
     # IE-BME with areas: W4A4 4096^2 at 50 %, 16 x 64 local tiles, 2 x 2 areas, with
     # and without the offline row reordering; encoded bytes and the SpMM time
@@ -645,7 +801,8 @@ def measure_extras(us, torch, wl, dev, stream):
         sq = torch.empty(N, dtype=torch.int16, device=dev)
         ms = time_graph(torch, stream, us, lambda: us.us_quantize_x(Xh, N, 4096, Xq, sq, stream), 20)
         byt = N * 4096 * 2 + N * 2048 + N * 2
-        qz[str(N)] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1)}
+        qz[str(N)] = {"us": round(ms * 1e3, 2), "GB/s": round(byt / (ms * 1e-3) / 1e9, 1),
+                      "pct_hbm_measured": pct(byt / (ms * 1e-3) / 1e9, hbm_peak)}
     out["quantize_x_k4096"] = qz
     return out
 
