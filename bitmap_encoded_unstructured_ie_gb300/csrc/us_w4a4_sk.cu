@@ -241,8 +241,11 @@ w4a4_sk_kernel(const UsKParams p) {
                 ps |= ((sel >> (4 * i)) & 0xFu) << (4 * to);
             }
             // clear positions take rank 7's byte, which the odd-rank mask empties
-            // unless all eight positions are set
-            const uint2 ent = make_uint2(ps, e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u);
+            // unless all eight positions are set.  Only high nibbles of the
+            // odd/even bytes reach the dense word, so the mask's lowest nibble
+            // carries the byte's popcount (POPC issues at a quarter of the
+            // logic-op rate on this GPU; this costs one AND)
+            const uint2 ent = make_uint2(ps, (e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u) | (uint32_t)__popc(e));
 #pragma unroll
             for (int r = 0; r < kLutRep; ++r) lut[e * kLutRep + r] = ent;
         }
@@ -329,10 +332,10 @@ w4a4_sk_kernel(const UsKParams p) {
                     const uint32_t even = (win << 4) & 0xF0F0F0F0u;         // 16 w, ranks 0,2,4,6
                     const uint32_t d0 = __byte_perm(even, odd, ent.x);
                     const uint32_t d1 = __byte_perm(even, odd, ent.x >> 16);
-                    // byte i = d0's nibble i | d1's nibble i << 4; the mma consumer
-                    // keeps w + 8 (unsigned) for its fp16 conversion
-                    pw[h][bt] = (((d0 >> 4) & 0x0F0F0F0Fu) | (d1 & 0xF0F0F0F0u)) ^ (NT ? 0x88888888u : 0u);
-                    ob[h] += (uint32_t)__popc(bb);
+                    // byte i = d0's nibble i | d1's nibble i << 4 (two's complement;
+                    // the mma consumer's fp16 conversion adds the bias of 8)
+                    pw[h][bt] = ((d0 >> 4) & 0x0F0F0F0Fu) | (d1 & 0xF0F0F0F0u);
+                    ob[h] += ent.y & 0xFu;
                 }
             }
 #pragma unroll
@@ -472,9 +475,12 @@ w4a4_sk_kernel(const UsKParams p) {
                             acc[mb][nt][c] = 0.f;
                         }
             };
-            // word of eight nibbles u = w + 8, nibbles (0,4), (1,5), (2,6), (3,7)
-            // paired -> four fp16 pairs.  0x6400 | u is 1024 + u; 0x6400 | 16 u is
-            // 1024 + 16 u, which (x / 16) - 72 maps to u - 8 exactly
+            // word of eight two's complement nibbles w, nibbles (0,4), (1,5),
+            // (2,6), (3,7) paired -> four fp16 pairs.  With u = w + 8 (the nibble
+            // with its top bit flipped), 0x6400 | u is 1024 + u and 0x6400 | 16 u
+            // is 1024 + 16 u: one AND and one XOR of constants, 0x6408 flipping
+            // the low nibble's top bit and 0x6480 the high one's.  Then
+            // (1024 + u) - 1032 and (1024 + 16 u) / 16 - 72 are w exactly
             auto cvt = [](uint32_t pw, uint32_t* o) {
                 const __half2 b0 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));   // 1032
                 const __half2 s1 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));   // 1/16
@@ -482,7 +488,7 @@ w4a4_sk_kernel(const UsKParams p) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t v = j ? pw >> 8 : pw;
-                    uint32_t l = (v & 0x000F000Fu) | 0x64006400u, h = (v & 0x00F000F0u) | 0x64006400u;
+                    uint32_t l = (v & 0x000F000Fu) ^ 0x64086408u, h = (v & 0x00F000F0u) ^ 0x64806480u;
                     const __half2 fl = __hsub2(*reinterpret_cast<const __half2*>(&l), b0);
                     const __half2 fh = __hfma2(*reinterpret_cast<const __half2*>(&h), s1, b1);
                     o[2 * j] = *reinterpret_cast<const uint32_t*>(&fl);
