@@ -32,6 +32,12 @@
 // deterministic protocol (the last CTA of a band adds the slices in slice
 // order and clears them).
 //
+// Launches overlap (programmatic dependent launch): a CTA starts while the
+// previous kernel drains; with US_BITMAP_STATIC weights its issuing lanes
+// request the first stages' bitmaps and value runs before the dependency
+// wait and the activation tiles after it; nothing else global is read or
+// written before the wait.
+//
 // Every wait is bounded (US_ERR_TIMEOUT); offsets that are not a valid run
 // and runs shorter than their bitmap's popcount record US_ERR_CORRUPT and
 // the tile is skipped, so no access leaves its buffer.
@@ -114,6 +120,8 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
     uint8_t* strip_g = stages + kGroups * kStages * S::kStage + warp * kStripBytes;
     const uint32_t strip = us::smem_addr(strip_g);
 
+    const bool early = (p.flags & US_BITMAP_STATIC) != 0;   // weights may be fetched before the wait
+    if (!early) us::pdl_wait();
     for (int q = threadIdx.x; q <= nk; q += kThreads) offs[q] = p.tile_off[tile0 + q];
     if (threadIdx.x < kGroups * kStages) {
         us::mbar_init(&h.full[threadIdx.x / kStages][threadIdx.x % kStages], 1);
@@ -121,13 +129,16 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
     }
     us::fence_mbar_init();
     __syncthreads();
+    us::pdl_launch_dependents();
 
     // the group's tiles: q = grp + kGroups * r, r = 0 .. nr - 1
     const int nr = nk > grp ? (nk - grp + kGroups - 1) / kGroups : 0;
     uint8_t* gstages = stages + grp * kStages * S::kStage;
     const bool issuer = sw == 0 && lane == 0;
 
-    auto issue = [&](int r) {            // the group's issuing lane only
+    // a stage's three copies complete on its full barrier: the weights
+    // (bitmap, value run; the barrier expects all three) and the activations
+    auto issue_w = [&](int r) {          // the group's issuing lane only
         const int st = r % kStages;
         const int q = grp + kGroups * r;
         uint8_t* sp = gstages + st * S::kStage;
@@ -138,12 +149,20 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
         const uint32_t len = ok ? o1 - o0 : 0u;
         h.len[grp][st] = len;
         us::mbar_arrive_expect_tx(&h.full[grp][st], S::kXBytes + kBmBytes + len * 2u);
-        tma_load_2d(us::smem_addr(sp), &xmap, (kt0 + q) * 64, tb * TB, &h.full[grp][st]);
         us::bulk_g2s(sp + S::kXBytes, p.bitmap + (tile0 + q) * 64, kBmBytes, &h.full[grp][st]);
         if (len) us::bulk_g2s(sp + S::kXBytes + kBmBytes, p.values + (uint64_t)o0 * 2u, len * 2u, &h.full[grp][st]);
     };
+    auto issue_x = [&](int r) {
+        const int st = r % kStages;
+        const int q = grp + kGroups * r;
+        tma_load_2d(us::smem_addr(gstages + st * S::kStage), &xmap, (kt0 + q) * 64, tb * TB, &h.full[grp][st]);
+    };
     if (issuer)
-        for (int r = 0; r < nr && r < kStages; ++r) issue(r);
+        for (int r = 0; r < nr && r < kStages; ++r) issue_w(r);
+    // everything below reads the activations or writes global memory
+    if (early) us::pdl_wait();
+    if (issuer)
+        for (int r = 0; r < nr && r < kStages; ++r) issue_x(r);
 
     float acc[NB][4];
 #pragma unroll
@@ -240,7 +259,10 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
         __syncwarp();
         if (lane == 0) us::mbar_arrive(&h.empty[grp][st]);
         if (issuer && r + kStages < nr) {
-            if (us::mbar_wait(&h.empty[grp][st], ph, p.status)) issue(r + kStages);
+            if (us::mbar_wait(&h.empty[grp][st], ph, p.status)) {
+                issue_w(r + kStages);
+                issue_x(r + kStages);
+            }
         }
         __syncwarp();                           // reconverge before the warp-wide ldmatrix / mma
 
@@ -328,9 +350,17 @@ us_status launch_nb(const UsKParams& p, cudaStream_t st) {
     auto kern = spmm_f16_dec_kernel<NB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
-    const dim3 grid((unsigned)(p.nTM * p.split), (unsigned)((p.N + 8 * NB - 1) / (8 * NB)));
-    kern<<<grid, kThreads, smem, st>>>(p, map);
-    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.nTM * p.split), (unsigned)((p.N + 8 * NB - 1) / (8 * NB)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p, map) == cudaSuccess ? US_OK : US_ERR_CUDA;
 }
 
 }  // namespace
