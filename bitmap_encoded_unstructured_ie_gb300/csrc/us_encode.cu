@@ -8,12 +8,18 @@
 // section 4.1), each tile's run padded to 16 bytes (same page, 4.2.3).
 //
 // Three launches:
-//   1. count: one CTA per tile builds the tile's 64-bit words with warp
-//      ballots over the scan positions and stores P_t (its popcount);
+//   1. count: one CTA per tile builds the tile's 64-bit words and stores P_t
+//      (its popcount);
 //   2. scan:  one CTA turns roundup(P_t, E) into the exclusive prefix tile_off;
 //   3. pack:  one CTA per tile ranks its set positions (word prefix +
 //      masked popcount), compacts them in shared memory and writes the run,
 //      zero padding included, with 16-byte stores.
+// Row-scan tiles 64 columns wide (a row of the tile is one bitmap word) whose
+// rows start on 16-byte boundaries take count and pack kernels that read W
+// 16 bytes per lane: the nonzero bytes / halves of a load become mask bits by
+// word-parallel bit tricks, and the lanes of one row combine their pieces of
+// the row word by shuffles.  Every other shape takes kernels that read W one
+// element per lane, with warp ballots over the scan positions.
 #include "us_common.cuh"
 #include "us_internal.h"
 
@@ -73,7 +79,9 @@ enc_count_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nT
     }
 }
 
-// Exclusive scan of the padded run lengths; one CTA of 1024 threads.
+// Exclusive scan of the padded run lengths; one CTA of 1024 threads, four
+// tiles a thread per pass (counts is 16-byte aligned, passes start at
+// multiples of 4096 tiles), so a 4096-tile matrix takes one pass.
 __global__ void __launch_bounds__(1024)
 enc_scan_kernel(const uint32_t* __restrict__ counts, int64_t nT, int E, uint32_t* __restrict__ tile_off,
                 unsigned* status) {
@@ -82,11 +90,23 @@ enc_scan_kernel(const uint32_t* __restrict__ counts, int64_t nT, int E, uint32_t
     if (threadIdx.x == 0) { carry_s = 0; tile_off[0] = 0; }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int64_t base = 0; base < nT; base += 1024) {
-        const int64_t t = base + threadIdx.x;
-        uint32_t v = 0;
-        if (t < nT) v = (counts[t] + (uint32_t)E - 1u) / (uint32_t)E * (uint32_t)E;
-        uint32_t incl = v;
+    for (int64_t base = 0; base < nT; base += 4096) {
+        const int64_t t0 = base + 4 * (int64_t)threadIdx.x;
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+        if (t0 + 3 < nT) {
+            const uint4 c = *reinterpret_cast<const uint4*>(counts + t0);
+            v[0] = c.x; v[1] = c.y; v[2] = c.z; v[3] = c.w;
+        } else {
+            for (int i = 0; i < 4; ++i)
+                if (t0 + i < nT) v[i] = counts[t0 + i];
+        }
+        uint32_t mine = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i] = (v[i] + (uint32_t)E - 1u) / (uint32_t)E * (uint32_t)E;
+            mine += v[i];
+        }
+        uint32_t incl = mine;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
@@ -104,11 +124,14 @@ enc_scan_kernel(const uint32_t* __restrict__ counts, int64_t nT, int E, uint32_t
             wsum[lane] = s;   // inclusive over warps
         }
         __syncthreads();
-        const uint64_t carry = carry_s;
-        const uint64_t prefix = carry + (warp > 0 ? wsum[warp - 1] : 0u) + incl;
-        if (t < nT) {
-            if (prefix >= (1ull << 32)) us::set_status(status, US_ERR_TOO_LARGE);
-            tile_off[t + 1] = (uint32_t)prefix;
+        uint64_t prefix = carry_s + (warp > 0 ? wsum[warp - 1] : 0u) + incl - mine;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            prefix += v[i];
+            if (t0 + i < nT) {
+                if (prefix >= (1ull << 32)) us::set_status(status, US_ERR_TOO_LARGE);
+                tile_off[t0 + i + 1] = (uint32_t)prefix;
+            }
         }
         __syncthreads();
         if (threadIdx.x == 1023) carry_s = prefix;
@@ -216,6 +239,196 @@ enc_pack_kernel(const void* __restrict__ W, int64_t ldw, int TM, int TK, int nTK
         *reinterpret_cast<uint4*>(dst + q) = make_uint4(v[0], v[1], v[2], v[3]);
     }
     (void)EB;
+}
+
+// -------------------------------------- row-scan tiles 64 columns wide --
+// Bit k of the result is set iff byte k of the 16 bytes is nonzero: for each
+// word, (x & 0x7F..) + 0x7F.. carries into bit 7 of every byte whose low seven
+// bits are not all zero; OR-ing x covers the top bit; the four byte flags
+// (bits 0, 8, 16, 24 after the shift) are gathered into bits 24..27 by one
+// multiplication by 2^24 + 2^17 + 2^10 + 2^3 (no two partial products share
+// a bit below 28).
+__device__ __forceinline__ uint32_t nz_bytes16(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const uint32_t t = ((((w[r] & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w[r]) & 0x80808080u) >> 7;
+        m |= ((t * 0x01020408u) >> 24) << (4 * r);
+    }
+    return m;
+}
+// Bit k set iff half k of the 8 halves is nonzero (+0 and -0 count as zero).
+__device__ __forceinline__ uint32_t nz_halves8(uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const uint32_t t = (((w[r] & 0x7FFF7FFFu) + 0x7FFF7FFFu) & 0x80008000u) >> 15;   // bits 0 and 16
+        m |= ((t | (t >> 15)) & 3u) << (2 * r);
+    }
+    return m;
+}
+// Nonzero if some byte of the 16 lies outside the code range [-lim, lim - 1]
+// (lim = 8 for int4, 2 for int2): bytes + lim, added byte by byte, must stay
+// below 2 lim.
+__device__ __forceinline__ uint32_t out_of_range16(uint4 v, uint32_t lim) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t add = lim * 0x01010101u, bad = (~(2u * lim - 1u) & 0xFFu) * 0x01010101u;
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r |= (((w[i] & 0x7F7F7F7Fu) + add) ^ (w[i] & 0x80808080u)) & bad;
+    return r;
+}
+
+// ELEM's 16-byte loads: LPR lanes per tile row (64 elements), RPW rows per warp
+template <int ELEM>
+struct Row64 {
+    static constexpr int kLPR = ELEM == US_F16 ? 8 : 4;
+    static constexpr int kRPW = 32 / kLPR;
+    static constexpr int kBPL = 64 / kLPR;          // mask bits per lane
+    static constexpr int kEB = ELEM == US_F16 ? 2 : 1;
+};
+
+template <int ELEM>
+__global__ void __launch_bounds__(kEncThreads)
+enc_count_row64_kernel(const void* __restrict__ W, int64_t ldw, int TM, int nTK, uint64_t* __restrict__ bitmap,
+                       uint32_t* __restrict__ counts, unsigned* status) {
+    using R = Row64<ELEM>;
+    const int t = blockIdx.x;
+    const int tm = t / nTK, tk = t - tm * nTK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg = lane % R::kLPR, rsub = lane / R::kLPR;
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(W) + ((int64_t)tm * TM * ldw + (int64_t)tk * 64) * R::kEB;
+    __shared__ int warp_sum[kEncThreads / 32];
+    int my = 0;
+    for (int r0 = warp * R::kRPW; r0 < TM; r0 += (kEncThreads / 32) * R::kRPW) {
+        const int row = r0 + rsub;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)row * ldw * R::kEB) + seg);
+        const uint32_t m = ELEM == US_F16 ? nz_halves8(v) : nz_bytes16(v);
+        if (ELEM != US_F16 && out_of_range16(v, ELEM == US_I4 ? 8u : 2u)) us::set_status(status, US_ERR_INVALID_ARG);
+        uint64_t word = (uint64_t)m << (R::kBPL * seg);
+#pragma unroll
+        for (int d = 1; d < R::kLPR; d <<= 1) word |= __shfl_xor_sync(0xffffffffu, word, d);
+        if (seg == 0) bitmap[(int64_t)t * TM + row] = word;
+        my += __popc(m);
+    }
+#pragma unroll
+    for (int d = 16; d; d >>= 1) my += __shfl_xor_sync(0xffffffffu, my, d);
+    if (lane == 0) warp_sum[warp] = my;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int sum = 0;
+        for (int i = 0; i < kEncThreads / 32; ++i) sum += warp_sum[i];
+        counts[t] = (uint32_t)sum;
+    }
+}
+
+template <int ELEM>
+__global__ void __launch_bounds__(kEncThreads)
+enc_pack_row64_kernel(const void* __restrict__ W, int64_t ldw, int TM, int nTK, const uint64_t* __restrict__ bitmap,
+                      const uint32_t* __restrict__ tile_off, uint8_t* __restrict__ values, uint64_t values_cap,
+                      unsigned* status) {
+    using R = Row64<ELEM>;
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int t = blockIdx.x;
+    const int tm = t / nTK, tk = t - tm * nTK;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg = lane % R::kLPR, rsub = lane / R::kLPR;
+    uint32_t* wpre = reinterpret_cast<uint32_t*>(smem);                // TM row prefixes
+    uint8_t* cbuf = smem + TM * 4;                                     // compacted elements, 1 or 2 bytes each
+    __shared__ uint32_t warp_tot[kEncThreads / 32];
+
+    const uint64_t o0 = tile_off[t], o1 = tile_off[t + 1];
+    const int bits = (ELEM == US_F16) ? 16 : (ELEM == US_I4 ? 4 : 2);
+    if (o1 < o0 || o1 * bits > values_cap * 8 || o1 - o0 > (uint64_t)TM * 64) {
+        if (threadIdx.x == 0) us::set_status(status, US_ERR_WORKSPACE);
+        return;
+    }
+    const uint64_t* words = bitmap + (int64_t)t * TM;
+    // exclusive prefix of the row popcounts (TM <= 256: one row a thread)
+    const uint32_t c = threadIdx.x < TM ? (uint32_t)__popcll(words[threadIdx.x]) : 0u;
+    uint32_t incl = c;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += o;
+    }
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, P = 0;
+    for (int i = 0; i < kEncThreads / 32; ++i) {
+        if (i < warp) before += warp_tot[i];
+        P += warp_tot[i];
+    }
+    if (threadIdx.x < TM) wpre[threadIdx.x] = before + incl - c;
+    const uint32_t run = (uint32_t)(o1 - o0);
+    if (P > run) {                           // cannot happen after enc_scan; guard anyway
+        if (threadIdx.x == 0) us::set_status(status, US_ERR_CORRUPT);
+        return;
+    }
+    // the padding elements of the run are zero
+    for (uint32_t e = P + threadIdx.x; e < run; e += kEncThreads) {
+        if (ELEM == US_F16) reinterpret_cast<uint16_t*>(cbuf)[e] = 0;
+        else cbuf[e] = 0;
+    }
+    __syncthreads();
+
+    // each lane: its 16-byte piece of a row, its set elements to their ranks
+    const uint8_t* base = reinterpret_cast<const uint8_t*>(W) + ((int64_t)tm * TM * ldw + (int64_t)tk * 64) * R::kEB;
+    for (int r0 = warp * R::kRPW; r0 < TM; r0 += (kEncThreads / 32) * R::kRPW) {
+        const int row = r0 + rsub;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)row * ldw * R::kEB) + seg);
+        const uint64_t word = words[row];
+        uint32_t m = (uint32_t)(word >> (R::kBPL * seg)) & ((1u << R::kBPL) - 1u);
+        uint32_t rank = wpre[row] + (uint32_t)__popcll(word & ((1ull << (R::kBPL * seg)) - 1ull));
+        const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+        while (m) {
+            const int k = __ffs(m) - 1;
+            m &= m - 1u;
+            if (ELEM == US_F16) {
+                reinterpret_cast<uint16_t*>(cbuf)[rank++] = (uint16_t)(vw[k >> 1] >> (16 * (k & 1)));
+            } else {
+                cbuf[rank++] = (uint8_t)((vw[k >> 2] >> (8 * (k & 3))) & (ELEM == US_I4 ? 0x0Fu : 0x03u));
+            }
+        }
+    }
+    __syncthreads();
+
+    // write the run, 16 bytes per thread-step (the run is a whole number of 16 bytes)
+    const uint32_t run_bytes = run * (uint32_t)bits / 8u;
+    uint8_t* dst = values + o0 * bits / 8;
+    for (uint32_t q = threadIdx.x * 16u; q < run_bytes; q += kEncThreads * 16u) {
+        uint4 out;
+        if (ELEM == US_F16) {
+            out = *reinterpret_cast<const uint4*>(cbuf + q);
+        } else if (ELEM == US_I4) {
+            // 32 elements, one per byte -> 16 bytes of nibble pairs (earlier low)
+            const uint4 a = *reinterpret_cast<const uint4*>(cbuf + 2 * q);
+            const uint4 b = *reinterpret_cast<const uint4*>(cbuf + 2 * q + 16);
+            auto pair2 = [](uint32_t x, uint32_t y) {
+                return __byte_perm(x | (x >> 4), y | (y >> 4), 0x6420u);
+            };
+            out = make_uint4(pair2(a.x, a.y), pair2(a.z, a.w), pair2(b.x, b.y), pair2(b.z, b.w));
+        } else {
+            // 64 elements -> 16 bytes, four per byte (earlier lower)
+            uint32_t o[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 a = *reinterpret_cast<const uint4*>(cbuf + 4 * q + 16 * i);
+                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+                uint32_t word = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t x = aw[j];
+                    word |= ((x | (x >> 6) | (x >> 12) | (x >> 18)) & 0xFFu) << (8 * j);
+                }
+                o[i] = word;
+            }
+            out = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        *reinterpret_cast<uint4*>(dst + q) = out;
+    }
 }
 
 // ---------------------------------------------------- IE-BME with areas --
@@ -404,11 +617,41 @@ size_t encode_pack_smem(int TM, int TK, int elem) {
     return (size_t)((nw * 4 + 15) & ~15) + (size_t)TM * TK * (elem == US_F16 ? 2 : 1);
 }
 
+// The 16-byte-load kernels: row scan, 64-column tiles, W and every row start
+// 16-byte aligned.
+template <int ELEM>
+us_status launch_encode_row64(const void* W, int64_t ldw, int TM, int nTK, int64_t nT, uint64_t* bitmap,
+                              uint32_t* tile_off, void* values, size_t values_cap, uint32_t* counts, unsigned* status,
+                              cudaStream_t st) {
+    enc_count_row64_kernel<ELEM><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, nTK, bitmap, counts, status);
+    if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
+    enc_scan_kernel<<<1, 1024, 0, st>>>(counts, nT, ELEM == US_F16 ? 8 : (ELEM == US_I4 ? 32 : 64), tile_off, status);
+    if (cudaGetLastError() != cudaSuccess) return US_ERR_CUDA;
+    const size_t smem = (size_t)TM * 4 + (size_t)TM * 64 * (ELEM == US_F16 ? 2 : 1);
+    if (cudaFuncSetAttribute(enc_pack_row64_kernel<ELEM>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return US_ERR_CUDA;
+    enc_pack_row64_kernel<ELEM><<<(unsigned)nT, kEncThreads, smem, st>>>(W, ldw, TM, nTK, bitmap, tile_off,
+                                                                         (uint8_t*)values, values_cap, status);
+    return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
+}
+
 us_status launch_encode(const void* W, int64_t ldw, int M, int K, int TM, int TK, int elem, int order,
                         uint64_t* bitmap, uint32_t* tile_off, void* values, size_t values_cap,
                         uint32_t* counts, unsigned* status, cudaStream_t st) {
     const int nTM = M / TM, nTK = K / TK;
     const int64_t nT = (int64_t)nTM * nTK;
+    const int eb = elem == US_F16 ? 2 : 1;
+    if (order == US_ORDER_ROW && TK == 64 && (reinterpret_cast<uintptr_t>(W) & 15u) == 0 && (ldw * eb) % 16 == 0) {
+        if (elem == US_F16)
+            return launch_encode_row64<US_F16>(W, ldw, TM, nTK, nT, bitmap, tile_off, values, values_cap, counts,
+                                               status, st);
+        if (elem == US_I4)
+            return launch_encode_row64<US_I4>(W, ldw, TM, nTK, nT, bitmap, tile_off, values, values_cap, counts,
+                                              status, st);
+        return launch_encode_row64<US_I2>(W, ldw, TM, nTK, nT, bitmap, tile_off, values, values_cap, counts, status,
+                                          st);
+    }
     const size_t smem = encode_pack_smem(TM, TK, elem);
     if (elem == US_F16) {
         enc_count_kernel<US_F16><<<(unsigned)nT, kEncThreads, 0, st>>>(W, ldw, TM, TK, nTK, order, bitmap, counts,
