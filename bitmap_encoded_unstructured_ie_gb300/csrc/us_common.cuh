@@ -106,20 +106,6 @@ US_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* status) {
     return mbar_wait_for(bar, parity, status, kWaitLimitNs);
 }
 
-// As mbar_wait, polling without the suspend hint (for a thread whose next
-// step is on the critical path as soon as the phase completes); the timer is
-// read every 64 polls.
-US_DEV bool mbar_wait_spin(uint64_t* bar, uint32_t parity, unsigned* status) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((n & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
-            set_status(status, US_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
 
 // Bulk copy global -> shared (TMA, 1-D, no tensor map), completing `bytes`
 // transactions on `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
