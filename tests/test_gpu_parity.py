@@ -103,12 +103,54 @@ def test_encode_strided_input_and_signed_zero(us, orc):
     assert np.array_equal(bm, obm) and np.array_equal(off, ooff) and np.array_equal(vals, ovals)
 
 
+@pytest.mark.parametrize("elem", [F16, I4, 2])
+@pytest.mark.parametrize("TM", [64, 128, 256])
+def test_encode_row64_tiles_match_oracle(us, orc, TM, elem):
+    """Row-scan tiles 64 columns wide take the 16-byte-load count and pack
+    kernels (fp16 up to 128-row tiles): every tile height, element type and
+    density, a strided input whose rows stay 16-byte aligned (same kernels) and
+    one shifted by an element (the one-element-per-lane kernels), all equal to
+    the oracle byte for byte."""
+    M, K = 512, 448
+    rng = np.random.default_rng(TM + 7 * elem)
+    for density in (0.0, 0.004, 0.5, 1.0):
+        if elem == F16:
+            W = rand_f16(rng, M, K, density)
+        else:
+            lo, hi = (-8, 8) if elem == I4 else (-2, 2)
+            W = rng.integers(lo, hi, size=(M, K)).astype(np.int8)
+            W[rng.random((M, K)) >= density] = 0
+        E = encode_gpu(us, W, TM, 64, elem, ROW)
+        bm, off, vals = gpu_arrays(E)
+        obm, ooff, ovals = orc.encode(W, TM, 64, elem, ROW)
+        assert np.array_equal(bm, obm) and np.array_equal(off, ooff) and np.array_equal(vals, ovals), density
+    for shift in (64, 1):
+        view = W.view(np.int16) if elem == F16 else W
+        big = np.zeros((M, K + 128), view.dtype)
+        big[:, shift:shift + K] = view
+        Wt = torch.from_numpy(big).cuda()[:, shift:shift + K]
+        E = us.us_encode(Wt, TM, 64, elem, ROW)
+        torch.cuda.synchronize()
+        assert us.us_get_last_device_status() == us.US_OK
+        bm, off, vals = gpu_arrays(E)
+        assert np.array_equal(bm, obm) and np.array_equal(off, ooff) and np.array_equal(vals, ovals), shift
+
+
 def test_encode_reports_out_of_range_codes(us):
     W = torch.zeros(64, 64, dtype=torch.int8, device="cuda")
     W[3, 4] = 9
     us.us_encode(W, 64, 64, I4, ROW)
     assert us.us_get_last_device_status() == us.US_ERR_INVALID_ARG
     assert us.us_get_last_device_status() == us.US_OK        # cleared by the read
+    for v in (2, -3):                                         # int2 codes lie in [-2, 1]
+        W2 = torch.zeros(128, 128, dtype=torch.int8, device="cuda")
+        W2[70, 100] = v
+        us.us_encode(W2, 64, 64, 2, ROW)
+        assert us.us_get_last_device_status() == us.US_ERR_INVALID_ARG
+    W8 = torch.full((64, 64), -8, dtype=torch.int8, device="cuda")   # the int4 range's ends pass
+    W8[:, 1::2] = 7
+    us.us_encode(W8, 64, 64, I4, ROW)
+    assert us.us_get_last_device_status() == us.US_OK
 
 
 # -------------------------------------------------------------------- W4A4 --
