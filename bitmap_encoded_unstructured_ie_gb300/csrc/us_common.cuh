@@ -246,7 +246,7 @@ US_DEV void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a
 // 4 + r/2 of the odd one.  Clear positions take byte 7 (rank 7), which the
 // masked window leaves empty unless all eight positions are set.  Low 16 bits
 // cover positions 0-3, high 16 bits positions 4-7.
-US_DEV uint32_t make_sel(uint32_t v) {
+__host__ __device__ constexpr uint32_t make_sel(uint32_t v) {
     uint32_t sel = 0, r = 0;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {

@@ -61,11 +61,46 @@ struct SkSmem {
     uint32_t pos[kR];                       // ring offset of the chunk in slot s
     uint32_t bad[kR];                       // its offsets failed the checks
     uint32_t abort;
+    // this CTA's tile range [t0, t1), its first band, its band count, the
+    // highest CTA sharing its last band, and t0's K tile: worked out once by
+    // thread 0 (divisions by launch values), read by all after the barrier
+    int t0, t1, band0, nb, c_hi, tk0;
 };
 static_assert(sizeof(SkSmem) <= kHeader, "header");
 
 __host__ __device__ inline int sk_cta_of(int64_t t, int G, int nT) { return (int)(((t + 1) * G - 1) / nT); }
 __host__ __device__ inline int sk_start(int c, int G, int nT) { return (int)((int64_t)c * nT / G); }
+
+// Selector table entries {selector pair, odd-rank mask | popcount} for both
+// consumers, generated at compile time (mma: 1).  The selectors move rank r
+// to position p (make_sel); the consumer asks for a position order.  The dp4a
+// consumer takes (p0 p2 p4 p6 | p1 p3 p5 p7), which packs the positions in the
+// order of the packed activations (position 2i low, 2i + 1 high in byte i);
+// the mma one (p0 p4 p1 p5 | p2 p6 p3 p7), the nibble order that its fp16
+// conversion pairs up.  Clear positions take rank 7's byte, which the
+// odd-rank mask empties unless all eight positions are set.  Only high
+// nibbles of the odd/even bytes reach the dense word, so the mask's lowest
+// nibble carries the byte's popcount (POPC issues at a quarter of the
+// logic-op rate on this GPU; this costs one AND).
+struct SelEntry { uint32_t sel, mask; };
+struct SelTable { SelEntry e[2][256]; };
+constexpr SelTable build_sel_table() {
+    SelTable t{};
+    for (int mma = 0; mma < 2; ++mma)
+        for (uint32_t e = 0; e < 256; ++e) {
+            const uint32_t sel = us::make_sel(e);
+            uint32_t ps = 0, pop = 0;
+            for (int i = 0; i < 8; ++i) {
+                const int to = mma ? ((i & 3) * 2 + (i >> 2)) : ((i & 1) * 4 + (i >> 1));
+                ps |= ((sel >> (4 * i)) & 0xFu) << (4 * to);
+                pop += (e >> i) & 1u;
+            }
+            t.e[mma][e].sel = ps;
+            t.e[mma][e].mask = (e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u) | pop;
+        }
+    return t;
+}
+__device__ const SelTable kSelTable = build_sel_table();
 
 
 // Eight int2 values (low 16 bits, the earlier value in the lower bits) as
@@ -96,8 +131,6 @@ w4a4_sk_kernel(const UsKParams p) {
     const uint32_t D = (uint32_t)p.sk_ring;
     const int nT = p.nTM * p.nTK, G = p.sk_grid;
     const int cta = blockIdx.x;
-    const int t0 = sk_start(cta, G, nT), t1 = sk_start(cta + 1, G, nT);
-    const int per = t1 - t0;
     uint32_t* offs = reinterpret_cast<uint32_t*>(ring + D);                       // per + 1
     // activations as given (packed int4): NTOK x xcols x XROW bytes; column xq of
     // token n holds K tile tk, where xq = tk when the CTAs span whole band
@@ -106,8 +139,9 @@ w4a4_sk_kernel(const UsKParams p) {
     int* accs = reinterpret_cast<int*>(xs + NTOK * p.sk_xcols * XROW);          // bands x NTOK x 64
     uint16_t* sws = reinterpret_cast<uint16_t*>(accs + p.sk_nb * NTOK * kTM);     // bands x 64 row scales
     uint16_t* sxs = sws + p.sk_nb * kTM;                                          // NTOK token scales
-    const int band0 = t0 / p.nTK;
-    const int nb = (t1 - 1) / p.nTK - band0 + 1;
+    // per tile of the range: its band (relative to band0) << 16 | its K tile
+    uint32_t* tinfo = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(sws) +
+                                                  (((size_t)p.sk_nb * kTM + NTOK) * 2 + 15) / 16 * 16);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool early = (p.flags & US_BITMAP_STATIC) != 0;   // weights may be fetched before the wait
     constexpr uint32_t kQ = 128u / WB;                      // elements per 16 bytes (run padding)
@@ -120,10 +154,23 @@ w4a4_sk_kernel(const UsKParams p) {
         }
         us::mbar_init(&S.xfull, 1);
         S.abort = 0;
+        // 32-bit divisions while G x nT fits (below 28 M tiles), else 64-bit
+        const bool n32 = (uint64_t)nT * (uint64_t)(G + 1) < (1ull << 32);
+        const int a = n32 ? (int)((uint32_t)cta * (uint32_t)nT / (uint32_t)G) : sk_start(cta, G, nT);
+        const int b = n32 ? (int)((uint32_t)(cta + 1) * (uint32_t)nT / (uint32_t)G) : sk_start(cta + 1, G, nT);
+        const int ba = (int)((uint32_t)a / (uint32_t)p.nTK), bz = (int)((uint32_t)(b - 1) / (uint32_t)p.nTK);
+        const int tl = (bz + 1) * p.nTK - 1;                  // last tile of the last band
+        S.t0 = a;
+        S.t1 = b;
+        S.band0 = ba;
+        S.nb = bz - ba + 1;
+        S.c_hi = n32 ? (int)((((uint32_t)tl + 1u) * (uint32_t)G - 1u) / (uint32_t)nT) : sk_cta_of(tl, G, nT);
+        S.tk0 = a - ba * p.nTK;
         us::fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < nb * NTOK * kTM; i += kThreads) accs[i] = 0;
+    for (int i = threadIdx.x; i < p.sk_nb * NTOK * kTM; i += kThreads) accs[i] = 0;
     __syncthreads();
+    const int t0 = S.t0, t1 = S.t1, per = t1 - t0, band0 = S.band0, nb = S.nb;
     us::pdl_launch_dependents();
 
     int issued = 0, tail = 0;                                 // producer bookkeeping (lane 0)
@@ -213,7 +260,7 @@ w4a4_sk_kernel(const UsKParams p) {
         if (lane == 0) us::mbar_arrive_expect_tx(&S.xfull, (uint32_t)p.N * row);
         __syncwarp();
         const uint8_t* xg = reinterpret_cast<const uint8_t*>(p.X);
-        const int tk0 = all_k ? 0 : t0 % p.nTK;
+        const int tk0 = all_k ? 0 : S.tk0;
         const int len1 = min(ncols, p.nTK - tk0);            // the range may wrap past the band's end
         for (int n = lane; n < p.N; n += 32) {
             const uint8_t* src = xg + (int64_t)n * (p.K / 2);
@@ -225,27 +272,11 @@ w4a4_sk_kernel(const UsKParams p) {
     }
     else {
         // ----------------------------------------------------------- consumers
-        // selector table, 16 w form: d0's bytes become the low nibbles of a
-        // packed word, d1's the high ones.  The dp4a consumer asks for
-        // (p0 p2 p4 p6 | p1 p3 p5 p7), which packs the positions in the order of
-        // the packed activations (position 2i low, 2i + 1 high in byte i); the
-        // mma one for (p0 p4 p1 p5 | p2 p6 p3 p7), the nibble order that the fp16
-        // conversion below pairs up
+        // selector table (16 w form: d0's bytes become the low nibbles of a
+        // packed word, d1's the high ones), kLutRep copies for bank spreading
         for (int e = threadIdx.x; e < 256; e += kNW * 32) {
-            const uint32_t sel = us::make_sel((uint32_t)e);
-            uint32_t ps = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // position i -> selector nibble
-                const int to = NT ? ((i & 3) * 2 + (i >> 2)) : ((i & 1) * 4 + (i >> 1));
-                ps |= ((sel >> (4 * i)) & 0xFu) << (4 * to);
-            }
-            // clear positions take rank 7's byte, which the odd-rank mask empties
-            // unless all eight positions are set.  Only high nibbles of the
-            // odd/even bytes reach the dense word, so the mask's lowest nibble
-            // carries the byte's popcount (POPC issues at a quarter of the
-            // logic-op rate on this GPU; this costs one AND)
-            const uint2 ent = make_uint2(ps, (e == 255 ? 0xF0F0F0F0u : 0x00F0F0F0u) | (uint32_t)__popc(e));
+            const SelEntry v = kSelTable.e[NT ? 1 : 0][e];
+            const uint2 ent = make_uint2(v.sel, v.mask);
 #pragma unroll
             for (int r = 0; r < kLutRep; ++r) lut[e * kLutRep + r] = ent;
         }
@@ -258,6 +289,10 @@ w4a4_sk_kernel(const UsKParams p) {
         // static weights: their row scales are fixed too
         if (p.Y && early)
             for (int i = threadIdx.x; i < nb * kTM; i += kNW * 32) sws[i] = p.s_w[band0 * kTM + i];
+        for (int i = threadIdx.x; i < per; i += kNW * 32) {
+            const uint32_t t = (uint32_t)(t0 + i), b = t / (uint32_t)p.nTK;
+            tinfo[i] = ((b - (uint32_t)band0) << 16) | (t - b * (uint32_t)p.nTK);
+        }
         us::named_bar_sync(1, kNW * 32);
 
         const uint32_t lut_lane = (uint32_t)(lane % kLutRep);
@@ -405,8 +440,8 @@ w4a4_sk_kernel(const UsKParams p) {
                     }
             };
             for (int q = warp; q < per && ok; q += kNW) {
-                const int t = t0 + q;
-                const int brel = t / p.nTK - band0;
+                const uint32_t ti = tinfo[q];
+                const int brel = (int)(ti >> 16), tk = (int)(ti & 0xFFFFu);
                 if (brel != cur_b) {
                     flush();
                     cur_b = brel;
@@ -429,7 +464,7 @@ w4a4_sk_kernel(const UsKParams p) {
                     pw[h][4] = b.x; pw[h][5] = b.y; pw[h][6] = b.z; pw[h][7] = b.w;
                 }
                 __syncwarp();                                 // the slot may be refilled next
-                const int8_t* xt = xs + (int64_t)(all_k ? t % p.nTK : q) * XROW;
+                const int8_t* xt = xs + (int64_t)(all_k ? tk : q) * XROW;
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
 #pragma unroll
@@ -496,8 +531,8 @@ w4a4_sk_kernel(const UsKParams p) {
                 }
             };
             for (int q = warp; q < per && ok; q += kNW) {
-                const int t = t0 + q;
-                const int brel = t / p.nTK - band0;
+                const uint32_t ti = tinfo[q];
+                const int brel = (int)(ti >> 16), tk = (int)(ti & 0xFFFFu);
                 if (brel != cur_b) {
                     flush();
                     cur_b = brel;
@@ -509,7 +544,7 @@ w4a4_sk_kernel(const UsKParams p) {
                 }
                 // B fragments: token 8 nt + g, positions 16 tig .. 16 tig + 15 as fp16
                 uint32_t bf[NT][8];
-                const int8_t* xt = xs + (int64_t)(all_k ? t % p.nTK : q) * XROW;
+                const int8_t* xt = xs + (int64_t)(all_k ? tk : q) * XROW;
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const uint2 v = *reinterpret_cast<const uint2*>(xt + (int64_t)(8 * nt + g) * p.sk_xcols * XROW + 8 * tig);
@@ -595,7 +630,7 @@ w4a4_sk_kernel(const UsKParams p) {
         // owned, continued by CTAs cta+1 .. c_hi, whose first band it is.  A
         // thread's loads of up to kE elements x 4 CTAs are all in flight before
         // the first is used: usually one L2 round trip for the whole band
-        const int c_hi = sk_cta_of((int64_t)(b + 1) * p.nTK - 1, G, nT);
+        const int c_hi = S.c_hi;                              // b is the last band
         constexpr int kAll = NTOK * kTM;
         constexpr int kE = (kAll + kThreads - 1) / kThreads < 4 ? (kAll + kThreads - 1) / kThreads : 4;
         for (int i0 = threadIdx.x; i0 < kAll; i0 += kE * kThreads) {
@@ -678,7 +713,7 @@ bool sk_plan(int nTM, int nTK, int N, bool pre, SkPlan& pl) {
     pl.nb = (pl.per + nTK - 1) / nTK + 1;
     const size_t fixed = kHeader + kLutBytes + (size_t)((pl.per + 1 + 3) & ~3) * 4 +
                          (size_t)ntok * pl.xcols * (kTK / 2) + (size_t)pl.nb * ntok * kTM * 4 +
-                         (((size_t)pl.nb * kTM + ntok) * 2 + 15) / 16 * 16;
+                         (((size_t)pl.nb * kTM + ntok) * 2 + 15) / 16 * 16 + (size_t)(pl.per * 4 + 15) / 16 * 16;
     // every warp needs a slot of its own; static weights want one per tile
     const int want = pre ? (pl.per > nw ? pl.per : nw) : nw;
     for (size_t budget : {kSmemTwoPerSm, kSmemMax}) {
