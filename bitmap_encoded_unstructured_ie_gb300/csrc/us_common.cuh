@@ -132,6 +132,18 @@ US_DEV void bulk_prefetch_l2(const void* src, uint32_t bytes) {
 US_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 US_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// One three-input logic op: bit i of the result is bit (a_i b_i c_i) of LUT,
+// the truth table over a = 0xF0, b = 0xCC, c = 0xAA.  Written out because
+// the compiler does not always merge a mask-and-combine into one.
+template <uint32_t LUT>
+US_DEV uint32_t lop3(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, %4;" : "=r"(d) : "r"(a), "r"(b), "r"(c), "n"(LUT));
+    return d;
+}
+constexpr uint32_t kLopAndXor = (0xF0u & 0xCCu) ^ 0xAAu;                  // (a & b) ^ c
+constexpr uint32_t kLopMux = (0xF0u & 0xCCu) | (0xAAu & ~0xCCu & 0xFFu);   // (a & b) | (c & ~b)
+
 // Named barrier over the first `threads` threads (a multiple of 32), id 1..15.
 US_DEV void named_bar_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -364,12 +364,14 @@ w4a4_sk_kernel(const UsKParams p) {
                                                  : int2x8_to_int4x8(__funnelshift_r(cur[h], nxt[h], ob[h] << 1));
                     const uint2 ent = lut[bb * kLutRep + lut_lane];
                     const uint32_t odd = win & ent.y;                       // 16 w, ranks 1,3,5,(7)
-                    const uint32_t even = (win << 4) & 0xF0F0F0F0u;         // 16 w, ranks 0,2,4,6
+                    // 16 w, ranks 0,2,4,6; the low nibbles that the shift brings in
+                    // are dropped with the odd bytes' by the pack below
+                    const uint32_t even = win << 4;
                     const uint32_t d0 = __byte_perm(even, odd, ent.x);
                     const uint32_t d1 = __byte_perm(even, odd, ent.x >> 16);
                     // byte i = d0's nibble i | d1's nibble i << 4 (two's complement;
                     // the mma consumer's fp16 conversion adds the bias of 8)
-                    pw[h][bt] = ((d0 >> 4) & 0x0F0F0F0Fu) | (d1 & 0xF0F0F0F0u);
+                    pw[h][bt] = us::lop3<us::kLopMux>(d0 >> 4, 0x0F0F0F0Fu, d1);
                     ob[h] += ent.y & 0xFu;
                 }
             }
@@ -523,7 +525,8 @@ w4a4_sk_kernel(const UsKParams p) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const uint32_t v = j ? pw >> 8 : pw;
-                    uint32_t l = (v & 0x000F000Fu) ^ 0x64086408u, h = (v & 0x00F000F0u) ^ 0x64806480u;
+                    uint32_t l = us::lop3<us::kLopAndXor>(v, 0x000F000Fu, 0x64086408u);
+                    uint32_t h = us::lop3<us::kLopAndXor>(v, 0x00F000F0u, 0x64806480u);
                     const __half2 fl = __hsub2(*reinterpret_cast<const __half2*>(&l), b0);
                     const __half2 fh = __hfma2(*reinterpret_cast<const __half2*>(&h), s1, b1);
                     o[2 * j] = *reinterpret_cast<const uint32_t*>(&fl);
@@ -552,8 +555,9 @@ w4a4_sk_kernel(const UsKParams p) {
                     for (int hh = 0; hh < 2; ++hh) {
                         const uint32_t w = hh ? v.y : v.x;
                         // w + 8 per element: element 2i in byte i of lo, 2i + 1 in byte i of hi
-                        const uint4 h = us::u8x8_to_f16x8((w & 0x0F0F0F0Fu) ^ 0x08080808u,
-                                                         ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u, 0x73625140u);
+                        const uint4 h = us::u8x8_to_f16x8(us::lop3<us::kLopAndXor>(w, 0x0F0F0F0Fu, 0x08080808u),
+                                                         us::lop3<us::kLopAndXor>(w >> 4, 0x0F0F0F0Fu, 0x08080808u),
+                                                         0x73625140u);
                         bf[nt][4 * hh + 0] = h.x;
                         bf[nt][4 * hh + 1] = h.y;
                         bf[nt][4 * hh + 2] = h.z;
