@@ -357,18 +357,18 @@ def kernel_name(N: int) -> str:
     return "spmm_generic_kernel<I4,64>"
 
 
-KERNEL_SOURCES = {"w4a4_sk_kernel": "us_w4a4_sk.cu",
-                  "w4a4_small_n_kernel": "us_w4a4.cu", "spmm_generic_kernel": "us_spmm.cu"}
+KERNEL_SOURCES = {"w4a4_sk_kernel": ("us_w4a4_sk.cuh", "us_w4a4_sk.cu"),
+                  "w4a4_small_n_kernel": ("us_w4a4.cu",), "spmm_generic_kernel": ("us_spmm.cu",)}
 
 
 def kernel_source_sha(kernel: str):
-    """sha256 over the kernel's translation unit and the shared device header."""
+    """sha256 over the kernel's source files and the shared device header."""
     import hashlib
-    src = KERNEL_SOURCES.get(kernel.split("<")[0])
-    if not src:
+    srcs = KERNEL_SOURCES.get(kernel.split("<")[0])
+    if not srcs:
         return None
     h = hashlib.sha256()
-    for f in (src, "us_common.cuh"):
+    for f in (*srcs, "us_common.cuh"):
         with open(os.path.join(ROOT, "bitmap_encoded_unstructured_ie_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -779,17 +779,38 @@ def measure_extras(us, torch, wl, dev, stream, hbm_peak, bf16_peak, cpu=True):
     perm = us.us_reorder_rows(d["Wq"], 16, 64, 2, 2, us.US_I4)
     reorder_s = _t.time() - t_re
     permt = torch.from_numpy(perm).to(dev)
+    swi = torch.from_numpy(d["s_w"].view(np.int16)).to(dev)
     for name, pm in (("areas_2x2_16x64", None), ("areas_2x2_16x64_reordered", permt)):
         Ei = us.us_encode_ie(Wq, 16, 64, 2, 2, us.US_I4, pm)
-        row = {"bitmap_bytes": Ei.E.bitmap.numel() * 8, "value_bytes": Ei.E.values_bytes,
-               "perm_bytes": 0 if pm is None else pm.numel(),
-               "total_bytes": Ei.E.nbytes() + (0 if pm is None else pm.numel())}
+        Ei.E.flags = us.US_BITMAP_STATIC
+        pbytes = 0 if pm is None else pm.numel()
+        wbytes = Ei.E.nbytes() + pbytes
+        ni = max(2, math.ceil(2.2 * l2 / wbytes))      # rotating copies: every launch reads from HBM
+        cpi = [Ei] + [us.EncodedIE(us.Encoded(Ei.E.M, Ei.E.K, 16, 64, Ei.E.elem, Ei.E.order, Ei.E.bitmap.clone(),
+                                              Ei.E.tile_off.clone(), Ei.E.values.clone(), Ei.E.values_bytes,
+                                              us.US_BITMAP_STATIC), 2, 2, None if pm is None else pm.clone())
+                      for _ in range(ni - 1)]
+        row = {"bitmap_bytes": Ei.E.bitmap.numel() * 8, "value_bytes": Ei.E.values_bytes, "perm_bytes": pbytes,
+               "total_bytes": wbytes, "copies": ni,
+               "kernel": "balanced" if us.us_pick_split_k_ie(Ei, 1) == 0 else "generic"}
         for N in (1, 8, 16):
             X = torch.from_numpy(wl.pack_int4(d["Xq"][:N])).to(dev)
+            sxi = torch.from_numpy(d["s_x"][:N].view(np.int16)).to(dev)
             Ya = torch.empty(N, 4096, dtype=torch.int32, device=dev)
+            Yh = torch.empty(N, 4096, dtype=torch.int16, device=dev)
             wsi = us.workspace_ie(Ei, N)
-            ms = time_graph(torch, stream, us, lambda: us.us_spmm_w4a4_ie(Ei, X, None, None, N, Ya, None, wsi, 0, stream), 20)
-            row[f"N{N}_us"] = round(ms * 1e3, 2)
+            ms = time_graph(torch, stream, us, lambda: [us.us_spmm_w4a4_ie(E, X, swi, sxi, N, Ya, Yh, wsi, 0, stream)
+                                                    for E in cpi], 10)
+            t = ms * 1e3 / ni
+            b = wbytes + N * 4096 // 2 + 2 * (4096 + N) + N * 4096 * 6       # weights, X, scales, Yacc + Y
+            row[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": b, "GB/s": round(b / (t * 1e-6) / 1e9, 1),
+                            "pct_hbm_measured": pct(b / (t * 1e-6) / 1e9, hbm_peak)}
+        # the generic CUDA-core kernel on the same matrix (split_k = 1), N = 1
+        X = torch.from_numpy(wl.pack_int4(d["Xq"][:1])).to(dev)
+        Ya = torch.empty(1, 4096, dtype=torch.int32, device=dev)
+        wsg = us.workspace_ie(Ei, 1, 1)
+        ms = time_graph(torch, stream, us, lambda: us.us_spmm_w4a4_ie(Ei, X, None, None, 1, Ya, None, wsg, 1, stream), 5)
+        row["generic_N1_us"] = round(ms * 1e3, 2)
         ie[name] = row
     ie["reorder_host_s"] = round(reorder_s, 2)
     out["w4a4_ie_areas_4096"] = ie

@@ -32,6 +32,7 @@ US_BITMAP_STATIC = 1
 EXPORTED = ("us_encode_sizes", "us_encode", "us_spmm_w4a4", "us_spmm_f16", "us_spmm_f16_noalloc", "us_spmspv_f16",
             "us_colinfo", "us_spmspv_f16_ci", "us_quantize_x",
             "us_encode_ie_sizes", "us_encode_ie", "us_reorder_rows", "us_spmm_w4a4_ie", "us_workspace_bytes_ie",
+            "us_pick_split_k_ie",
             "us_workspace_bytes", "us_pick_split_k", "us_validate", "us_get_last_device_status",
             "us_selftest_wait_timeout", "us_status_string", "us_version")
 
@@ -87,6 +88,7 @@ def load(path: str = LIB_PATH):
         lib.us_reorder_rows.argtypes = [P, i64, i32, i32, i32, i32, i32, i32, i32, P, i32]
         lib.us_spmm_w4a4_ie.argtypes = [pie, P, P, P, i32, P, P, P, sz, i32, P]
         lib.us_workspace_bytes_ie.argtypes = [pie, i32, i32, psz]
+        lib.us_pick_split_k_ie.argtypes = [pie, i32, ctypes.POINTER(ctypes.c_int)]
         lib.us_spmspv_f16_ci.argtypes = [pbm, P, P, i32, ctypes.c_float, P, P, sz, P]
         lib.us_quantize_x.argtypes = [P, i32, i32, P, P, P]
         lib.us_workspace_bytes.argtypes = [i32, pbm, i32, i32, psz]
@@ -247,6 +249,14 @@ def us_workspace_bytes_ie(E: EncodedIE, N: int, split_k: int = 0) -> int:
     d = E.desc()
     _check("us_workspace_bytes_ie", load().us_workspace_bytes_ie(ctypes.byref(d), N, split_k, ctypes.byref(n)))
     return n.value
+
+
+def us_pick_split_k_ie(E: EncodedIE, N: int = 1) -> int:
+    """0 when the balanced kernel serves us_spmm_w4a4_ie on E with N tokens."""
+    s = ctypes.c_int()
+    d = E.desc()
+    _check("us_pick_split_k_ie", load().us_pick_split_k_ie(ctypes.byref(d), N, ctypes.byref(s)))
+    return s.value
 
 
 def workspace_ie(E: EncodedIE, N: int, split_k: int = 0) -> torch.Tensor:

@@ -438,6 +438,14 @@ us_status check_bitmap_ie(const us_bitmap_ie* B, int elem) {
 Plan plan_ie(const us_bitmap_ie* B, int N, int split_k) {
     Plan pl{};
     const us_bitmap* W = &B->W;
+    // automatic split on 16 x 64 local tiles: the balanced kernel (no K slices)
+    if (split_k == 0 && W->elem == US_I4 &&
+        us::w4a4_sk_ie_supported(W->M, W->K, W->TM, W->TK, B->RA, B->CA, N)) {
+        pl.sk = true;
+        pl.tok_block = N;
+        pl.ws = us::w4a4_sk_ie_ws(W->M, W->K, N);
+        return pl;
+    }
     const int nTM = W->M / W->TM, nTK = W->K / W->TK;
     pl.tok_block = us::spmm_generic_tok_block(N);
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
@@ -488,6 +496,15 @@ us_status us_workspace_bytes_ie(const us_bitmap_ie* B, int N, int split_k, size_
     return US_OK;
 }
 
+us_status us_pick_split_k_ie(const us_bitmap_ie* B, int N, int* split_k) {
+    if (!split_k) return US_ERR_INVALID_ARG;
+    us_status s = check_bitmap_ie(B, US_I4);
+    if (s != US_OK) return s;
+    if (N < 1 || N > 2048) return US_ERR_INVALID_ARG;
+    *split_k = plan_ie(B, N, 0).split;
+    return US_OK;
+}
+
 us_status us_spmm_w4a4_ie(const us_bitmap_ie* B, const uint8_t* Xq, const uint16_t* s_w, const uint16_t* s_x, int N,
                           int32_t* Yacc, uint16_t* Y, void* ws, size_t ws_bytes, int split_k, void* stream) {
     us_status s = check_bitmap_ie(B, US_I4);
@@ -504,6 +521,11 @@ us_status us_spmm_w4a4_ie(const us_bitmap_ie* B, const uint8_t* Xq, const uint16
     p.X = Xq; p.s_w = s_w; p.s_x = s_x; p.Yacc = Yacc; p.Y = Y;
     p.split = pl.split; p.tok_block = pl.tok_block;
     p.ie_ra = B->RA; p.ie_ca = B->CA; p.perm = B->perm;
+    if (pl.sk) {
+        p.nTM = W->M / 64;                                    // 64-row bands of super-tiles
+        p.ws = ws;
+        return us::launch_w4a4_sk_ie(p, static_cast<cudaStream_t>(stream));
+    }
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
     p.counters = static_cast<unsigned*>(ws);
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);

@@ -38,6 +38,11 @@ bool w4a4_sk_supported(int TM, int TK, int M, int K, int N);
 size_t w4a4_sk_ws(int M, int K, int N);
 int w4a4_sk_variant(int N);   // 0: dp4a consumer, else the mma consumer's 8-token blocks
 us_status launch_w4a4_sk(UsKParams p, cudaStream_t st);
+// the same kernel on IE-BME 16 x 64 local tiles with areas (us_w4a4_sk_ie.cu);
+// p.nTM counts 64-row bands there
+bool w4a4_sk_ie_supported(int M, int K, int TM, int TK, int RA, int CA, int N);
+size_t w4a4_sk_ie_ws(int M, int K, int N);
+us_status launch_w4a4_sk_ie(UsKParams p, cudaStream_t st);
 
 // tensor-core fp16 SpMM for many tokens (us_tc.cu)
 bool tc_f16_supported(int TM, int TK, int M, int N);

@@ -247,6 +247,14 @@ us_status us_spmm_w4a4_ie(const us_bitmap_ie* W, const uint8_t* Xq, const uint16
                           int32_t* Yacc, uint16_t* Y, void* ws, size_t ws_bytes, int split_k, void* stream);
 us_status us_workspace_bytes_ie(const us_bitmap_ie* W, int N, int split_k, size_t* bytes);
 
+/* The split_k the automatic rule picks for us_spmm_w4a4_ie on W with N tokens:
+ * 0 when the balanced kernel serves the call (16 x 64 local tiles, RA in
+ * {1, 2, 4}, CA in {1, 2}, M a multiple of 64, 1..32 tokens: four local tiles
+ * along M make one 64 x 64 tile of the even partition that us_spmm_w4a4
+ * uses), else the K slices of the generic kernel.  W's pointers are not read
+ * beyond the null checks. */
+us_status us_pick_split_k_ie(const us_bitmap_ie* W, int N, int* split_k);
+
 /* ColInfo of a COL-order matrix ("Unified Static-Dynamic Pruning for
  * Efficient LLM Inference", section 4.1, Tiled-CBC storage structure): one
  * uint32 per column of every tile, tile-major (colinfo[t * TK + j] for tile t,
