@@ -814,6 +814,45 @@ def measure_extras(us, torch, wl, dev, stream, hbm_peak, bf16_peak, cpu=True):
         ie[name] = row
     ie["reorder_host_s"] = round(reorder_s, 2)
     out["w4a4_ie_areas_4096"] = ie
+    # rows that share sparsity patterns (groups of four with common column
+    # scales before pruning, shuffled within each 16-row block) at 70 %:
+    # plain 64 x 64 tiles against IE-BME 4 x 1 areas with the row reordering
+    dc = wl.w4a4(4096, 4096, 16, 0.7, seed=0, rows="clustered")
+    Wc = torch.from_numpy(dc["Wq"]).to(dev)
+    swc = torch.from_numpy(dc["s_w"].view(np.int16)).to(dev)
+    cl = {}
+    Ep = us.us_encode(Wc, 64, 64, us.US_I4, us.US_ORDER_ROW)
+    Ep.flags = us.US_BITMAP_STATIC
+    permc = torch.from_numpy(us.us_reorder_rows(dc["Wq"], 16, 64, 4, 1, us.US_I4)).to(dev)
+    Ec = us.us_encode_ie(Wc, 16, 64, 4, 1, us.US_I4, permc)
+    Ec.E.flags = us.US_BITMAP_STATIC
+    for name, E0, wb in (("plain_64x64", Ep, Ep.nbytes()), ("areas_4x1_16x64_reordered", Ec, Ec.E.nbytes() + permc.numel())):
+        n0 = max(2, math.ceil(2.2 * l2 / wb))
+        if name == "plain_64x64":
+            cps0 = [E0] + [us.Encoded(E0.M, E0.K, 64, 64, E0.elem, E0.order, E0.bitmap.clone(), E0.tile_off.clone(),
+                                      E0.values.clone(), E0.values_bytes, us.US_BITMAP_STATIC) for _ in range(n0 - 1)]
+        else:
+            cps0 = [E0] + [us.EncodedIE(us.Encoded(E0.E.M, E0.E.K, 16, 64, E0.E.elem, E0.E.order, E0.E.bitmap.clone(),
+                                                   E0.E.tile_off.clone(), E0.E.values.clone(), E0.E.values_bytes,
+                                                   us.US_BITMAP_STATIC), 4, 1, permc.clone()) for _ in range(n0 - 1)]
+        row = {"weight_bytes": wb, "copies": n0}
+        for N in (1, 16):
+            X = torch.from_numpy(wl.pack_int4(dc["Xq"][:N])).to(dev)
+            sxc = torch.from_numpy(dc["s_x"][:N].view(np.int16)).to(dev)
+            Ya = torch.empty(N, 4096, dtype=torch.int32, device=dev)
+            Yh = torch.empty(N, 4096, dtype=torch.int16, device=dev)
+            if name == "plain_64x64":
+                wsc = us.workspace(us.US_OP_SPMM_W4A4, E0, N)
+                fn = lambda: [us.us_spmm_w4a4(E, X, swc, sxc, N, Ya, Yh, wsc, 0, stream) for E in cps0]
+            else:
+                wsc = us.workspace_ie(E0, N)
+                fn = lambda: [us.us_spmm_w4a4_ie(E, X, swc, sxc, N, Ya, Yh, wsc, 0, stream) for E in cps0]
+            ms = time_graph(torch, stream, us, fn, 10)
+            t = ms * 1e3 / n0
+            b = wb + N * 4096 // 2 + 2 * (4096 + N) + N * 4096 * 6
+            row[f"N{N}"] = {"us_per_launch": round(t, 3), "bytes_per_call": b, "GB/s": round(b / (t * 1e-6) / 1e9, 1)}
+        cl[name] = row
+    out["w4a4_clustered_rows_4096_s70"] = cl
     # per-token activation quantisation, fp16 -> int4 + scale (reads 2NK, writes NK/2 + 2N bytes)
     qz = {}
     for N in (16, 2048):

@@ -87,15 +87,44 @@ def f16_weights(M: int, K: int, sparsity: float, seed: int, mode: str = "uniform
     return np.where(mask, W, np.float32(0)).astype(np.float16)
 
 
+def clustered_importance(seed: int, M: int, K: int, group: int = 4, sigma: float = 3.0) -> np.ndarray:
+    """Per-row column scales shared by groups of `group` consecutive rows:
+    exp(sigma * N(0, 1)) per (group, column).  A magnitude mask taken on
+    W * scales keeps mostly the same positions within a group: rows that share
+    sparsity patterns, the structure the bitmap-aware row reordering of
+    UnionSparse (section V-B) groups into one union mask."""
+    rng = np.random.default_rng(seed)
+    g = np.exp(rng.standard_normal(((M + group - 1) // group, K)) * sigma).astype(np.float32)
+    return np.repeat(g, group, axis=0)[:M]
+
+
+def scatter_within_tiles(seed: int, M: int, TM: int) -> np.ndarray:
+    """A row order that shuffles the rows inside every TM-row block (seeded),
+    so that only a reordering finds the groups again."""
+    rng = np.random.default_rng(seed)
+    order = np.arange(M)
+    for b in range(0, M - M % TM, TM):
+        order[b:b + TM] = b + rng.permutation(TM)
+    return order
+
+
 def w4a4(M: int, K: int, N: int, sparsity: float, seed: int, rows: str = "fixed"):
     """W4A4 workload: magnitude-pruned, per-row int4 W; per-token int4 X.
+    rows: "fixed" (every row keeps 1 - sparsity), "beta" (per-row keep rates
+    from Beta(2, 2)), "clustered" (groups of four rows share column scales
+    before pruning, then the rows are shuffled within each 16-row block).
 
     Returns dict with Wq (int8 M x K), s_w (fp16 M), Xq (int8 N x K),
     Xq_packed (uint8 N*K/2), s_x (fp16 N).
     """
     W = _normal(seed, (M, K), 0.02)
     keep = beta_row_keep(seed + 2, M) if rows == "beta" else np.full(M, 1.0 - sparsity)
-    W = np.where(magnitude_mask(W, keep), W, np.float32(0))
+    # clustered: the mask comes from the magnitudes under the shared column
+    # scales; the kept values stay N(0, 0.02)
+    score = W * clustered_importance(seed + 3, M, K) if rows == "clustered" else W
+    W = np.where(magnitude_mask(score, keep), W, np.float32(0))
+    if rows == "clustered":
+        W = W[scatter_within_tiles(seed + 4, M, 16)]
     Wq, s_w = quantize_int4_rows(W)
     X = _normal(seed + 1, (N, K), 1.0)
     Xq, s_x = quantize_int4_rows(X)

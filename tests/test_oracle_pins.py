@@ -352,6 +352,23 @@ def test_workload_statistics():
     assert abs((x == 0).mean() - 0.9) < 1e-3
 
 
+def test_clustered_workload_shares_patterns(orc):
+    """Rows in groups of four share column scales before magnitude pruning,
+    then are shuffled within each 16-row block: the density stays near the
+    target, the recipe is seeded, and the row reordering finds groups whose
+    4 x 1 area union is much sparser than that of the plain random workload."""
+    c = wl.w4a4(64, 256, 1, 0.7, seed=0, rows="clustered")
+    assert np.array_equal(c["Wq"], wl.w4a4(64, 256, 1, 0.7, seed=0, rows="clustered")["Wq"])
+    assert 0.25 < (c["Wq"] != 0).mean() < 0.31
+    r = wl.w4a4(64, 256, 1, 0.7, seed=0)
+    cost = {}
+    for name, W in (("clustered", c["Wq"]), ("random", r["Wq"])):
+        cost[name] = sum(orc.reorder_rows(W[b:b + 16, k:k + 64] != 0, 4, 1)[1]
+                         for b in range(0, 64, 16) for k in range(0, 256, 64))
+    # union cost in set positions over 16 tiles of 4 x 64 logical positions
+    assert cost["clustered"] < 0.8 * cost["random"], cost
+
+
 # ------------------------------------------------- activation quantisation --
 # UnionSparse Fig. 2 "Quant" (FP16 X -> INT4 X, per-token scale): s = fp16(amax / 7),
 # codes = clamp(rint(x / s), -8, 7) with ties to even, s = 1 for an all-zero token.
