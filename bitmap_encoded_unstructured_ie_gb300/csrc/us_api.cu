@@ -124,6 +124,7 @@ Plan plan_spmm(us_op op, const us_bitmap* W, int N, int split_k) {
         pl.tok_block = us::tc_tok_block(N);
         pl.split = split_k > 0 ? split_k : us::tc_split(W->M, N, W->K / W->TK);
         if (pl.split > W->K / W->TK) pl.split = W->K / W->TK;
+        if (pl.split > us::tc_max_split()) pl.split = us::tc_max_split();
         pl.ws = us::tc_ws(W->M, N, pl.split);
         return pl;
     }
@@ -326,10 +327,7 @@ us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
     p.split = pl.split; p.tok_block = pl.tok_block;
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
     p.counters = static_cast<unsigned*>(ws);
-    if (pl.tc) {
-        p.ws = static_cast<uint8_t*>(ws) + (((size_t)(W->M / 128) * ntb * 4 + 255) & ~(size_t)255);
-        return us::launch_tc_f16(p, static_cast<cudaStream_t>(stream));
-    }
+    if (pl.tc) return us::launch_tc_f16(p, static_cast<cudaStream_t>(stream));
     p.ws = static_cast<uint8_t*>(ws) + counters_bytes(p.nTM, ntb);
     if (pl.dec) return us::launch_f16_dec(p, static_cast<cudaStream_t>(stream));
     return us::launch_spmm_generic(p, US_F16, static_cast<cudaStream_t>(stream));
@@ -380,13 +378,14 @@ us_status us_spmm_f16_noalloc(const us_bitmap* W, const uint16_t* X, int N, uint
     p.X = X; p.Y = Y;
     p.split = pl.split; p.tok_block = pl.tok_block;
     const int ntb = (N + pl.tok_block - 1) / pl.tok_block;
-    const size_t cbytes = pl.tc ? (((size_t)(W->M / 128) * ntb * 4 + 255) & ~(size_t)255) : counters_bytes(p.nTM, ntb);
+    // the tensor-core path reduces its K slices inside a cluster: no scratch
+    if (pl.tc) return us::launch_tc_f16(p, st);
+    const size_t cbytes = counters_bytes(p.nTM, ntb);
     // the split-K arrival counters must start at zero; the partials are fully
     // written before they are read, so only the counters are cleared
     if (cudaMemsetAsync(scratch, 0, cbytes, st) != cudaSuccess) return US_ERR_CUDA;
     p.counters = reinterpret_cast<unsigned*>(scratch);
     p.ws = scratch + cbytes;
-    if (pl.tc) return us::launch_tc_f16(p, st);
     return pl.dec ? us::launch_f16_dec(p, st) : us::launch_spmm_generic(p, US_F16, st);
 }
 

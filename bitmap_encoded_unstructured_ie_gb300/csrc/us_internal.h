@@ -48,6 +48,7 @@ us_status launch_w4a4_sk_ie(UsKParams p, cudaStream_t st);
 bool tc_f16_supported(int TM, int TK, int M, int N);
 int tc_tok_block(int N);
 int tc_split(int M, int N, int nTK);
+int tc_max_split();                  // K slices of one output tile form one cluster
 size_t tc_ws(int M, int N, int split);
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st);
 // the driver's cuTensorMapEncodeTiled (nullptr if the driver lacks it)

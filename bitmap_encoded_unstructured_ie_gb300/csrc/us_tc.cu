@@ -33,8 +33,12 @@
 //    K step to that step's "done" barrier, which frees its A and B stages;
 //  * warps 3 .. 3+4NH-1 (epilogue): tcgen05.ld the accumulators (one TMEM lane
 //    per output row, one warp per lane quarter and token half) and write fp16
-//    outputs, or, under split-K, fp32 partials that the last CTA of the tile
-//    sums in fixed slice order.
+//    outputs.  Under split-K the K slices of an output tile form one
+//    thread-block cluster: each CTA parks its fp32 partial of one token half in
+//    its own shared memory (the operand stages are free by then), and after a
+//    cluster barrier every CTA sums its share of the rows over the cluster's
+//    partials (distributed shared memory) in fixed slice order and writes
+//    fp16; a second barrier keeps the partials alive until all have read them.
 #include <cudaTypedefs.h>
 
 #include "us_common.cuh"
@@ -105,46 +109,30 @@ struct TcParams {
     int n_tiles;          // ceil(N / (256 NH))
 };
 
-// Sums the split-K partials of one output tile in slice order and writes fp16.
-// An item is four consecutive rows of one token (float4); with SP slices per
-// pass a thread keeps 8 / SP items, eight 16-byte loads, in flight at once.
-// part points at the tile's first row and token in slice 0, token-major with
-// row stride M; slice_stride separates the slices.
-template <int SP>
-US_DEV void tc_reduce(const UsKParams& p, float* part, int64_t slice_stride, int mt, int n0, int nitems) {
-    constexpr int PER = 8 / SP;
-    for (int i0 = threadIdx.x; i0 < nitems; i0 += kThreads * PER) {
-        float4 acc[PER];
-#pragma unroll
-        for (int j = 0; j < PER; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int s0 = 0; s0 < p.split; s0 += SP) {
-            float4 w[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = u / SP, sl = s0 + u % SP, idx = i0 + j * kThreads;
-                if (sl < p.split && idx < nitems)
-                    w[u] = __ldcg(reinterpret_cast<const float4*>(
-                        part + sl * slice_stride + (int64_t)(idx >> 5) * p.M + (idx & 31) * 4));
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int j = u / SP, sl = s0 + u % SP, idx = i0 + j * kThreads;
-                if (sl < p.split && idx < nitems) {
-                    acc[j].x += w[u].x; acc[j].y += w[u].y; acc[j].z += w[u].z; acc[j].w += w[u].w;
-                    __stcg(reinterpret_cast<float4*>(part + sl * slice_stride + (int64_t)(idx >> 5) * p.M + (idx & 31) * 4),
-                           make_float4(0.f, 0.f, 0.f, 0.f));
-                }
-            }
+// The largest K split of the tensor-core path: the slices of an output tile
+// form one thread-block cluster (portable cluster size).
+constexpr int kMaxSplit = 8;
+
+// Split-K reduction of one token half (ntok tokens from n0) inside the
+// cluster: every CTA's fp32 partial sits token-major in its own shared memory
+// at `part` (part[n * kBM + row]).  This CTA sums the row groups of four
+// [rank * 32 / split, (rank + 1) * 32 / split) over the slices in slice order
+// (0 + s0 + s1 + ..., as a plain sequential sum) and writes them as fp16.
+US_DEV void tc_cluster_reduce(const UsKParams& p, const float* part, int mt, int n0, int ntok) {
+    const uint32_t rank = us::cluster_ctarank();
+    const int g0 = (int)(rank * 32u / (uint32_t)p.split), g1 = (int)((rank + 1u) * 32u / (uint32_t)p.split);
+    const int ng = g1 - g0;
+    for (int it = threadIdx.x; it < ntok * ng; it += kThreads) {
+        const int n = it / ng, g = g0 + (it - n * ng);
+        const uint32_t off = (uint32_t)(n * kBM + 4 * g) * 4u;
+        float4 acc = us::ld_cluster_v4f32(us::cluster_map(part, 0) + off);
+        for (int sl = 1; sl < p.split; ++sl) {
+            const float4 w = us::ld_cluster_v4f32(us::cluster_map(part, (uint32_t)sl) + off);
+            acc.x += w.x; acc.y += w.y; acc.z += w.z; acc.w += w.w;
         }
-#pragma unroll
-        for (int j = 0; j < PER; ++j) {
-            const int idx = i0 + j * kThreads;
-            if (idx >= nitems) break;
-            const int n = n0 + (idx >> 5), m = mt * kBM + (idx & 31) * 4;
-            const uint32_t lo = (uint32_t)us::float_to_half_bits(acc[j].x) | ((uint32_t)us::float_to_half_bits(acc[j].y) << 16);
-            const uint32_t hi = (uint32_t)us::float_to_half_bits(acc[j].z) | ((uint32_t)us::float_to_half_bits(acc[j].w) << 16);
-            *reinterpret_cast<uint2*>(p.Y + (int64_t)n * p.M + m) = make_uint2(lo, hi);
-        }
+        const uint32_t lo = (uint32_t)us::float_to_half_bits(acc.x) | ((uint32_t)us::float_to_half_bits(acc.y) << 16);
+        const uint32_t hi = (uint32_t)us::float_to_half_bits(acc.z) | ((uint32_t)us::float_to_half_bits(acc.w) << 16);
+        *reinterpret_cast<uint2*>(p.Y + (int64_t)(n0 + n) * p.M + mt * kBM + 4 * g) = make_uint2(lo, hi);
     }
 }
 
@@ -166,8 +154,8 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x;                              // 128-row block
-    const int nt = blockIdx.y % tp.n_tiles;                 // token tile
-    const int slice = blockIdx.y / tp.n_tiles;              // K slice
+    const int slice = blockIdx.y % p.split;                 // K slice (cluster rank under split-K)
+    const int nt = blockIdx.y / p.split;                    // token tile
     const int kt0 = (int)((int64_t)slice * p.nTK / p.split);
     const int kt1 = (int)((int64_t)(slice + 1) * p.nTK / p.split);
     const int nk = kt1 - kt0;
@@ -483,29 +471,22 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
         for (int q = ix > kBStages ? ix - kBStages : 0; q < ix; ++q)
             us::mbar_wait(&S.b_full[q % kBStages], (q / kBStages) & 1, nullptr);
     }
+    bool ready = false;
     if (warp >= 3 && warp < 3 + 4 * halves) {
         // the final commit also covers MMAs issued before a failure: wait for it (bounded)
-        const bool ready = us::mbar_wait(&S.done, 0, any_failed ? nullptr : p.status) && !any_failed;
+        ready = us::mbar_wait(&S.done, 0, any_failed ? nullptr : p.status) && !any_failed;
         us::tc_fence_after();
-        const int quarter = warp & 3;                       // TMEM lanes 32*quarter .. +31
-        const int half = (warp - 3) >> 2;                   // token half: TMEM columns 256 half ..
-        const int m = mt * kBM + quarter * 32 + lane;
-        const int nbase = nt * kBN;
-        float* part = reinterpret_cast<float*>(p.ws);
-        const int nTB = tp.n_tiles;
-        for (int c0 = half * kBH; c0 < (half + 1) * kBH && nbase + c0 < p.N; c0 += 32) {
-            float v[32];
-            us::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
-            if (!ready) continue;
-            if (p.split > 1) {
-                // partials token-major, [slice][token tile][n][m]: a warp's 32 lanes
-                // (rows) store 128 contiguous bytes per column; columns past N are
-                // never written, so they stay zero
-                const int64_t base = (((int64_t)slice * nTB + nt) * kBN + c0) * p.M + m;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (nbase + c0 + i < p.N) __stcg(part + base + (int64_t)i * p.M, v[i]);
-            } else {
+    }
+    const int quarter = warp & 3;                           // TMEM lanes 32*quarter .. +31
+    const int m = mt * kBM + quarter * 32 + lane;
+    const int nbase = nt * kBN;
+    if (p.split == 1) {
+        if (warp >= 3 && warp < 3 + 4 * halves) {
+            const int half = (warp - 3) >> 2;               // token half: TMEM columns 256 half ..
+            for (int c0 = half * kBH; c0 < (half + 1) * kBH && nbase + c0 < p.N; c0 += 32) {
+                float v[32];
+                us::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+                if (!ready) continue;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int n = nbase + c0 + i;
@@ -513,32 +494,31 @@ spmm_f16_tc_kernel(const TcParams tp, const __grid_constant__ CUtensorMap xmap) 
                 }
             }
         }
+    } else {
+        // split-K inside the cluster, one token half at a time: every thread of
+        // every CTA reaches both barriers of every round (the rounds depend on
+        // nt only, the same for the whole cluster); a failed CTA writes nothing
+        // and its outputs are not valid (the status word says why)
+        __syncthreads();                                    // the copies of a failed CTA have landed
+        float* part = reinterpret_cast<float*>(smem);       // 128 rows x 256 tokens fp32, token-major
+        for (int hh = 0; hh < halves; ++hh) {
+            if (warp >= 3 + 4 * hh && warp < 7 + 4 * hh) {
+                for (int c0 = 0; c0 < kBH; c0 += 32) {
+                    float v[32];
+                    us::tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(hh * kBH + c0), v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) part[(c0 + i) * kBM + quarter * 32 + lane] = ready ? v[i] : 0.f;
+                }
+            }
+            us::cluster_sync();
+            const int n0 = nbase + hh * kBH;
+            if (!any_failed) tc_cluster_reduce(p, part, mt, n0, min(kBH, p.N - n0));
+            us::cluster_sync();                             // the partials stay until every CTA has read them
+        }
     }
     us::tc_fence_before();
     __syncthreads();
     if (warp == 1) us::tmem_dealloc(tmem, kBN);
-    if (p.split > 1 && !any_failed) {
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0)
-            S.flag = (atomicAdd(&p.counters[mt * tp.n_tiles + nt], 1u) == (unsigned)p.split - 1u) ? 1u : 0u;
-        __syncthreads();
-        if (!S.flag) return;
-        __threadfence();
-        // the last CTA of this output tile sums the slices in fixed order and
-        // clears the partials behind (a workspace may be shared with kernels that
-        // need it all zero); the slices wrote the columns of real tokens only
-        const int ntok = min(kBN, p.N - nt * kBN);
-        float* part = reinterpret_cast<float*>(p.ws) + ((int64_t)nt * kBN) * p.M + mt * kBM;
-        const int64_t slice_stride = (int64_t)tp.n_tiles * kBN * p.M;
-        if (p.split == 2)
-            tc_reduce<2>(p, part, slice_stride, mt, nt * kBN, ntok * (kBM / 4));
-        else if (p.split <= 4)
-            tc_reduce<4>(p, part, slice_stride, mt, nt * kBN, ntok * (kBM / 4));
-        else
-            tc_reduce<8>(p, part, slice_stride, mt, nt * kBN, ntok * (kBM / 4));
-        if (threadIdx.x == 0) p.counters[mt * tp.n_tiles + nt] = 0u;
-    }
 }
 
 }  // namespace
@@ -571,16 +551,14 @@ int tc_split(int M, int N, int nTK) {
     const int bn = tc_tok_block(N);
     const int ctas = (M / kBM) * ((N + bn - 1) / bn);
     int s = 1;
-    while (ctas * s * 2 <= num_sms() && nTK / (s * 2) >= 8 && s < 8) s *= 2;
+    while (ctas * s * 2 <= num_sms() && nTK / (s * 2) >= 8 && s < kMaxSplit) s *= 2;
     return s;
 }
 
-size_t tc_ws(int M, int N, int split) {
-    const int bn = tc_tok_block(N);
-    const int n_tiles = (N + bn - 1) / bn;
-    const size_t counters = ((size_t)(M / kBM) * n_tiles * 4 + 255) & ~(size_t)255;
-    return split <= 1 ? counters : counters + (size_t)split * n_tiles * M * bn * 4;
-}
+int tc_max_split() { return kMaxSplit; }
+
+// The split-K partials stay in the cluster's shared memory: no workspace.
+size_t tc_ws(int, int, int) { return 0; }
 
 us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     auto enc = tensor_map_encoder();
@@ -607,10 +585,19 @@ us_status launch_tc_f16(const UsKParams& p, cudaStream_t st) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
+    if (p.split < 1 || p.split > kMaxSplit) return US_ERR_INVALID_ARG;
     cfg.gridDim = dim3((unsigned)(p.M / kBM), (unsigned)(tp.n_tiles * p.split));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
+    // the K slices of an output tile (consecutive blockIdx.y) form one cluster
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)p.split;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.split > 1 ? 1 : 0;
     if (cudaLaunchKernelEx(&cfg, kern, tp, map) != cudaSuccess) return US_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? US_OK : US_ERR_CUDA;
 }

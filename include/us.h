@@ -150,11 +150,13 @@ us_status us_spmm_w4a4(const us_bitmap* W, const uint8_t* Xq, const uint16_t* s_
  * spMspV layout serves this product too).  X: N x K fp16 token-major,
  * Y: N x M fp16, 1 <= N <= 2048.  split_k as above.  With 64 x 64 tiles,
  * N >= 64 and M % 128 == 0 the product runs on the tensor cores (tcgen05);
- * 1-63 tokens on ROW tiles run on the mma.sync decode kernel; every other
- * case on the generic CUDA-core kernel.  The fp32 partial sums are reduced in
- * fixed slice order, so repeated calls with the same arguments give bitwise
- * identical results; calls that take different kernels may differ in the
- * last bits. */
+ * there K is cut into at most 8 slices (a larger split_k is lowered to 8):
+ * the slices of an output tile form one thread-block cluster and reduce in
+ * its shared memory, so that path uses no workspace.  1-63 tokens on ROW
+ * tiles run on the mma.sync decode kernel; every other case on the generic
+ * CUDA-core kernel.  The fp32 partial sums are reduced in fixed slice order,
+ * so repeated calls with the same arguments give bitwise identical results;
+ * calls that take different kernels may differ in the last bits. */
 us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
                       void* ws, size_t ws_bytes, int split_k, void* stream);
 
@@ -170,8 +172,9 @@ us_status us_spmm_f16(const us_bitmap* W, const uint16_t* X, int N, uint16_t* Y,
  * fit; an explicit split_k whose scratch exceeds the array returns
  * US_ERR_TOO_LARGE before anything is enqueued.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress), so make that
- * first call before any stream capture.  Each call clears the split-K
- * counters with cudaMemsetAsync on `stream` (no allocation).  All calls share
+ * first call before any stream capture.  Each call off the tensor-core path
+ * clears the split-K counters with cudaMemsetAsync on `stream` (no
+ * allocation); the tensor-core path needs no scratch.  All calls share
  * the one array: calls that may run at the same time on the GPU (different
  * streams, overlapping graph branches) race and must not be issued. */
 #define US_NOALLOC_SCRATCH_BYTES (8u << 20)

@@ -63,19 +63,23 @@ def test_noalloc_matches_workspace_entry_point_twice(us, orc, N, split):
 
 
 def test_noalloc_rejects_scratch_beyond_its_limit(us, orc):
+    """256-row tiles run on the generic kernel, whose split-K partials live in
+    the scratch array: an explicit split whose partials exceed it is refused,
+    and an automatic split that would exceed it falls back to one slice.  (The
+    tensor-core path reduces its slices in a cluster and needs no scratch.)"""
     rng = np.random.default_rng(3)
     M = K = 4096
     W = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
     W[rng.random((M, K)) < 0.5] = 0
-    E = us.us_encode(torch.from_numpy(W.view(np.int16)).cuda(), 64, 64, us.US_F16, us.US_ORDER_ROW)
-    N = 256
+    E = us.us_encode(torch.from_numpy(W.view(np.int16)).cuda(), 256, 64, us.US_F16, us.US_ORDER_ROW)
+    N = 40
     X = rng.standard_normal((N, K)).astype(np.float16)
     Xt = torch.from_numpy(X.view(np.int16)).cuda()
     Y = torch.empty(N, M, dtype=torch.int16, device="cuda")
     # an explicit split whose partials exceed the 8 MiB array is refused on the host
-    assert us.us_workspace_bytes(us.US_OP_SPMM_F16, E, N, 8) > SCRATCH
+    assert us.us_workspace_bytes(us.US_OP_SPMM_F16, E, N, 16) > SCRATCH
     with pytest.raises(us.UsError) as ei:
-        us.us_spmm_f16_noalloc(E, Xt, N, Y, 8)
+        us.us_spmm_f16_noalloc(E, Xt, N, Y, 16)
     assert ei.value.code == us.US_ERR_TOO_LARGE
     # the automatic choice would not fit either, so it falls back to one slice:
     # the same result, bit for bit, as an explicit split of 1 with a workspace
@@ -92,3 +96,23 @@ def test_noalloc_rejects_scratch_beyond_its_limit(us, orc):
     m_idx = s.integers(0, M, 4000).astype(np.int32)
     y = Y.cpu().numpy().view(np.float16)[n_idx, m_idx]
     _check_oracle(orc, W, X, y, n_idx, m_idx, "fallback, sampled outputs")
+
+
+def test_noalloc_tensor_core_path_needs_no_scratch(us, orc):
+    """The tensor-core path with the largest split (8 slices in one cluster)
+    through the no-allocation entry point: bitwise equal to us_spmm_f16."""
+    rng = np.random.default_rng(4)
+    M = K = 4096
+    W = (rng.standard_normal((M, K)) * 0.02).astype(np.float16)
+    W[rng.random((M, K)) < 0.6] = 0
+    E = us.us_encode(torch.from_numpy(W.view(np.int16)).cuda(), 64, 64, us.US_F16, us.US_ORDER_ROW)
+    N = 256
+    Xt = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float16).view(np.int16)).cuda()
+    assert us.us_workspace_bytes(us.US_OP_SPMM_F16, E, N, 8) <= 16
+    Y = torch.empty(N, M, dtype=torch.int16, device="cuda")
+    Y1 = torch.empty_like(Y)
+    us.us_spmm_f16_noalloc(E, Xt, N, Y, 8)
+    us.us_spmm_f16(E, Xt, N, Y1, us.workspace(us.US_OP_SPMM_F16, E, N, 8), 8)
+    torch.cuda.synchronize()
+    assert us.us_get_last_device_status() == us.US_OK
+    assert torch.equal(Y, Y1)
