@@ -156,3 +156,27 @@ def test_balanced_ie_full_size(us, orc):
         n_idx, m_idx = rng.integers(0, N, 3000), rng.integers(0, 4096, 3000)
         oacc, _ = orc.spmm_w4a4_at(W, d["Xq"][:N], one, np.ones(N, np.float16), n_idx, m_idx)
         assert np.array_equal(outs[0][0][n_idx, m_idx], oacc)
+
+
+def test_balanced_ie_ffn_shape_ring_recycles(us, orc):
+    """11008 x 4096 as 16 x 64 local tiles with 2 x 1 areas: 73 super-tiles a
+    CTA, more chunks than the byte ring holds at once (the producer waits for
+    the consumers to free it, before and after the dependency wait), with
+    random row permutations; N = 1 (dp4a) and 32 (four mma token blocks),
+    sampled outputs exact."""
+    M, K = 11008, 4096
+    rng, W, Xq, s_w, s_x = problem(21, M, K, 32)
+    nT = (M // 16) * (K // 64)
+    pm = np.concatenate([rng.permutation(16) for _ in range(nT)]).astype(np.uint8)
+    E = us.us_encode_ie(torch.from_numpy(W).cuda(), 16, 64, 2, 1, I4, torch.from_numpy(pm).cuda())
+    torch.cuda.synchronize()
+    assert us.us_get_last_device_status() == us.US_OK
+    for N in (1, 32):
+        assert us.us_pick_split_k_ie(E, N) == 0
+        for static in (False, True):
+            acc, y = call(us, E, Xq[:N], s_w, s_x[:N], N, static, reps=1)[0]
+            assert us.us_get_last_device_status() == us.US_OK
+            n_idx, m_idx = rng.integers(0, N, 3000), rng.integers(0, M, 3000)
+            oacc, oy = orc.spmm_w4a4_at(W, Xq[:N], s_w, s_x[:N], n_idx, m_idx)
+            assert np.array_equal(acc[n_idx, m_idx], oacc), f"N {N} static {static}"
+            assert np.array_equal(y[n_idx, m_idx], oy.view(np.uint16)), f"N {N} static {static}"
