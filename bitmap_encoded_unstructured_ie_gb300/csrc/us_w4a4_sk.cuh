@@ -833,7 +833,9 @@ w4a4_sk_kernel(const UsKParams p) {
         }
         // owned, continued by CTAs cta+1 .. c_hi, whose first band it is.  A
         // thread's loads of up to kE elements x 4 CTAs are all in flight before
-        // the first is used: usually one L2 round trip for the whole band
+        // the first is used, and every poll round re-loads all the words still
+        // untagged together: once the last post lands, the band is seen within
+        // about one L2 round trip, however many of the thread's words it held
         const int c_hi = S.c_hi;                              // b is the last band
         constexpr int kAll = NTOK * kTM;
         constexpr int kE = (kAll + kThreads - 1) / kThreads < 4 ? (kAll + kThreads - 1) / kThreads : 4;
@@ -843,6 +845,7 @@ w4a4_sk_kernel(const UsKParams p) {
             for (int e = 0; e < kE; ++e) v[e] = i0 + e * kThreads < kAll ? a[i0 + e * kThreads] : 0;
             for (int c0 = cta + 1; c0 <= c_hi; c0 += 4) {
                 uint64_t w[kE][4];
+                uint32_t missing = 0;                         // bit 4 e + u: word not posted yet
 #pragma unroll
                 for (int e = 0; e < kE; ++e)
 #pragma unroll
@@ -855,23 +858,42 @@ w4a4_sk_kernel(const UsKParams p) {
 #pragma unroll
                 for (int e = 0; e < kE; ++e)
 #pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if ((w[e][u] >> 32) != 1ull) missing |= 1u << (4 * e + u);
+                if (missing) {
+                    // wait for the rest, bounded; each round polls them all at once
+                    const uint64_t tw = us::globaltimer_ns();
+                    while (missing) {
+#pragma unroll
+                        for (int e = 0; e < kE; ++e)
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if (missing & (1u << (4 * e + u)))
+                                    w[e][u] = us::ld_relaxed_gpu_u64(post + (int64_t)(c0 + u) * kAll + i0 + e * kThreads);
+#pragma unroll
+                        for (int e = 0; e < kE; ++e)
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                if ((w[e][u] >> 32) == 1ull) missing &= ~(1u << (4 * e + u));
+                        if (missing && us::globaltimer_ns() - tw > us::kWaitLimitNs) {
+                            us::set_status(p.status, US_ERR_TIMEOUT);
+#pragma unroll
+                            for (int e = 0; e < kE; ++e)
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    if (missing & (1u << (4 * e + u))) w[e][u] = 0;
+                            break;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < kE; ++e)
+#pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = i0 + e * kThreads;
                         if (c0 + u > c_hi || i >= kAll) continue;
-                        uint64_t* src = post + (int64_t)(c0 + u) * kAll + i;
-                        if ((w[e][u] >> 32) != 1ull) {
-                            // not posted yet: wait for it, bounded
-                            const uint64_t tw = us::globaltimer_ns();
-                            while (((w[e][u] = us::ld_relaxed_gpu_u64(src)) >> 32) != 1ull) {
-                                if (us::globaltimer_ns() - tw > us::kWaitLimitNs) {
-                                    us::set_status(p.status, US_ERR_TIMEOUT);
-                                    w[e][u] = 0;
-                                    break;
-                                }
-                            }
-                        }
                         v[e] += (int)(uint32_t)w[e][u];
-                        us::st_relaxed_gpu_u64(src, 0ull);           // ready for the next call
+                        us::st_relaxed_gpu_u64(post + (int64_t)(c0 + u) * kAll + i, 0ull);   // ready for the next call
                     }
             }
 #pragma unroll
