@@ -511,6 +511,28 @@ def test_w4a4_ffn_full(us, orc, M, K, static):
         assert np.array_equal(y[n_idx, m_idx].view(np.uint16), oy.view(np.uint16))
 
 
+@pytest.mark.parametrize("static", [False, True])
+def test_w4a4_balanced_wide_activation_block(us, orc, static):
+    """153 x 257 tiles of 64 x 64: 259 tiles per CTA, so a CTA spans whole band
+    widths and stages all 257 K tiles of every token (16 KB a token row at
+    N = 16, one CTA per SM).  N = 2 (dp4a) and 16 (mma.sync); sampled outputs
+    exact."""
+    M, K = 64 * 153, 64 * 257
+    rng = np.random.default_rng(257)
+    W = rand_i4(rng, M, K, 0.3)
+    Xq = rng.integers(-8, 8, size=(16, K)).astype(np.int8)
+    s_w = (rng.random(M) * 0.01 + 1e-3).astype(np.float16)
+    s_x = (rng.random(16) * 0.5 + 0.05).astype(np.float16)
+    E = encode_gpu(us, W, 64, 64, I4, ROW)
+    for N in (2, 16):
+        assert us.us_pick_split_k(us.US_OP_SPMM_W4A4, E, N) == 0
+        acc, y = run_w4a4(us, E, wl.pack_int4(Xq[:N]), s_w, s_x[:N], N, static=static)
+        n_idx, m_idx = rng.integers(0, N, 3000), rng.integers(0, M, 3000)
+        oacc, oy = orc.spmm_w4a4_at(W, Xq[:N], s_w, s_x[:N], n_idx, m_idx)
+        assert np.array_equal(acc[n_idx, m_idx], oacc), N
+        assert np.array_equal(y[n_idx, m_idx].view(np.uint16), oy.view(np.uint16)), N
+
+
 @pytest.mark.parametrize("N", [256, 2048])
 def test_f16_prefill_sampled(us, orc, N):
     d = wl.f16_spmm(4096, 4096, N, 0.6, seed=0)
