@@ -10,7 +10,8 @@
 // Per CTA: one 64-row band x one K slice x one block of 8, 16 or 32 tokens;
 // eight warps in two groups of four.  A group takes every other tile of the
 // slice and its four warps decode the same tile together, one 16-row strip
-// each.  Each group runs a three-stage ring: one lane issues, per tile, a bulk
+// each.  Each group runs a three-stage ring (two stages when three CTAs share
+// an SM, for grids of more than one wave at two): one lane issues, per tile, a bulk
 // copy of the 512-byte bitmap, a bulk copy of the value run (16-byte padded,
 // its length from the offset array) and a 2-D TMA load of the 64-column
 // activation tile for the token block (128-byte swizzle), all completing on
@@ -52,7 +53,7 @@ constexpr int kGroups = 2;                      // warp groups, each on its own 
 constexpr int kGroupWarps = 4;                  // one 16-row strip of the tile each
 constexpr int kWarps = kGroups * kGroupWarps;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kStages = 3;                      // per group
+constexpr int kStages = 3;                      // per group, at most (two CTAs an SM)
 constexpr uint32_t kBmBytes = 512;              // 64 words of a 64 x 64 tile
 constexpr uint32_t kRunCap = 64 * 64 * 2;       // a full tile of fp16 values
 constexpr uint32_t kStripBytes = 16 * 128;      // 16 rows x 64 fp16
@@ -90,16 +91,20 @@ US_DEV void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint
         : "memory");
 }
 
-size_t dec_smem(int nk, int NB) {
+// three CTAs an SM (grids of more than one wave at two) keep two stages a group
+__host__ __device__ constexpr int stages_for(int minb) { return minb >= 3 ? 2 : kStages; }
+
+size_t dec_smem(int nk, int NB, int stages = kStages) {
     const uint32_t stage = ((uint32_t)(8 * NB) * 128u + kBmBytes + kRunCap + 1023u) & ~1023u;
     const size_t offs = (((size_t)nk + 1) * 4 + 1023) & ~(size_t)1023;
-    return 1024 + kHeader + offs + (size_t)kGroups * kStages * stage + (size_t)kWarps * kStripBytes;
+    return 1024 + kHeader + offs + (size_t)kGroups * stages * stage + (size_t)kWarps * kStripBytes;
 }
 
-template <int NB>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int NB, int MINB>
+__global__ void __launch_bounds__(kThreads, MINB)
 spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap) {
     using S = DecShape<NB>;
+    constexpr int kSt = stages_for(MINB);              // stages a group
     constexpr int TB = S::kTB;
     extern __shared__ uint8_t smem_raw[];
     // the swizzled TMA destinations want 1024-byte alignment
@@ -117,15 +122,15 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
     uint32_t* offs = reinterpret_cast<uint32_t*>(smem + kHeader);
     const uint32_t offs_bytes = ((uint32_t)(nk + 1) * 4u + 1023u) & ~1023u;
     uint8_t* stages = smem + kHeader + offs_bytes;
-    uint8_t* strip_g = stages + kGroups * kStages * S::kStage + warp * kStripBytes;
+    uint8_t* strip_g = stages + kGroups * kSt * S::kStage + warp * kStripBytes;
     const uint32_t strip = us::smem_addr(strip_g);
 
     const bool early = (p.flags & US_BITMAP_STATIC) != 0;   // weights may be fetched before the wait
     if (!early) us::pdl_wait();
     for (int q = threadIdx.x; q <= nk; q += kThreads) offs[q] = p.tile_off[tile0 + q];
-    if (threadIdx.x < kGroups * kStages) {
-        us::mbar_init(&h.full[threadIdx.x / kStages][threadIdx.x % kStages], 1);
-        us::mbar_init(&h.empty[threadIdx.x / kStages][threadIdx.x % kStages], kGroupWarps);
+    if (threadIdx.x < kGroups * kSt) {
+        us::mbar_init(&h.full[threadIdx.x / kSt][threadIdx.x % kSt], 1);
+        us::mbar_init(&h.empty[threadIdx.x / kSt][threadIdx.x % kSt], kGroupWarps);
     }
     us::fence_mbar_init();
     __syncthreads();
@@ -133,13 +138,13 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
 
     // the group's tiles: q = grp + kGroups * r, r = 0 .. nr - 1
     const int nr = nk > grp ? (nk - grp + kGroups - 1) / kGroups : 0;
-    uint8_t* gstages = stages + grp * kStages * S::kStage;
+    uint8_t* gstages = stages + grp * kSt * S::kStage;
     const bool issuer = sw == 0 && lane == 0;
 
     // a stage's three copies complete on its full barrier: the weights
     // (bitmap, value run; the barrier expects all three) and the activations
     auto issue_w = [&](int r) {          // the group's issuing lane only
-        const int st = r % kStages;
+        const int st = r % kSt;
         const int q = grp + kGroups * r;
         uint8_t* sp = gstages + st * S::kStage;
         const uint32_t o0 = offs[q], o1 = offs[q + 1];
@@ -153,16 +158,16 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
         if (len) us::bulk_g2s(sp + S::kXBytes + kBmBytes, p.values + (uint64_t)o0 * 2u, len * 2u, &h.full[grp][st]);
     };
     auto issue_x = [&](int r) {
-        const int st = r % kStages;
+        const int st = r % kSt;
         const int q = grp + kGroups * r;
         tma_load_2d(us::smem_addr(gstages + st * S::kStage), &xmap, (kt0 + q) * 64, tb * TB, &h.full[grp][st]);
     };
     if (issuer)
-        for (int r = 0; r < nr && r < kStages; ++r) issue_w(r);
+        for (int r = 0; r < nr && r < kSt; ++r) issue_w(r);
     // everything below reads the activations or writes global memory
     if (early) us::pdl_wait();
     if (issuer)
-        for (int r = 0; r < nr && r < kStages; ++r) issue_x(r);
+        for (int r = 0; r < nr && r < kSt; ++r) issue_x(r);
 
     float acc[NB][4];
 #pragma unroll
@@ -175,13 +180,13 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
     const uint64_t below = (1ull << (4 * c4)) - 1ull;
     bool failed = false;
     for (int r = 0; r < nr; ++r) {
-        const int st = r % kStages;
-        const uint32_t ph = (uint32_t)(r / kStages) & 1u;
+        const int st = r % kSt;
+        const uint32_t ph = (uint32_t)(r / kSt) & 1u;
         uint8_t* sp = gstages + st * S::kStage;
         if (!__all_sync(0xffffffffu, us::mbar_wait(&h.full[grp][st], ph, p.status))) {
             // give each copy that may still be in flight one more bounded wait, then stop
-            for (int r2 = r + 1; r2 < nr && r2 < r + kStages; ++r2)
-                us::mbar_wait(&h.full[grp][r2 % kStages], (uint32_t)(r2 / kStages) & 1u, nullptr);
+            for (int r2 = r + 1; r2 < nr && r2 < r + kSt; ++r2)
+                us::mbar_wait(&h.full[grp][r2 % kSt], (uint32_t)(r2 / kSt) & 1u, nullptr);
             failed = true;
             break;
         }
@@ -258,10 +263,10 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
         //    once all four warps of the group are
         __syncwarp();
         if (lane == 0) us::mbar_arrive(&h.empty[grp][st]);
-        if (issuer && r + kStages < nr) {
+        if (issuer && r + kSt < nr) {
             if (us::mbar_wait(&h.empty[grp][st], ph, p.status)) {
-                issue_w(r + kStages);
-                issue_x(r + kStages);
+                issue_w(r + kSt);
+                issue_x(r + kSt);
             }
         }
         __syncwarp();                           // reconverge before the warp-wide ldmatrix / mma
@@ -330,7 +335,7 @@ spmm_f16_dec_kernel(const UsKParams p, const __grid_constant__ CUtensorMap xmap)
     }
 }
 
-template <int NB>
+template <int NB, int MINB>
 us_status launch_nb(const UsKParams& p, cudaStream_t st) {
     auto enc = us::tensor_map_encoder();
     if (!enc) return US_ERR_CUDA;
@@ -345,9 +350,9 @@ us_status launch_nb(const UsKParams& p, cudaStream_t st) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return US_ERR_CUDA;
     const int nk = (p.nTK + p.split - 1) / p.split;
-    const size_t smem = dec_smem(nk, NB);
+    const size_t smem = dec_smem(nk, NB, stages_for(MINB));
     if (smem > 227 * 1024) return US_ERR_UNSUPPORTED;
-    auto kern = spmm_f16_dec_kernel<NB>;
+    auto kern = spmm_f16_dec_kernel<NB, MINB>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return US_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -392,10 +397,18 @@ int f16_dec_split(int nTM, int nTK, int N) {
 }
 
 us_status launch_f16_dec(const UsKParams& p, cudaStream_t st) {
+    // a grid of more than one wave at two CTAs an SM runs three an SM with two
+    // stages a group (measured: 11008 x 4096, N = 1 / 16: 39.6 / 45.7 ->
+    // 34.9 / 42.0 us); a smaller grid keeps the deeper ring (4096 x 4096, N =
+    // 1: 17.1 us with it, 21.2 without)
+    const int ntb = (p.N + p.tok_block - 1) / p.tok_block;
+    const int nk = (p.nTK + p.split - 1) / p.split;
+    const bool three = p.tok_block <= 16 && (int64_t)p.nTM * p.split * ntb > 2 * num_sms() &&
+                       3 * (dec_smem(nk, p.tok_block / 8, stages_for(3)) + 1024) <= 228 * 1024;
     switch (p.tok_block) {
-        case 8: return launch_nb<1>(p, st);
-        case 16: return launch_nb<2>(p, st);
-        case 32: return launch_nb<4>(p, st);
+        case 8: return three ? launch_nb<1, 3>(p, st) : launch_nb<1, 2>(p, st);
+        case 16: return three ? launch_nb<2, 3>(p, st) : launch_nb<2, 2>(p, st);
+        case 32: return launch_nb<4, 2>(p, st);
     }
     return US_ERR_INVALID_ARG;
 }

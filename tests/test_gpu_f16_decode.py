@@ -105,14 +105,17 @@ def test_f16_decode_empty_matrix(us):
     assert not np.any(y.view(np.uint16))
 
 
-def test_f16_decode_ffn_shape_sampled(us, orc):
-    """11008 x 4096, 50 % sparse, 8 tokens, in the launch shape the library
-    picks: 20000 sampled outputs against the oracle."""
+@pytest.mark.parametrize("N", [8, 12])
+def test_f16_decode_ffn_shape_sampled(us, orc, N):
+    """11008 x 4096, 50 % sparse, 8 and 12 tokens (8- and 16-token blocks), in
+    the launch shape the library picks: 688 CTAs, more than one wave at two an
+    SM, so three an SM with two stages a group.  20000 sampled outputs against
+    the oracle."""
     rng = np.random.default_rng(7)
     W = rand_f16(rng, 11008, 4096, 0.5)
-    X = rng.standard_normal((8, 4096)).astype(np.float16)
+    X = rng.standard_normal((N, 4096)).astype(np.float16)
     y = run(us, encode(us, W), X)
-    n = rng.integers(0, 8, 20000)
+    n = rng.integers(0, N, 20000)
     m = rng.integers(0, 11008, 20000)
     _, exact = orc.spmm_f16_at(W, X, n.astype(np.int32), m.astype(np.int32))
     check(y[n, m], exact, "fp16 decode 11008 x 4096")
