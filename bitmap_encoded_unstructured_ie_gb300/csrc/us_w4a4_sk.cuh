@@ -798,20 +798,18 @@ w4a4_sk_kernel(const UsKParams p) {
                         bf[nt][4 * hh + 3] = h.w;
                     }
                 }
-                uint4 av[4];
+                // one 16-row block at a time: its 16 bytes are loaded just before
+                // they are converted, which keeps three blocks' words out of the
+                // registers (4096 x 4096, N = 16: 7.50 -> 7.34 us)
 #pragma unroll
                 for (int mb = 0; mb < 4; ++mb) {
                     const int sg = mb * 32 + lane;
-                    av[mb] = *reinterpret_cast<const uint4*>(src + (sg ^ ((sg >> 3) & 3)) * 16);
-                }
-                __syncwarp();                                 // the slot may be refilled next
-#pragma unroll
-                for (int mb = 0; mb < 4; ++mb) {
+                    const uint4 av = *reinterpret_cast<const uint4*>(src + (sg ^ ((sg >> 3) & 3)) * 16);
                     uint32_t af[2][8];                        // rows g, g + 8: position pairs 0..7
-                    cvt(av[mb].x, &af[0][0]);
-                    cvt(av[mb].y, &af[0][4]);
-                    cvt(av[mb].z, &af[1][0]);
-                    cvt(av[mb].w, &af[1][4]);
+                    cvt(av.x, &af[0][0]);
+                    cvt(av.y, &af[0][4]);
+                    cvt(av.z, &af[1][0]);
+                    cvt(av.w, &af[1][4]);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
@@ -819,6 +817,7 @@ w4a4_sk_kernel(const UsKParams p) {
                             us::mma_m16n8k16_f16(acc[mb][nt], af[0][2 * kk], af[1][2 * kk], af[0][2 * kk + 1],
                                                  af[1][2 * kk + 1], bf[nt][2 * kk], bf[nt][2 * kk + 1]);
                 }
+                __syncwarp();                                 // the slot may be refilled next
             }
             flush();
         }
